@@ -1,0 +1,218 @@
+"""CPU oracle for exact Gumbel-max token sampling fused with the LM-head projection.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s
+CPU-baseline / reference leg may import this package.  It shares no code with the CUDA library
+in ``lm_head_gumbel_lmhead_gb300`` and never imports it.
+
+The arithmetic lives in ``lms_oracle.c`` (plain C, fp64, compiled with gcc on first use); this
+module only marshals numpy arrays.  Each function cites the page passage it follows; the
+readings taken where the pages are silent are listed in ``lms_oracle.c``'s header.
+
+Every function here has a pin in ``tests/test_oracle_*.py`` (Philox against Triton's own
+Philox run in its CPU interpreter, the noise ranges the Megatron-LM PR prints, the tail-rate
+closed form, chi-square against softmax, brute force over tile widths, fp64 GEMM against
+numpy's matmul, greedy against numpy's argmax).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "lms_oracle.c")
+_LIB_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_LIB_DIR, "liblms_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+FP32_NOISE = 0
+WIDE53_NOISE = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no CUDA).  Returns the shared-library path."""
+    os.makedirs(_LIB_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+               _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i64, u64, i32 = ctypes.c_int64, ctypes.c_uint64, ctypes.c_int
+            lib.orc_philox4x32_many.argtypes = [i64, P, P, i32, P]
+            lib.orc_noise_fill.argtypes = [i64, i64, P, P, u64, u64, i32, P, P, P, P]
+            lib.orc_sample_from_logits.argtypes = [P, i64, i64, i64, P, P, P, P, i64, P, i64, u64,
+                                                   u64, i32, i64, P, P, P, P, P, P, P, i32]
+            lib.orc_lmhead_logits.argtypes = [P, i64, P, i64, i64, i64, i64, P, i32]
+            lib.orc_lmhead_sample.argtypes = [P, i64, P, i64, i64, i64, i64, P, P, P, P, i64, P,
+                                              i64, u64, u64, i32, i64, P, P, P, P, P, P, P, i32]
+            lib.orc_lmhead_sample.restype = ctypes.c_int
+            lib.orc_lmhead_scores_at.argtypes = [P, i64, P, i64, i64, i64, i64, P, P, P, P, i64,
+                                                 P, i64, u64, u64, i32, i64, P, P, P]
+            lib.orc_uniform.argtypes = [ctypes.c_uint32, ctypes.c_uint32, i32]
+            lib.orc_uniform.restype = ctypes.c_double
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+def default_threads() -> int:
+    return max(1, min(64, os.cpu_count() or 1))
+
+
+def philox4x32(ctr, key, rounds: int = 10) -> np.ndarray:
+    """Philox4x32-R (Salmon et al., SC'11) on arrays ctr [n,4] and key [n,2] (uint32)."""
+    ctr = _c(np.asarray(ctr).reshape(-1, 4), np.uint32)
+    key = _c(np.asarray(key).reshape(-1, 2), np.uint32)
+    assert ctr.shape[0] == key.shape[0]
+    out = np.empty_like(ctr)
+    _load().orc_philox4x32_many(ctr.shape[0], _ptr(ctr), _ptr(key), rounds, _ptr(out))
+    return out
+
+
+def uniform(w0: int, w1: int, wide: bool) -> float:
+    """The midpoint uniform (k + 1/2) / 2^m from one (fp32 noise) or two (wide) Philox words."""
+    return _load().orc_uniform(int(w0) & 0xFFFFFFFF, int(w1) & 0xFFFFFFFF, int(bool(wide)))
+
+
+def noise(B, V, seeds, positions, base_seed, offset, wide):
+    """Noise grid [B, V]: Philox words [B,V,4], u, E = -log u, g = -log E (fp64).
+
+    Keyed by (request seed, absolute position, vocabulary index) for seeded rows, as in the
+    Megatron-LM PR ("The change"); unseeded rows by (base_seed, offset, row)."""
+    seeds = _c(seeds, np.int64)
+    positions = _c(positions, np.int64)
+    words = np.empty((B, V, 4), np.uint32)
+    u = np.empty((B, V)); E = np.empty((B, V)); g = np.empty((B, V))
+    _load().orc_noise_fill(B, V, _ptr(seeds), _ptr(positions), base_seed, offset, int(bool(wide)),
+                           _ptr(words), _ptr(u), _ptr(E), _ptr(g))
+    return words, u, E, g
+
+
+class RowResult:
+    """Per-row outcome of the race: index (-1 if none), status, top-two scores, tile maxima."""
+
+    def __init__(self, out, status, top1, top2, tile_max, tile_idx, scores):
+        self.out, self.status, self.top1, self.top2 = out, status, top1, top2
+        self.tile_max, self.tile_idx, self.scores = tile_max, tile_idx, scores
+
+
+def _row_outputs(B, V, tile_v, want_scores):
+    nt = (V + tile_v - 1) // tile_v if tile_v else 0
+    return (np.empty(B, np.int64), np.empty(B, np.int32), np.empty(B), np.empty(B),
+            np.empty((B, nt)), np.empty((B, nt), np.int64),
+            np.empty((B, V)) if want_scores else None)
+
+
+def sample_from_logits(logits, *, B=None, temperature=None, seeds=None, positions=None, bias=None,
+                       mask=None, base_seed=0, offset=0, wide=False, tile_v=0,
+                       want_scores=False, threads=None) -> RowResult:
+    """Gumbel-max race over materialised logits [B, V] (or one broadcast row [V] with B given).
+
+    FlashSampling "method step details" steps 2-6 and Stage 2, with the transform order of the
+    sampling-kernel guide (bias before temperature; T == 0 greedy)."""
+    y = np.asarray(logits, dtype=np.float64)
+    if y.ndim == 1:
+        assert B is not None
+        ld_y, V = 0, y.shape[0]
+    else:
+        B = y.shape[0] if B is None else B
+        ld_y, V = y.shape[1], y.shape[1]
+    y = np.ascontiguousarray(y)
+    T = _c(temperature, np.float64)
+    bias_a = _c(bias, np.float64)
+    ld_bias = 0 if bias_a is None or bias_a.ndim == 1 else bias_a.shape[1]
+    mask_a = _c(mask, np.uint32)
+    ld_mask = 0 if mask_a is None or mask_a.ndim == 1 else mask_a.shape[1]
+    seeds_a, pos_a = _c(seeds, np.int64), _c(positions, np.int64)
+    outs = _row_outputs(B, V, tile_v, want_scores)
+    _load().orc_sample_from_logits(
+        _ptr(y), ld_y, B, V, _ptr(T), _ptr(seeds_a), _ptr(pos_a), _ptr(bias_a), ld_bias,
+        _ptr(mask_a), ld_mask, base_seed, offset, int(bool(wide)), tile_v,
+        *[_ptr(o) for o in outs], threads or default_threads())
+    return RowResult(*outs)
+
+
+def _bits16(t):
+    """bf16 bit patterns as uint16 from a torch bf16 tensor or a uint16/int16 array."""
+    if hasattr(t, "view") and hasattr(t, "dtype") and str(t.dtype) == "torch.bfloat16":
+        import torch
+        t = t.detach().cpu().contiguous().view(torch.int16).numpy()
+    a = np.asarray(t)
+    if a.dtype != np.uint16:
+        a = a.view(np.uint16)
+    return np.ascontiguousarray(a)
+
+
+def lmhead_logits(H_bits, W_bits, threads=None) -> np.ndarray:
+    """Y = H W^T in fp64 from bf16 bit patterns H [B, D], W [V, D] (FlashSampling step 1)."""
+    H, W = _bits16(H_bits), _bits16(W_bits)
+    B, D = H.shape
+    V = W.shape[0]
+    y = np.empty((B, V))
+    _load().orc_lmhead_logits(_ptr(H), D, _ptr(W), D, B, D, V, _ptr(y), threads or default_threads())
+    return y
+
+
+def lmhead_sample(H_bits, W_bits, *, temperature=None, seeds=None, positions=None, bias=None,
+                  mask=None, base_seed=0, offset=0, wide=False, tile_v=128, want_scores=False,
+                  threads=None) -> RowResult:
+    """The fused path's result: fp64 logits from bf16 H, W, then the per-row race."""
+    H, W = _bits16(H_bits), _bits16(W_bits)
+    B, D = H.shape
+    V = W.shape[0]
+    T = _c(temperature, np.float64)
+    bias_a = _c(bias, np.float64)
+    ld_bias = 0 if bias_a is None or bias_a.ndim == 1 else bias_a.shape[1]
+    mask_a = _c(mask, np.uint32)
+    ld_mask = 0 if mask_a is None or mask_a.ndim == 1 else mask_a.shape[1]
+    seeds_a, pos_a = _c(seeds, np.int64), _c(positions, np.int64)
+    outs = _row_outputs(B, V, tile_v, want_scores)
+    rc = _load().orc_lmhead_sample(
+        _ptr(H), D, _ptr(W), D, B, D, V, _ptr(T), _ptr(seeds_a), _ptr(pos_a), _ptr(bias_a),
+        ld_bias, _ptr(mask_a), ld_mask, base_seed, offset, int(bool(wide)), tile_v,
+        *[_ptr(o) for o in outs], threads or default_threads())
+    if rc != 0:
+        raise MemoryError("oracle could not allocate the fp64 logits")
+    return RowResult(*outs)
+
+
+def lmhead_scores_at(H_bits, W_bits, rows, cols, *, temperature=None, seeds=None, positions=None,
+                     bias=None, mask=None, base_seed=0, offset=0, wide=False) -> np.ndarray:
+    """Perturbed scores s[b, v] of the fused path at chosen (b, v) pairs, one by one."""
+    H, W = _bits16(H_bits), _bits16(W_bits)
+    B, D = H.shape
+    V = W.shape[0]
+    rows = _c(rows, np.int64); cols = _c(cols, np.int64)
+    T = _c(temperature, np.float64)
+    bias_a = _c(bias, np.float64)
+    ld_bias = 0 if bias_a is None or bias_a.ndim == 1 else bias_a.shape[1]
+    mask_a = _c(mask, np.uint32)
+    ld_mask = 0 if mask_a is None or mask_a.ndim == 1 else mask_a.shape[1]
+    seeds_a, pos_a = _c(seeds, np.int64), _c(positions, np.int64)
+    s = np.empty(rows.shape[0])
+    _load().orc_lmhead_scores_at(
+        _ptr(H), D, _ptr(W), D, B, D, V, _ptr(T), _ptr(seeds_a), _ptr(pos_a), _ptr(bias_a),
+        ld_bias, _ptr(mask_a), ld_mask, base_seed, offset, int(bool(wide)), rows.shape[0],
+        _ptr(rows), _ptr(cols), _ptr(s))
+    return s

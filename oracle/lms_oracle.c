@@ -1,0 +1,356 @@
+/*
+ * CPU oracle for exact Gumbel-max token sampling fused with the LM-head projection.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's CPU-baseline /
+ * reference leg may load this library.  The product path (the CUDA library) never calls it, and
+ * the two share no code: no header, helper, table or constant generator.
+ *
+ * Everything is plain, slow and in fp64, written so that each step can be checked by eye
+ * against the pages it follows:
+ *
+ *   [MLM]  "Megatron-LM pull request 8370: fp64_sampling_noise" -- sections "Problem" (the
+ *          exponential race argmax(p/E), E = -log U; the tail-rate closed form) and
+ *          "The change" (seeded noise keyed by (request seed, absolute position, vocabulary
+ *          index); two Philox words forming the 52-bit midpoint uniform (k + 1/2)/2^52).
+ *   [FS]   "FlashSampling: fast and memory-efficient exact sampling" (summary page of
+ *          arXiv 2603.15854) -- "Gumbel-Max trick" (i* = argmax_i e_i + g_i), "core method"
+ *          and "method step details" (Stage 1 steps 1-6 per vocab tile, Stage 2 argmax over
+ *          tile maxima; g = -log(-log u)).
+ *   [SDO]  "spec-decode-ops" kernels card -- "Randomness is counter-based Philox".
+ *   [SK]   "Write Triton Sampling Kernel" -- reasoning steps 3-4 (greedy short-circuit at T == 0
+ *          with smallest-index tie-break; bias added before division by T), "Kernel design
+ *          rules" (out-of-range / masked entries are -inf).
+ *   [P123] Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11:
+ *          the Philox4x32 round function, its multipliers and the Weyl key schedule.
+ *
+ * Readings where the pages leave a step open (each is also listed with the design notes):
+ *   - Philox variant: Philox4x32 with 10 rounds (the pages say "Philox" and "two words ... the
+ *     other three", i.e. four 32-bit words per call).
+ *   - Key and counter: seeded row  -> key = (seed lo, seed hi), counter = (v, pos lo, pos hi, 0);
+ *                      unseeded row -> key = (base_seed lo, base_seed hi),
+ *                                      counter = (v, offset lo, offset hi, 0x80000000 | b).
+ *   - fp32 noise uses word 0: k = w0 >> 8 (24 bits), u = (k + 1/2) / 2^24.
+ *     wide noise uses words 0 and 1: k = ((w1 << 32) | w0) >> 12 (52 bits), u = (k + 1/2) / 2^52.
+ *     Both u are exact in fp64.  E = -log(u), g = -log(E).
+ *   - Transform: masked -> -inf; T == 0 -> greedy, s = y + bias (no noise); otherwise
+ *     s = (y + bias) / T + g.  T < 0 or NaN -> the row is invalid (status 2, index -1).
+ *     A NaN score counts as -inf.
+ *   - Argmax: largest s; ties go to the smallest vocabulary index; -inf never wins; a row with
+ *     no finite-or-+inf score gives index -1 and status 1.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------------------------ */
+/* Philox4x32-10 [P123]                                                                        */
+/* ------------------------------------------------------------------------------------------ */
+
+/* Round multipliers and Weyl key increments as published in [P123] (Table / section 5:
+ * M0, M1 for Philox4x32; W0 = golden ratio, W1 = sqrt(3) - 1, both scaled to 32 bits). */
+#define ORC_PHILOX_M0 0xD2511F53u
+#define ORC_PHILOX_M1 0xCD9E8D57u
+#define ORC_PHILOX_W0 0x9E3779B9u
+#define ORC_PHILOX_W1 0xBB67AE85u
+
+/* One Philox4x32 round: two 32x32->64 products, the high halves mixed with the other words and
+ * the round key, the low halves carried over (the S-box / permutation of [P123]). */
+static void orc_philox_round(uint32_t x[4], const uint32_t k[2]) {
+    uint64_t p0 = (uint64_t)ORC_PHILOX_M0 * (uint64_t)x[0];
+    uint64_t p1 = (uint64_t)ORC_PHILOX_M1 * (uint64_t)x[2];
+    uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+    uint32_t y0 = hi1 ^ x[1] ^ k[0];
+    uint32_t y1 = lo1;
+    uint32_t y2 = hi0 ^ x[3] ^ k[1];
+    uint32_t y3 = lo0;
+    x[0] = y0; x[1] = y1; x[2] = y2; x[3] = y3;
+}
+
+/* Philox4x32 with R rounds: the first round uses the key as given, each later round the key
+ * bumped once more by (W0, W1). */
+void orc_philox4x32(const uint32_t ctr[4], const uint32_t key[2], int rounds, uint32_t out[4]) {
+    uint32_t x[4] = {ctr[0], ctr[1], ctr[2], ctr[3]};
+    uint32_t k[2] = {key[0], key[1]};
+    for (int r = 0; r < rounds; ++r) {
+        if (r > 0) {
+            k[0] += ORC_PHILOX_W0;
+            k[1] += ORC_PHILOX_W1;
+        }
+        orc_philox_round(x, k);
+    }
+    out[0] = x[0]; out[1] = x[1]; out[2] = x[2]; out[3] = x[3];
+}
+
+/* Batched form for tests: n calls, ctr [n][4], key [n][2], out [n][4]. */
+void orc_philox4x32_many(int64_t n, const uint32_t* ctr, const uint32_t* key, int rounds,
+                         uint32_t* out) {
+    for (int64_t i = 0; i < n; ++i) orc_philox4x32(ctr + 4 * i, key + 2 * i, rounds, out + 4 * i);
+}
+
+/* (request seed, absolute position, vocabulary index) -> (key, counter) [MLM "The change"];
+ * unseeded rows are keyed by (base_seed, offset, row) instead [SDO "Randomness"]. */
+void orc_key_counter(int seeded, int64_t seed, int64_t pos, uint64_t base_seed, uint64_t offset,
+                     int64_t row, uint32_t v, uint32_t ctr[4], uint32_t key[2]) {
+    if (seeded) {
+        uint64_t s = (uint64_t)seed, p = (uint64_t)pos;
+        key[0] = (uint32_t)s; key[1] = (uint32_t)(s >> 32);
+        ctr[0] = v; ctr[1] = (uint32_t)p; ctr[2] = (uint32_t)(p >> 32); ctr[3] = 0u;
+    } else {
+        key[0] = (uint32_t)base_seed; key[1] = (uint32_t)(base_seed >> 32);
+        ctr[0] = v; ctr[1] = (uint32_t)offset; ctr[2] = (uint32_t)(offset >> 32);
+        ctr[3] = 0x80000000u | (uint32_t)row;
+    }
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Uniform and noise [MLM "Problem", "The change"; FS step 3]                                  */
+/* ------------------------------------------------------------------------------------------ */
+
+/* The midpoint uniform: u = (k + 1/2) / 2^m, exact in fp64 (m = 24 or 52). */
+double orc_uniform(uint32_t w0, uint32_t w1, int wide) {
+    if (wide) {
+        uint64_t k = ((((uint64_t)w1) << 32) | (uint64_t)w0) >> 12;
+        return ldexp((double)k + 0.5, -52);
+    } else {
+        uint32_t k = w0 >> 8;
+        return ldexp((double)k + 0.5, -24);
+    }
+}
+
+/* Exponential variate E = -log U and Gumbel variate g = -log E = -log(-log U). */
+double orc_exponential(double u) { return -log(u); }
+double orc_gumbel(double u) { return -log(-log(u)); }
+
+static int row_is_seeded(const int64_t* seeds, int64_t b) { return seeds != NULL && seeds[b] >= 0; }
+
+/* Noise for a [B][V] grid, any of the outputs may be NULL:
+ *   words [B][V][4] uint32, u [B][V], E [B][V], g [B][V] (fp64). */
+void orc_noise_fill(int64_t B, int64_t V, const int64_t* seeds, const int64_t* positions,
+                    uint64_t base_seed, uint64_t offset, int wide, uint32_t* words, double* u,
+                    double* E, double* g) {
+    for (int64_t b = 0; b < B; ++b) {
+        int seeded = row_is_seeded(seeds, b);
+        int64_t seed = seeded ? seeds[b] : 0, pos = seeded ? positions[b] : 0;
+        for (int64_t v = 0; v < V; ++v) {
+            uint32_t ctr[4], key[2], w[4];
+            orc_key_counter(seeded, seed, pos, base_seed, offset, b, (uint32_t)v, ctr, key);
+            orc_philox4x32(ctr, key, 10, w);
+            int64_t i = b * V + v;
+            if (words) memcpy(words + 4 * i, w, sizeof w);
+            double uu = orc_uniform(w[0], w[1], wide);
+            if (u) u[i] = uu;
+            if (E) E[i] = orc_exponential(uu);
+            if (g) g[i] = orc_gumbel(uu);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Per-row race: transform, perturb, argmax, per-tile maxima [FS steps 2-6, Stage 2; SK]        */
+/* ------------------------------------------------------------------------------------------ */
+
+typedef struct {
+    /* logits: either y [B][ld_y] (fp64; ld_y == 0 broadcasts one row) or computed on the fly */
+    const double* y; int64_t ld_y;
+    int64_t B, V;
+    const double* T;              /* [B] or NULL (all 1) */
+    const int64_t* seeds;         /* [B] or NULL (all unseeded); seed < 0 -> unseeded row */
+    const int64_t* positions;     /* [B] (read for seeded rows) */
+    const double* bias; int64_t ld_bias;    /* [B][ld_bias] or NULL; ld_bias == 0 broadcasts */
+    const uint32_t* mask; int64_t ld_mask;  /* [B][ld_mask] allow bits or NULL; 0 broadcasts */
+    uint64_t base_seed, offset;
+    int wide;
+    int64_t tile_v;               /* > 0: also report per-tile maxima */
+    /* outputs */
+    int64_t* out; int32_t* status; double* top1; double* top2;
+    double* tile_max; int64_t* tile_idx;   /* [B][n_tiles] when tile_v > 0 */
+    double* scores;                /* optional [B][V] perturbed scores */
+} orc_rows_args;
+
+/* Perturbed score s for row b, column v, given the (untransformed) logit y. */
+static double orc_score(const orc_rows_args* a, int64_t b, int64_t v, double y) {
+    if (a->mask) {
+        uint32_t word = a->mask[b * a->ld_mask + (v >> 5)];
+        if (((word >> (v & 31)) & 1u) == 0u) return -INFINITY;
+    }
+    double T = a->T ? a->T[b] : 1.0;
+    double bias = a->bias ? a->bias[b * a->ld_bias + v] : 0.0;
+    double t = y + bias;                       /* bias before temperature [SK step 4] */
+    double s;
+    if (T == 0.0) {
+        s = t;                                 /* greedy: no noise [SK step 3] */
+    } else {
+        int seeded = row_is_seeded(a->seeds, b);
+        uint32_t ctr[4], key[2], w[4];
+        orc_key_counter(seeded, seeded ? a->seeds[b] : 0, seeded ? a->positions[b] : 0,
+                        a->base_seed, a->offset, b, (uint32_t)v, ctr, key);
+        orc_philox4x32(ctr, key, 10, w);
+        s = t / T + orc_gumbel(orc_uniform(w[0], w[1], a->wide));
+    }
+    if (isnan(s)) s = -INFINITY;
+    return s;
+}
+
+static void orc_one_row(const orc_rows_args* a, int64_t b, const double* yrow) {
+    int64_t V = a->V;
+    double T = a->T ? a->T[b] : 1.0;
+    int64_t nt = a->tile_v > 0 ? (V + a->tile_v - 1) / a->tile_v : 0;
+    if (isnan(T) || T < 0.0) {                 /* invalid temperature: rejected per row */
+        a->out[b] = -1; a->status[b] = 2;
+        if (a->top1) a->top1[b] = -INFINITY;
+        if (a->top2) a->top2[b] = -INFINITY;
+        for (int64_t t = 0; t < nt; ++t) { a->tile_max[b * nt + t] = -INFINITY; a->tile_idx[b * nt + t] = -1; }
+        if (a->scores) for (int64_t v = 0; v < V; ++v) a->scores[b * V + v] = -INFINITY;
+        return;
+    }
+    double best = -INFINITY, second = -INFINITY;
+    int64_t arg = -1;
+    for (int64_t t = 0; t < nt; ++t) { a->tile_max[b * nt + t] = -INFINITY; a->tile_idx[b * nt + t] = -1; }
+    for (int64_t v = 0; v < V; ++v) {
+        double s = orc_score(a, b, v, yrow[v]);
+        if (a->scores) a->scores[b * V + v] = s;
+        if (s > -INFINITY) {
+            if (arg < 0 || s > best) {         /* strict '>' keeps the smallest index on ties */
+                second = best; best = s; arg = v;
+            } else if (s > second) {
+                second = s;
+            }
+            if (nt > 0) {
+                int64_t t = v / a->tile_v;
+                if (a->tile_idx[b * nt + t] < 0 || s > a->tile_max[b * nt + t]) {
+                    a->tile_max[b * nt + t] = s; a->tile_idx[b * nt + t] = v;
+                }
+            }
+        }
+    }
+    a->out[b] = arg;
+    a->status[b] = arg < 0 ? 1 : 0;
+    if (a->top1) a->top1[b] = best;
+    if (a->top2) a->top2[b] = second;
+}
+
+typedef struct { const orc_rows_args* a; int64_t b0, b1; } orc_rows_job;
+
+static void* orc_rows_worker(void* p) {
+    const orc_rows_job* j = (const orc_rows_job*)p;
+    for (int64_t b = j->b0; b < j->b1; ++b) orc_one_row(j->a, b, j->a->y + b * j->a->ld_y);
+    return NULL;
+}
+
+static void orc_run_rows(const orc_rows_args* a, int nthreads) {
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > a->B) nthreads = (int)(a->B > 0 ? a->B : 1);
+    pthread_t th[256];
+    orc_rows_job jobs[256];
+    if (nthreads > 256) nthreads = 256;
+    for (int i = 0; i < nthreads; ++i) {
+        jobs[i].a = a;
+        jobs[i].b0 = a->B * i / nthreads;
+        jobs[i].b1 = a->B * (i + 1) / nthreads;
+        pthread_create(&th[i], NULL, orc_rows_worker, &jobs[i]);
+    }
+    for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+}
+
+/* Gumbel race over materialised logits (the second entry point): y [B][ld_y] in fp64. */
+void orc_sample_from_logits(const double* y, int64_t ld_y, int64_t B, int64_t V, const double* T,
+                            const int64_t* seeds, const int64_t* positions, const double* bias,
+                            int64_t ld_bias, const uint32_t* mask, int64_t ld_mask,
+                            uint64_t base_seed, uint64_t offset, int wide, int64_t tile_v,
+                            int64_t* out, int32_t* status, double* top1, double* top2,
+                            double* tile_max, int64_t* tile_idx, double* scores, int nthreads) {
+    orc_rows_args a = {y, ld_y, B, V, T, seeds, positions, bias, ld_bias, mask, ld_mask,
+                       base_seed, offset, wide, tile_v, out, status, top1, top2,
+                       tile_max, tile_idx, scores};
+    orc_run_rows(&a, nthreads);
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* LM-head logits Y = H W^T in fp64 from bf16 inputs [FS step 1]                              */
+/* ------------------------------------------------------------------------------------------ */
+
+/* bf16 -> fp64: the bf16 bits are the upper half of an fp32; the conversion is exact. */
+static double orc_bf16(uint16_t h) {
+    uint32_t bits = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+typedef struct {
+    const uint16_t* H; int64_t ldh; const uint16_t* W; int64_t ldw;
+    int64_t B, D, V; double* y; int64_t v0, v1;
+} orc_gemm_job;
+
+static void* orc_gemm_worker(void* p) {
+    const orc_gemm_job* j = (const orc_gemm_job*)p;
+    double* hrow = (double*)malloc(sizeof(double) * (size_t)j->D);
+    double* wrow = (double*)malloc(sizeof(double) * (size_t)j->D);
+    for (int64_t v = j->v0; v < j->v1; ++v) {
+        for (int64_t d = 0; d < j->D; ++d) wrow[d] = orc_bf16(j->W[v * j->ldw + d]);
+        for (int64_t b = 0; b < j->B; ++b) {
+            double acc = 0.0;
+            for (int64_t d = 0; d < j->D; ++d) acc += orc_bf16(j->H[b * j->ldh + d]) * wrow[d];
+            j->y[b * j->V + v] = acc;
+        }
+    }
+    free(hrow); free(wrow);
+    return NULL;
+}
+
+/* y [B][V] = sum_d H[b][d] * W[v][d], accumulated in fp64 in increasing d. */
+void orc_lmhead_logits(const uint16_t* H, int64_t ldh, const uint16_t* W, int64_t ldw, int64_t B,
+                       int64_t D, int64_t V, double* y, int nthreads) {
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t th[256];
+    orc_gemm_job jobs[256];
+    for (int i = 0; i < nthreads; ++i) {
+        orc_gemm_job j = {H, ldh, W, ldw, B, D, V, y, V * i / nthreads, V * (i + 1) / nthreads};
+        jobs[i] = j;
+        pthread_create(&th[i], NULL, orc_gemm_worker, &jobs[i]);
+    }
+    for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+}
+
+/* The fused path's result: logits in fp64, then the same per-row race. */
+int orc_lmhead_sample(const uint16_t* H, int64_t ldh, const uint16_t* W, int64_t ldw, int64_t B,
+                      int64_t D, int64_t V, const double* T, const int64_t* seeds,
+                      const int64_t* positions, const double* bias, int64_t ld_bias,
+                      const uint32_t* mask, int64_t ld_mask, uint64_t base_seed, uint64_t offset,
+                      int wide, int64_t tile_v, int64_t* out, int32_t* status, double* top1,
+                      double* top2, double* tile_max, int64_t* tile_idx, double* scores,
+                      int nthreads) {
+    double* y = (double*)malloc(sizeof(double) * (size_t)(B * V));
+    if (!y) return 1;
+    orc_lmhead_logits(H, ldh, W, ldw, B, D, V, y, nthreads);
+    orc_sample_from_logits(y, V, B, V, T, seeds, positions, bias, ld_bias, mask, ld_mask,
+                           base_seed, offset, wide, tile_v, out, status, top1, top2, tile_max,
+                           tile_idx, scores, nthreads);
+    free(y);
+    return 0;
+}
+
+/* Perturbed scores at n chosen (b, v) pairs of the fused path, each computed on its own:
+ * one fp64 dot product, the transform and the noise.  Used where a full-size oracle pass is
+ * too slow (sampled checks) and to score the index another implementation chose. */
+void orc_lmhead_scores_at(const uint16_t* H, int64_t ldh, const uint16_t* W, int64_t ldw,
+                          int64_t B, int64_t D, int64_t V, const double* T, const int64_t* seeds,
+                          const int64_t* positions, const double* bias, int64_t ld_bias,
+                          const uint32_t* mask, int64_t ld_mask, uint64_t base_seed,
+                          uint64_t offset, int wide, int64_t n, const int64_t* bs,
+                          const int64_t* vs, double* s_out) {
+    orc_rows_args a = {NULL, 0, B, V, T, seeds, positions, bias, ld_bias, mask, ld_mask,
+                       base_seed, offset, wide, 0, NULL, NULL, NULL, NULL, NULL, NULL, NULL};
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t b = bs[i], v = vs[i];
+        double Tb = T ? T[b] : 1.0;
+        if (isnan(Tb) || Tb < 0.0) { s_out[i] = -INFINITY; continue; }
+        double acc = 0.0;
+        for (int64_t d = 0; d < D; ++d) acc += orc_bf16(H[b * ldh + d]) * orc_bf16(W[v * ldw + d]);
+        s_out[i] = orc_score(&a, b, v, acc);
+    }
+}
