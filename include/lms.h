@@ -1,0 +1,165 @@
+/*
+ * lms.h -- C ABI of the GB300 (sm_103a) library for exact categorical token sampling fused
+ * into the decode-time LM-head projection, with a Gumbel race over materialised logits and a
+ * counter-based Philox noise generator.
+ *
+ * What the operations compute (sources are web pages, cited by title and section):
+ *
+ *  - "FlashSampling: fast and memory-efficient exact sampling" (summary of arXiv 2603.15854),
+ *    "Gumbel-Max trick": i* = argmax_i (e_i + g_i) with g ~ Gumbel(0,1) is an exact sample of
+ *    softmax(e).  "method step details": Stage 1 computes, per vocabulary tile, the logits
+ *    Y = H W^T on chip (step 1), applies the deterministic transform (step 2), adds
+ *    g = -log(-log u) (steps 3-4), keeps one (max, global index) candidate per row (step 5) and
+ *    writes it to memory (step 6); Stage 2 takes, per row, the candidate of the best tile.
+ *  - "Megatron-LM pull request 8370: fp64_sampling_noise", "Problem" and "The change": noise
+ *    keyed by (request seed, absolute position, vocabulary index); float32 noise loses the tail
+ *    beyond ~20 nats; two Philox words give a 52-bit midpoint uniform (k + 1/2)/2^52 that keeps
+ *    it to ~40 nats.  The same page ("Cost") proposes generating the noise in registers with
+ *    several blocks per row over materialised logits: lms_sample_from_logits.
+ *  - "Write Triton Sampling Kernel", reasoning steps 3-4 and "Kernel design rules": bias is added
+ *    before division by T; T == 0 short-circuits to argmax; ties go to the smallest index;
+ *    masked / out-of-range entries are -inf.
+ *
+ * Exact definitions used by every entry point (identical on all paths):
+ *   key/counter  seeded row b (seeds[b] >= 0): key = (seed lo32, seed hi32),
+ *                counter = (v, pos lo32, pos hi32, 0); unseeded row b: key = (base_seed lo32,
+ *                base_seed hi32), counter = (v, offset lo32, offset hi32, 0x80000000 | b).
+ *   Philox       Philox4x32, 10 rounds (Salmon et al., SC'11); words w0..w3.
+ *   uniform      FP32 noise: k = w0 >> 8, u = (k + 1/2) / 2^24.
+ *                WIDE53 noise: k = ((w1 << 32) | w0) >> 12, u = (k + 1/2) / 2^52.
+ *   noise        E = -log u, g = -log E (computed in fp32 from exact integer-derived u or 1 - u).
+ *   transform    masked -> -inf; T == 0 -> s = y + bias (greedy, no noise);
+ *                T > 0 -> s = (y + bias) / T + g;  NaN scores count as -inf.
+ *   race         per row, the largest s; ties -> smallest v; -inf never wins.
+ *   row status   0 ok; 1 no entry above -inf (index -1); 2 T < 0 or NaN (index -1);
+ *                3 a device-side wait ran out of time (index -1; the call's results for that
+ *                row are void, the CUDA context stays usable).
+ *
+ * Conventions: all data pointers are DEVICE memory owned by the caller; the library never
+ * allocates, frees or retains them.  Calls are asynchronous on `stream` (a cudaStream_t; NULL =
+ * the legacy default stream).  Host-detectable errors return a non-zero lms_status before
+ * anything is launched; lms_last_error() then holds a message (thread-local).  The library keeps
+ * no state between calls.
+ */
+#ifndef LMS_H_
+#define LMS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LMS_OK = 0,
+    LMS_ERR_INVALID_ARG = 1,  /* null required pointer, size <= 0 or too large, bad enum value */
+    LMS_ERR_UNSUPPORTED = 2,  /* alignment / shape the kernels do not handle (see each call)    */
+    LMS_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than lms_workspace_bytes()           */
+    LMS_ERR_CUDA = 4          /* a CUDA runtime / driver call failed (message in last_error)   */
+} lms_status;
+
+typedef enum { LMS_NOISE_FP32 = 0, LMS_NOISE_WIDE53 = 1 } lms_noise_mode;
+typedef enum { LMS_DTYPE_F32 = 0, LMS_DTYPE_BF16 = 1 } lms_dtype;
+typedef enum {
+    LMS_NOISE_OUT_WORDS = 0,      /* uint32 [B][V][4]: the four Philox words                   */
+    LMS_NOISE_OUT_UNIFORM = 1,    /* double [B][V]: u, exact                                    */
+    LMS_NOISE_OUT_EXPONENTIAL = 2,/* float  [B][V]: E = -log u as the sampling kernels compute it */
+    LMS_NOISE_OUT_GUMBEL = 3      /* float  [B][V]: g = -log E as the sampling kernels compute it */
+} lms_noise_kind;
+typedef enum { LMS_OP_LMHEAD = 0, LMS_OP_LOGITS = 1 } lms_op;
+typedef enum {
+    LMS_PATH_AUTO = 0,            /* pick by batch size                                        */
+    LMS_PATH_GEMV = 1,            /* CUDA-core dot products (B <= LMS_GEMV_MAX_B)                */
+    LMS_PATH_TCGEN05 = 2          /* TMA -> shared memory -> tcgen05.mma -> TMEM accumulators  */
+} lms_path;
+
+#define LMS_ROW_OK 0
+#define LMS_ROW_NO_CANDIDATE 1
+#define LMS_ROW_BAD_TEMPERATURE 2
+#define LMS_ROW_DEVICE_TIMEOUT 3
+
+#define LMS_GEMV_MAX_B 8
+#define LMS_FUSED_TILE_V 128
+
+/* Fault injection for tests of the timeout path only (0 in normal use): the fused tcgen05
+ * kernel's first CTA never issues its first shared-memory load, so the wait on it runs out. */
+#define LMS_DEBUG_WITHHOLD_FIRST_LOAD 1u
+
+typedef struct {
+    const float* temperature;   /* [B] or NULL (all 1).  0 = greedy row; < 0 or NaN = status 2 */
+    const int64_t* seeds;       /* [B] or NULL (all unseeded).  seeds[b] < 0 = unseeded row    */
+    const int64_t* positions;   /* [B] absolute position of the token being drawn; read for
+                                   seeded rows (required when seeds != NULL)                 */
+    const float* bias;          /* [B][ld_bias] fp32 additive bias or NULL; ld_bias == 0 shares
+                                   one [V] row across the batch.  May hold -inf.             */
+    int64_t ld_bias;
+    const uint32_t* allow_mask; /* [B][ld_mask] words or NULL: bit (v % 32) of word (v / 32)
+                                   set = token v allowed.  ld_mask == 0 shares one row.      */
+    int64_t ld_mask;
+    uint64_t base_seed;         /* key of unseeded rows                                       */
+    uint64_t offset;            /* step counter of unseeded rows; advance it every step      */
+    int32_t noise_mode;         /* lms_noise_mode                                             */
+    int32_t tile_v;             /* 0 = automatic; see lms_tile_info for the allowed values    */
+    int32_t path;               /* lms_path (fused entry point only)                          */
+    uint32_t timeout_ms;        /* bound on each device-side wait; 0 = 2000 ms                */
+    int32_t* row_status;        /* [B] per-row status out, or NULL                            */
+    uint32_t debug_flags;       /* 0, or LMS_DEBUG_* for fault-injection tests                */
+    uint32_t reserved;          /* must be 0                                                  */
+} lms_sample_params;
+
+/* Library version string. */
+const char* lms_version(void);
+
+/* Message for the last non-OK return on this thread ("" if none). */
+const char* lms_last_error(void);
+
+/* Tiling the entry point `op` will use for a call of these sizes.  tile_v_req = 0 asks for the
+ * automatic choice.  LMS_OP_LMHEAD: tile_v is 128 (one tcgen05 M=128 tile per vocabulary tile;
+ * the GEMV path uses the same tiles).  LMS_OP_LOGITS: tile_v is a power of two in
+ * [256, 65536].  Outputs (any may be NULL): the tile width, the number of vocabulary tiles
+ * nt = ceil(V / tile_v), the workspace size in bytes, and (fused op) the path auto selects.
+ * D is ignored for LMS_OP_LOGITS. */
+lms_status lms_tile_info(int32_t op, int64_t B, int64_t D, int64_t V, int32_t tile_v_req,
+                         int32_t* tile_v_out, int64_t* n_tiles_out, size_t* workspace_bytes_out,
+                         int32_t* path_out);
+
+/* Workspace bytes for a call of these sizes (0 if the sizes are invalid).  Layout, for tests
+ * that read the Stage-1 candidates: float score[B][nt] at offset 0, then int32 index[B][nt]
+ * at offset round_up(4*B*nt, 256).  index -1 = tile had no entry above -inf. */
+size_t lms_workspace_bytes(int32_t op, int64_t B, int64_t D, int64_t V, int32_t tile_v_req);
+
+/* Fused LM-head projection + Gumbel-max sampling (FlashSampling Stage 1 + Stage 2).
+ *   H   bf16 [B][ldh] hidden states (row-major), W bf16 [V][ldw] LM-head weight (row-major, the
+ *       vocabulary-major layout the FlashSampling page uses for W in R^{V x D}).
+ *   out int64 [B]: the sampled token per row (-1 when row status != 0).
+ * Logits are never written to memory: each CTA keeps its [128 x B] tile on chip (TMEM or
+ * registers) and writes one (score, index) candidate per row to the workspace; Stage 2 reduces
+ * them.  Requirements (LMS_ERR_UNSUPPORTED otherwise): D % 8 == 0, ldh and ldw multiples of
+ * 8 elements, H and W 16-byte aligned, 1 <= B <= 65536, 1 <= V < 2^31, D <= 65536.
+ * LMS_PATH_GEMV needs B <= LMS_GEMV_MAX_B. */
+lms_status lms_lmhead_sample(const void* H, int64_t ldh, const void* W, int64_t ldw, int64_t B,
+                             int64_t D, int64_t V, const lms_sample_params* params, int64_t* out,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* The same race over materialised logits [B][ld] (fp32 or bf16).  ld == 0 broadcasts one
+ * row to all B draws (each draw keyed by its own row index / position).  Several CTAs share a
+ * row (one per tile of tile_v entries); the noise is generated in registers.
+ * Requirements: 1 <= B < 2^31, 1 <= V < 2^31; any alignment (16-byte aligned rows are read
+ * with 128-bit loads). */
+lms_status lms_sample_from_logits(const void* logits, int32_t dtype, int64_t ld, int64_t B,
+                                  int64_t V, const lms_sample_params* params, int64_t* out,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* Noise grid [B][V] as the sampling kernels compute it, for testing and debugging
+ * (Megatron-LM PR 8370, "Tests": the noise replays bit-exactly; the words are the bit-exact
+ * surface).  kind selects the output (lms_noise_kind; element sizes 16, 8, 4, 4 bytes);
+ * noise_mode picks FP32 or WIDE53.  seeds / positions as in lms_sample_params. */
+lms_status lms_philox_fill_noise(void* out, int32_t kind, int32_t noise_mode, int64_t B,
+                                 int64_t V, const int64_t* seeds, const int64_t* positions,
+                                 uint64_t base_seed, uint64_t offset, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LMS_H_ */

@@ -1,0 +1,280 @@
+"""Exact Gumbel-max token sampling fused into the LM-head projection, for GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI in ``include/lms.h`` (library ``_lib/liblms.so``).  Every
+step of the computation runs in the library's CUDA kernels; this module only checks tensor
+metadata, allocates the workspace with PyTorch and passes raw device pointers and the current
+CUDA stream.  There is no CPU fallback: if the library is missing or no GPU is present, calls
+raise.
+
+    tokens = lmhead_sample(H, W, temperature=T, seeds=seeds, positions=pos)
+    tokens = sample_from_logits(logits, temperature=T, seeds=seeds, positions=pos)
+    noise  = philox_fill_noise(B, V, kind="gumbel", seeds=seeds, positions=pos)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "liblms.so")
+
+LMS_OK, LMS_ERR_INVALID_ARG, LMS_ERR_UNSUPPORTED, LMS_ERR_WORKSPACE, LMS_ERR_CUDA = range(5)
+NOISE_FP32, NOISE_WIDE53 = 0, 1
+DTYPE_F32, DTYPE_BF16 = 0, 1
+OP_LMHEAD, OP_LOGITS = 0, 1
+PATH_AUTO, PATH_GEMV, PATH_TCGEN05 = 0, 1, 2
+NOISE_KINDS = {"words": 0, "uniform": 1, "exponential": 2, "gumbel": 3}
+ROW_OK, ROW_NO_CANDIDATE, ROW_BAD_TEMPERATURE, ROW_DEVICE_TIMEOUT = range(4)
+DEBUG_WITHHOLD_FIRST_LOAD = 1
+FUSED_TILE_V = 128
+GEMV_MAX_B = 8
+
+
+class LmsError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"lms status {status}: {message}")
+        self.status = status
+
+
+class SampleParams(ctypes.Structure):
+    """Mirror of ``lms_sample_params``."""
+    _fields_ = [
+        ("temperature", ctypes.c_void_p),
+        ("seeds", ctypes.c_void_p),
+        ("positions", ctypes.c_void_p),
+        ("bias", ctypes.c_void_p),
+        ("ld_bias", ctypes.c_int64),
+        ("allow_mask", ctypes.c_void_p),
+        ("ld_mask", ctypes.c_int64),
+        ("base_seed", ctypes.c_uint64),
+        ("offset", ctypes.c_uint64),
+        ("noise_mode", ctypes.c_int32),
+        ("tile_v", ctypes.c_int32),
+        ("path", ctypes.c_int32),
+        ("timeout_ms", ctypes.c_uint32),
+        ("row_status", ctypes.c_void_p),
+        ("debug_flags", ctypes.c_uint32),
+        ("reserved", ctypes.c_uint32),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -m lm_head_gumbel_lmhead_gb300.build` (needs nvcc)")
+            L = ctypes.CDLL(LIB_PATH)
+            P, i32, i64, u64, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                    ctypes.c_uint64, ctypes.c_size_t)
+            L.lms_version.restype = ctypes.c_char_p
+            L.lms_last_error.restype = ctypes.c_char_p
+            L.lms_tile_info.argtypes = [i32, i64, i64, i64, i32, P, P, P, P]
+            L.lms_tile_info.restype = i32
+            L.lms_workspace_bytes.argtypes = [i32, i64, i64, i64, i32]
+            L.lms_workspace_bytes.restype = sz
+            L.lms_lmhead_sample.argtypes = [P, i64, P, i64, i64, i64, i64,
+                                            ctypes.POINTER(SampleParams), P, P, sz, P]
+            L.lms_lmhead_sample.restype = i32
+            L.lms_sample_from_logits.argtypes = [P, i32, i64, i64, i64, ctypes.POINTER(SampleParams),
+                                                 P, P, sz, P]
+            L.lms_sample_from_logits.restype = i32
+            L.lms_philox_fill_noise.argtypes = [P, i32, i32, i64, i64, P, P, u64, u64, P]
+            L.lms_philox_fill_noise.restype = i32
+            _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != LMS_OK:
+        raise LmsError(status, lib().lms_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t: Optional[torch.Tensor], dtype, name, device):
+    if t is None:
+        return None
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous() and t.dim() == 1:
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _row_ld(t: Optional[torch.Tensor], name) -> int:
+    if t is None or t.dim() == 1:
+        if t is not None and t.stride(0) != 1:
+            raise ValueError(f"{name} must have unit stride")
+        return 0
+    if t.stride(1) != 1:
+        raise ValueError(f"{name} must be row-major with unit inner stride")
+    return t.stride(0)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def tile_info(op: int, B: int, D: int, V: int, tile_v: int = 0):
+    """(tile_v, n_tiles, workspace_bytes, auto_path) for a call of these sizes."""
+    tv, nt, ws, path = ctypes.c_int32(), ctypes.c_int64(), ctypes.c_size_t(), ctypes.c_int32()
+    _check(lib().lms_tile_info(op, B, D, V, tile_v, ctypes.byref(tv), ctypes.byref(nt),
+                               ctypes.byref(ws), ctypes.byref(path)))
+    return tv.value, nt.value, ws.value, path.value
+
+
+def workspace_bytes(op: int, B: int, D: int, V: int, tile_v: int = 0) -> int:
+    return int(lib().lms_workspace_bytes(op, B, D, V, tile_v))
+
+
+def split_workspace(ws: torch.Tensor, B: int, n_tiles: int):
+    """Views of the Stage-1 candidates in a workspace: (score f32 [B, nt], index i32 [B, nt])."""
+    n = B * n_tiles
+    off = (4 * n + 255) // 256 * 256
+    raw = ws.view(torch.uint8)
+    score = raw[: 4 * n].view(torch.float32).view(B, n_tiles)
+    index = raw[off: off + 4 * n].view(torch.int32).view(B, n_tiles)
+    return score, index
+
+
+def _params(B, device, temperature, seeds, positions, bias, mask, base_seed, offset, wide, tile_v,
+            path, row_status, timeout_ms, debug_flags):
+    temperature = _dev(temperature, torch.float32, "temperature", device)
+    seeds = _dev(seeds, torch.int64, "seeds", device)
+    positions = _dev(positions, torch.int64, "positions", device)
+    bias = _dev(bias, torch.float32, "bias", device)
+    mask = _dev(mask, torch.int32, "mask", device)
+    row_status = _dev(row_status, torch.int32, "row_status", device)
+    for t, n in ((temperature, "temperature"), (seeds, "seeds"), (positions, "positions"),
+                 (row_status, "row_status")):
+        if t is not None and (t.dim() != 1 or t.shape[0] < B or t.stride(0) != 1):
+            raise ValueError(f"{n} must be a contiguous vector of length >= {B}")
+    p = SampleParams()
+    p.temperature = temperature.data_ptr() if temperature is not None else None
+    p.seeds = seeds.data_ptr() if seeds is not None else None
+    p.positions = positions.data_ptr() if positions is not None else None
+    p.bias = bias.data_ptr() if bias is not None else None
+    p.ld_bias = _row_ld(bias, "bias")
+    p.allow_mask = mask.data_ptr() if mask is not None else None
+    p.ld_mask = _row_ld(mask, "mask")
+    p.base_seed = int(base_seed) & (2**64 - 1)
+    p.offset = int(offset) & (2**64 - 1)
+    p.noise_mode = NOISE_WIDE53 if wide else NOISE_FP32
+    p.tile_v = int(tile_v)
+    p.path = int(path)
+    p.timeout_ms = int(timeout_ms)
+    p.row_status = row_status.data_ptr() if row_status is not None else None
+    p.debug_flags = int(debug_flags)
+    p.reserved = 0
+    return p
+
+
+def lmhead_sample(H: torch.Tensor, W: torch.Tensor, *, temperature=None, seeds=None,
+                  positions=None, bias=None, mask=None, base_seed: int = 0, offset: int = 0,
+                  wide: bool = False, path: int = PATH_AUTO, out=None, workspace=None,
+                  row_status=None, timeout_ms: int = 0, debug_flags: int = 0,
+                  stream=None) -> torch.Tensor:
+    """Sample one token per row of H [B, D] from softmax((H W^T + bias) / T) with W [V, D].
+
+    bf16 H and W on the GPU; per-row temperature (fp32, 0 = greedy), seeds / positions (int64,
+    seed < 0 = unseeded), bias fp32 [B, V] or [V], mask int32 allow-bit words [B, ceil(V/32)].
+    Returns int64 [B] (-1 on rows whose status is not 0)."""
+    if H.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise TypeError("H and W must be bfloat16")
+    if not H.is_cuda or W.device != H.device:
+        raise ValueError("H and W must be on the same CUDA device")
+    if H.dim() != 2 or W.dim() != 2 or H.shape[1] != W.shape[1]:
+        raise ValueError("H must be [B, D] and W [V, D]")
+    if H.stride(1) != 1 or W.stride(1) != 1:
+        raise ValueError("H and W must be row-major with unit inner stride")
+    B, D = H.shape
+    V = W.shape[0]
+    dev = H.device
+    p = _params(B, dev, temperature, seeds, positions, bias, mask, base_seed, offset, wide, 0, path,
+                row_status, timeout_ms, debug_flags)
+    if out is None:
+        out = torch.empty(B, dtype=torch.int64, device=dev)
+    if workspace is None:
+        workspace = torch.empty(workspace_bytes(OP_LMHEAD, B, D, V), dtype=torch.uint8, device=dev)
+    _check(lib().lms_lmhead_sample(_ptr(H), H.stride(0), _ptr(W), W.stride(0), B, D, V,
+                                   ctypes.byref(p), _ptr(out), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def sample_from_logits(logits: torch.Tensor, *, B: Optional[int] = None, temperature=None,
+                       seeds=None, positions=None, bias=None, mask=None, base_seed: int = 0,
+                       offset: int = 0, wide: bool = False, tile_v: int = 0, out=None,
+                       workspace=None, row_status=None, stream=None) -> torch.Tensor:
+    """The same race over materialised logits: fp32 or bf16 [B, V] (row-major), or one row [V]
+    broadcast to B draws (pass B)."""
+    if logits.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("logits must be float32 or bfloat16")
+    if not logits.is_cuda:
+        raise ValueError("logits must be on a CUDA device")
+    if logits.dim() == 1:
+        if B is None:
+            raise ValueError("pass B for a broadcast row")
+        ld, V = 0, logits.shape[0]
+        if logits.stride(0) != 1:
+            raise ValueError("logits must be contiguous")
+    else:
+        if logits.stride(1) != 1:
+            raise ValueError("logits must be row-major with unit inner stride")
+        B = logits.shape[0] if B is None else B
+        ld, V = logits.stride(0), logits.shape[1]
+    dev = logits.device
+    p = _params(B, dev, temperature, seeds, positions, bias, mask, base_seed, offset, wide, tile_v,
+                PATH_AUTO, row_status, 0, 0)
+    if out is None:
+        out = torch.empty(B, dtype=torch.int64, device=dev)
+    if workspace is None:
+        workspace = torch.empty(workspace_bytes(OP_LOGITS, B, 0, V, tile_v), dtype=torch.uint8,
+                                device=dev)
+    dt = DTYPE_F32 if logits.dtype == torch.float32 else DTYPE_BF16
+    _check(lib().lms_sample_from_logits(_ptr(logits), dt, ld, B, V, ctypes.byref(p), _ptr(out),
+                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        _stream(stream)))
+    return out
+
+
+def philox_fill_noise(B: int, V: int, *, kind: str = "gumbel", wide: bool = False, seeds=None,
+                      positions=None, base_seed: int = 0, offset: int = 0, device=None,
+                      out=None, stream=None) -> torch.Tensor:
+    """Noise grid [B, V] as the samplers compute it: kind 'words' (int32 [B, V, 4] holding the
+    uint32 Philox words), 'uniform' (float64, exact), 'exponential' or 'gumbel' (float32)."""
+    k = NOISE_KINDS[kind]
+    device = torch.device(device or "cuda")
+    if out is None:
+        if k == 0:
+            out = torch.empty(B, V, 4, dtype=torch.int32, device=device)
+        elif k == 1:
+            out = torch.empty(B, V, dtype=torch.float64, device=device)
+        else:
+            out = torch.empty(B, V, dtype=torch.float32, device=device)
+    seeds = _dev(seeds, torch.int64, "seeds", out.device)
+    positions = _dev(positions, torch.int64, "positions", out.device)
+    _check(lib().lms_philox_fill_noise(_ptr(out), k, NOISE_WIDE53 if wide else NOISE_FP32, B, V,
+                                       _ptr(seeds), _ptr(positions), int(base_seed) & (2**64 - 1),
+                                       int(offset) & (2**64 - 1), _stream(stream)))
+    return out
+
+
+def version() -> str:
+    return lib().lms_version().decode()

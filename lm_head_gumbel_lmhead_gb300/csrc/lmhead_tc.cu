@@ -1,0 +1,485 @@
+// Fused LM-head + Gumbel-max Stage 1 on the 5th-generation tensor cores (sm_103a).
+//
+// FlashSampling ("method step details", Stage 1): for each vocabulary tile, compute
+// Y = H W^T on chip (step 1), transform it (step 2), add Gumbel noise (steps 3-4), keep the
+// per-row (max, index) (step 5) and write that candidate (step 6).  The logits never reach
+// memory.
+//
+// Design for GB300 (one persistent CTA per SM, warp-specialised):
+//   warp 0      TMA producer: W[128 x 64] and H[n_pad x 64] bf16 chunks, 128-byte swizzle, into an
+//               S-stage shared-memory ring guarded by mbarriers (no multicast).
+//   warp 1      allocates TMEM; one lane issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32) with
+//               "swap-AB": M = 128 vocabulary rows of W, N = n_pad batch rows of H, K = 16 per
+//               instruction, into one of two TMEM accumulators [128 lanes x n_pad columns].
+//   warps 2..   epilogue (4 or 8 warps): tcgen05.ld the accumulator (thread = one vocabulary row,
+//               registers = batch columns), apply bias / mask / temperature, run Philox and the
+//               noise per element, reduce the argmax over the 128 rows with warp shuffles and
+//               shared memory, write one candidate per batch row.
+// The double-buffered accumulator lets the epilogue of tile i overlap the loads and MMAs of
+// tile i+1.  Every mbarrier wait is bounded in time; a CTA whose wait runs out flags the error,
+// drains its in-flight copies and MMAs, poisons its remaining candidates (index -2, reported
+// as row status 3 by Stage 2), frees TMEM and exits.
+#include <cuda.h>
+
+#include "lms.h"
+#include "lms_device.cuh"
+#include "lms_kernels.h"
+
+namespace lms {
+namespace {
+
+constexpr int kTileV = 128;                       // tcgen05 M
+constexpr int kBK = 64;                           // K elements per stage (one 128-byte row)
+constexpr int kWStageBytes = kTileV * kBK * 2;    // 16 KB
+constexpr int kMaxStages = 12;
+constexpr uint32_t kEpiBarrierId = 1;
+
+struct TcParams {
+    SampleArgs a;
+    int nk;              // number of K chunks, ceil(D / 64)
+    int n_pad;           // MMA N: batch rows padded to a multiple of 16 (16..256)
+    int stages;
+    uint32_t stage_bytes;
+    uint32_t tmem_cols;
+    uint64_t timeout_ns;
+    uint32_t debug_flags;
+};
+
+// ------------------------------------------------------------------------------------------
+// PTX wrappers
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits until the barrier phase of the given parity has completed.  Gives up (returns false)
+// when `timeout_ns` passes or, if `err` is non-null, when another role has flagged an error.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                          const volatile int* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t deadline = global_timer_ns() + timeout_ns;
+    for (uint32_t spin = 1;; ++spin) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((spin & 31u) == 0u) {
+            if (err != nullptr && *err != 0) return false;
+            if (global_timer_ns() > deadline) return false;
+        }
+    }
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 2-D tiled TMA load (box given by the descriptor) completing on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y,
+                                            uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate; issued by one thread.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when all tcgen05 operations issued so far by this thread have completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// 32 TMEM lanes x 16 consecutive 32-bit columns -> 16 registers per thread (lane = thread).
+__device__ __forceinline__ void tmem_load_16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void epi_barrier(int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(kEpiBarrierId), "r"(threads) : "memory");
+}
+
+// Barrier over the epilogue warps that also ANDs a flag across them, so that every epilogue
+// thread takes the same branch after a bounded wait (no thread can be left at a barrier).
+__device__ __forceinline__ bool epi_barrier_and(int threads, bool flag) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred p, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(flag ? 1u : 0u), "r"(kEpiBarrierId), "r"(threads)
+        : "memory");
+    return r != 0;
+}
+
+// Shared-memory matrix descriptor for a K-major operand tile written by TMA with the 128-byte
+// swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), the leading
+// byte offset unused for this layout, descriptor version 1, layout code 2 = 128-byte swizzle.
+__device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1u) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major, N and M.
+__host__ __device__ constexpr uint32_t mma_idesc_bf16(int n, int m) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// ------------------------------------------------------------------------------------------
+// Shared-memory layout (offsets from a 1024-byte aligned base)
+// ------------------------------------------------------------------------------------------
+struct SmemLayout {
+    uint32_t stages_off, bars_off, misc_off, rows_off, red_s_off, red_i_off, total;
+    __host__ __device__ SmemLayout(int stages, uint32_t stage_bytes, int n_pad) {
+        stages_off = 0;
+        bars_off = stages * stage_bytes;
+        // full[S], empty[S], acc_full[2], acc_empty[2], drain
+        misc_off = bars_off + (2 * stages + 5) * 8;
+        rows_off = (misc_off + 16 + 15) & ~15u;   // misc: tmem slot, error flag
+        red_s_off = rows_off + n_pad * static_cast<uint32_t>(sizeof(RowParams));
+        red_i_off = red_s_off + 4 * n_pad * 4;
+        total = red_i_off + 4 * n_pad * 4;
+    }
+};
+
+template <int kEpiWarps, bool kWide>
+__global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
+    lmhead_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
+                     const TcParams prm) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
+    uint8_t* base = smem_raw + (base_addr - raw_addr);
+    const SmemLayout L(prm.stages, prm.stage_bytes, prm.n_pad);
+
+    const SampleArgs& a = prm.a;
+    const int S = prm.stages;
+    const int n_pad = prm.n_pad;
+    const int B = static_cast<int>(a.B);
+    const int64_t nt = a.n_tiles;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const uint32_t bar0 = base_addr + L.bars_off;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+    auto accf_bar = [&](int ab) { return bar0 + 8u * (2 * S + ab); };
+    auto acce_bar = [&](int ab) { return bar0 + 8u * (2 * S + 2 + ab); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.misc_off);
+    volatile int* err = reinterpret_cast<volatile int*>(base + L.misc_off + 4);
+    RowParams* rows = reinterpret_cast<RowParams*>(base + L.rows_off);
+    float* red_s = reinterpret_cast<float*>(base + L.red_s_off);   // [4][n_pad]
+    int* red_i = reinterpret_cast<int*>(base + L.red_i_off);       // [4][n_pad]
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int ab = 0; ab < 2; ++ab) {
+            mbar_init(accf_bar(ab), 1);
+            mbar_init(acce_bar(ab), kEpiWarps);
+        }
+        mbar_init(drain_bar, 1);
+        *err = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmH)) : "memory");
+    }
+    for (int b = threadIdx.x; b < B; b += blockDim.x)
+        rows[b] = make_row_params(a.temperature, a.seeds, a.positions, a.base_seed, a.offset,
+                                  a.row0 + b);
+    if (warp == 1) tmem_alloc(base_addr + L.misc_off, prm.tmem_cols);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            const uint64_t pol_w = l2_policy_evict_first();
+            const uint64_t pol_h = l2_policy_evict_last();
+            uint32_t issued = 0, issued_parity = 0;   // per-stage: load in flight, its phase
+            int stage = 0;
+            uint32_t phase = 0;
+            bool first = true;
+            for (int64_t tile = blockIdx.x; tile < nt && *err == 0; tile += gridDim.x) {
+                for (int kc = 0; kc < prm.nk; ++kc) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, prm.timeout_ns, err)) {
+                        *err = 1;
+                        break;
+                    }
+                    const bool withhold = first && blockIdx.x == 0 &&
+                                          (prm.debug_flags & LMS_DEBUG_WITHHOLD_FIRST_LOAD);
+                    first = false;
+                    if (!withhold) {
+                        const uint32_t dst = base_addr + L.stages_off + stage * prm.stage_bytes;
+                        mbar_arrive_expect_tx(full_bar(stage), prm.stage_bytes);
+                        tma_load_2d(dst, &tmW, kc * kBK, static_cast<int>(tile * kTileV),
+                                    full_bar(stage), pol_w);
+                        tma_load_2d(dst + kWStageBytes, &tmH, kc * kBK, static_cast<int>(a.row0),
+                                    full_bar(stage), pol_h);
+                        issued |= 1u << stage;
+                        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    }
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // Drain: every copy this thread started must land before the CTA may exit.
+            for (int s = 0; s < S; ++s)
+                if (issued & (1u << s))
+                    mbar_wait(full_bar(s), (issued_parity >> s) & 1u, prm.timeout_ns, nullptr);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            const uint32_t idesc = mma_idesc_bf16(n_pad, kTileV);
+            int stage = 0;
+            uint32_t phase = 0;
+            int i = 0;
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; tile < nt && ok; tile += gridDim.x, ++i) {
+                const int ab = i & 1;
+                const uint32_t use_parity = (i >> 1) & 1;
+                if (!mbar_wait(acce_bar(ab), use_parity ^ 1u, prm.timeout_ns, err)) { ok = false; break; }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * n_pad);
+                for (int kc = 0; kc < prm.nk; ++kc) {
+                    if (!mbar_wait(full_bar(stage), phase, prm.timeout_ns, err)) { ok = false; break; }
+                    tc_fence_after_sync();
+                    const uint32_t sa = base_addr + L.stages_off + stage * prm.stage_bytes;
+                    const uint64_t adesc = kmajor_sw128_desc(sa);
+                    const uint64_t bdesc = kmajor_sw128_desc(sa + kWStageBytes);
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        // advance 16 bf16 = 32 bytes along K inside the swizzle atom
+                        mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc,
+                                 (kc | k) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(empty_bar(stage));
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                mma_commit(accf_bar(ab));
+            }
+            if (!ok) *err = 1;
+            // Drain: all MMAs issued by this thread complete before TMEM is freed.
+            mma_commit(drain_bar);
+            mbar_wait(drain_bar, 0, prm.timeout_ns, nullptr);
+        }
+    } else {
+        // ---------------- epilogue ----------------
+        const int epi_tid = threadIdx.x - 64;
+        const int epi_threads = 32 * kEpiWarps;
+        const int quad = warp & 3;                       // TMEM lanes 32*quad .. 32*quad+31
+        const int col_group = (warp - 2) >> 2;           // which column chunks this warp takes
+        constexpr int kColGroups = kEpiWarps / 4;
+        const int n_chunks = (B + 15) / 16;
+        int i = 0;
+        bool ok = true;
+        for (int64_t tile = blockIdx.x; tile < nt; tile += gridDim.x, ++i) {
+            const int ab = i & 1;
+            const uint32_t use_parity = (i >> 1) & 1;
+            if (ok) ok = mbar_wait(accf_bar(ab), use_parity, prm.timeout_ns, err);
+            ok = epi_barrier_and(epi_threads, ok);
+            if (!ok) {
+                // Poison this tile's candidates (and, through the loop, every later one).
+                if (epi_tid == 0) *err = 1;
+                for (int b = epi_tid; b < B; b += epi_threads) {
+                    a.cand_score[b * nt + tile] = -CUDART_INF_F;
+                    a.cand_index[b * nt + tile] = kPoisonIndex;
+                }
+                continue;
+            }
+            tc_fence_after_sync();
+            const int r = 32 * quad + lane;
+            const int64_t v = tile * kTileV + r;
+            const bool v_ok = v < a.V;
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) +
+                                   static_cast<uint32_t>(ab * n_pad);
+            for (int cc = col_group; cc < n_chunks; cc += kColGroups) {
+                uint32_t acc[16];
+                tmem_load_16(t_row + 16u * cc, acc);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int b = cc * 16 + j;
+                    if (b < B) {
+                        const RowParams p = rows[b];
+                        float s = -CUDART_INF_F;
+                        if (v_ok && !(p.flags & kRowInvalid)) {
+                            const int64_t row = a.row0 + b;
+                            const float bias = a.bias ? __ldg(a.bias + row * a.ld_bias + v) : 0.0f;
+                            const uint32_t* mrow = a.mask ? a.mask + row * a.ld_mask : nullptr;
+                            s = perturbed_score<kWide>(p, static_cast<uint32_t>(v),
+                                                       __uint_as_float(acc[j]), bias,
+                                                       allowed(mrow, static_cast<uint32_t>(v)));
+                        }
+                        int idx = static_cast<int>(v);
+                        warp_argmax(s, idx);
+                        if (lane == 0) { red_s[quad * n_pad + b] = s; red_i[quad * n_pad + b] = idx; }
+                    }
+                }
+            }
+            // The accumulator buffer is free for the MMA of tile i+2.
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce_bar(ab));
+            epi_barrier(epi_threads);
+            for (int b = epi_tid; b < B; b += epi_threads) {
+                float s = red_s[b];
+                int idx = red_i[b];
+#pragma unroll
+                for (int q = 1; q < 4; ++q)
+                    if (better(red_s[q * n_pad + b], red_i[q * n_pad + b], s, idx)) {
+                        s = red_s[q * n_pad + b];
+                        idx = red_i[q * n_pad + b];
+                    }
+                a.cand_score[b * nt + tile] = s;
+                a.cand_index[b * nt + tile] = candidate_index(s, idx);
+            }
+            epi_barrier(epi_threads);
+        }
+    }
+
+    pdl_launch_dependents();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, prm.tmem_cols);
+    }
+}
+
+template <int kEpiWarps, bool kWide>
+cudaError_t launch_variant(const CUtensorMap& tmW, const CUtensorMap& tmH, const TcParams& prm,
+                           size_t smem, int grid, cudaStream_t stream) {
+    auto kern = lmhead_tc_kernel<kEpiWarps, kWide>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    kern<<<grid, 32 * (2 + kEpiWarps), smem, stream>>>(tmW, tmH, prm);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int64_t D, int n_pad,
+                             bool wide, uint32_t timeout_ms, uint32_t debug_flags,
+                             const SampleArgs& a, cudaStream_t stream) {
+    TcParams prm;
+    prm.a = a;
+    prm.nk = static_cast<int>((D + kBK - 1) / kBK);
+    prm.n_pad = n_pad;
+    prm.stage_bytes = static_cast<uint32_t>(kWStageBytes + n_pad * kBK * 2);
+    const uint32_t budget = 227u * 1024u - 1024u;   // opt-in maximum minus alignment slack
+    const SmemLayout fixed(0, prm.stage_bytes, n_pad);
+    int stages = static_cast<int>((budget - fixed.total - (2 * kMaxStages + 5) * 8) / prm.stage_bytes);
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages < 2) return cudaErrorInvalidValue;
+    prm.stages = stages;
+    uint32_t cols = 32;
+    while (cols < static_cast<uint32_t>(2 * n_pad)) cols <<= 1;
+    prm.tmem_cols = cols;
+    prm.timeout_ns = static_cast<uint64_t>(timeout_ms) * 1000000ull;
+    prm.debug_flags = debug_flags;
+    const SmemLayout L(stages, prm.stage_bytes, n_pad);
+    const size_t smem = L.total + 1024;
+    int sms = device_sm_count();
+    int grid = static_cast<int>(a.n_tiles < sms ? a.n_tiles : sms);
+    if (n_pad <= 64) {
+        return wide ? launch_variant<4, true>(tmW, tmH, prm, smem, grid, stream)
+                    : launch_variant<4, false>(tmW, tmH, prm, smem, grid, stream);
+    }
+    return wide ? launch_variant<8, true>(tmW, tmH, prm, smem, grid, stream)
+                : launch_variant<8, false>(tmW, tmH, prm, smem, grid, stream);
+}
+
+}  // namespace lms

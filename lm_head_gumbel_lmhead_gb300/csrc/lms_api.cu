@@ -1,0 +1,304 @@
+// C-ABI entry points (include/lms.h): argument checks, tiling, TMA descriptors, launches.
+// Host-detectable errors return before anything is launched; nothing here allocates device
+// memory or keeps state between calls.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "lms.h"
+#include "lms_kernels.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+lms_status fail(lms_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+lms_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(LMS_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int64_t kMaxV = (int64_t{1} << 31) - 1;
+constexpr int kTcMaxBatchPerLaunch = 256;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Tiling {
+    int32_t tile_v;
+    int64_t n_tiles;
+    size_t workspace;
+    int32_t path;
+};
+
+int pick_logits_tile(int64_t B, int64_t V) {
+    // Several CTAs per row: aim for at least ~4 CTAs per SM over the whole grid, with tiles of
+    // 1K..8K entries (16 KB..32 KB of fp32 logits).
+    const int64_t target_ctas = 152 * 4;
+    int64_t t = 8192;
+    while (t > 1024 && B * ((V + t - 1) / t) < target_ctas) t >>= 1;
+    return static_cast<int>(t);
+}
+
+lms_status make_tiling(int32_t op, int64_t B, int64_t D, int64_t V, int32_t tile_req, Tiling* out) {
+    if (B <= 0 || V <= 0) return fail(LMS_ERR_INVALID_ARG, "B and V must be positive (B=%lld V=%lld)",
+                                      (long long)B, (long long)V);
+    if (V > kMaxV) return fail(LMS_ERR_INVALID_ARG, "V must be < 2^31 (V=%lld)", (long long)V);
+    if (op == LMS_OP_LMHEAD) {
+        if (D <= 0) return fail(LMS_ERR_INVALID_ARG, "D must be positive (D=%lld)", (long long)D);
+        if (B > 65536) return fail(LMS_ERR_INVALID_ARG, "B must be <= 65536 (B=%lld)", (long long)B);
+        if (tile_req != 0 && tile_req != LMS_FUSED_TILE_V)
+            return fail(LMS_ERR_UNSUPPORTED, "fused tile_v must be 0 or 128 (got %d)", tile_req);
+        out->tile_v = LMS_FUSED_TILE_V;
+        out->path = (B <= 2) ? LMS_PATH_GEMV : LMS_PATH_TCGEN05;
+    } else if (op == LMS_OP_LOGITS) {
+        if (B > (int64_t{1} << 31) - 1) return fail(LMS_ERR_INVALID_ARG, "B must be < 2^31");
+        if (tile_req == 0) {
+            out->tile_v = pick_logits_tile(B, V);
+        } else {
+            if (tile_req < 256 || tile_req > 65536 || (tile_req & (tile_req - 1)) != 0)
+                return fail(LMS_ERR_UNSUPPORTED, "logits tile_v must be a power of two in [256, 65536] (got %d)",
+                            tile_req);
+            out->tile_v = tile_req;
+        }
+        out->path = LMS_PATH_AUTO;
+    } else {
+        return fail(LMS_ERR_INVALID_ARG, "unknown op %d", op);
+    }
+    out->n_tiles = (V + out->tile_v - 1) / out->tile_v;
+    const int64_t grid = B * out->n_tiles;
+    if (op == LMS_OP_LOGITS && grid > (int64_t{1} << 31) - 1)
+        return fail(LMS_ERR_UNSUPPORTED, "B * n_tiles exceeds the launch grid limit");
+    const size_t cand = static_cast<size_t>(B) * static_cast<size_t>(out->n_tiles) * 4;
+    out->workspace = round_up(cand, 256) + round_up(cand, 256);
+    return LMS_OK;
+}
+
+lms_status check_params(const lms_sample_params* p, int64_t V) {
+    if (p == nullptr) return fail(LMS_ERR_INVALID_ARG, "params is NULL");
+    if (p->noise_mode != LMS_NOISE_FP32 && p->noise_mode != LMS_NOISE_WIDE53)
+        return fail(LMS_ERR_INVALID_ARG, "unknown noise_mode %d", p->noise_mode);
+    if (p->seeds != nullptr && p->positions == nullptr)
+        return fail(LMS_ERR_INVALID_ARG, "positions is required when seeds is given");
+    if (p->bias != nullptr && p->ld_bias != 0 && p->ld_bias < V)
+        return fail(LMS_ERR_INVALID_ARG, "ld_bias must be 0 or >= V");
+    if (p->allow_mask != nullptr && p->ld_mask != 0 && p->ld_mask < (V + 31) / 32)
+        return fail(LMS_ERR_INVALID_ARG, "ld_mask must be 0 or >= ceil(V/32)");
+    if (p->ld_bias < 0 || p->ld_mask < 0) return fail(LMS_ERR_INVALID_ARG, "negative leading dimension");
+    if (p->reserved != 0) return fail(LMS_ERR_INVALID_ARG, "reserved must be 0");
+    if (p->debug_flags & ~LMS_DEBUG_WITHHOLD_FIRST_LOAD)
+        return fail(LMS_ERR_INVALID_ARG, "unknown debug_flags 0x%x", p->debug_flags);
+    return LMS_OK;
+}
+
+lms::SampleArgs make_args(const lms_sample_params* p, int64_t B, int64_t V, const Tiling& t,
+                          void* workspace) {
+    lms::SampleArgs a;
+    a.temperature = p->temperature;
+    a.seeds = p->seeds;
+    a.positions = p->positions;
+    a.bias = p->bias;
+    a.ld_bias = p->ld_bias;
+    a.mask = p->allow_mask;
+    a.ld_mask = p->ld_mask;
+    a.base_seed = p->base_seed;
+    a.offset = p->offset;
+    a.B = B;
+    a.row0 = 0;
+    a.V = V;
+    a.n_tiles = t.n_tiles;
+    const size_t cand = static_cast<size_t>(B) * static_cast<size_t>(t.n_tiles) * 4;
+    a.cand_score = static_cast<float*>(workspace);
+    a.cand_index = reinterpret_cast<int*>(static_cast<char*>(workspace) + round_up(cand, 256));
+    return a;
+}
+
+// cuTensorMapEncodeTiled from the driver, found through the runtime (no link to libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// bf16 [rows][ld] row-major -> 2-D map {D, rows}, boxes of 64 x box_rows, 128-byte swizzle,
+// out-of-range elements read as zero.
+lms_status encode_bf16_map(CUtensorMap* tm, const void* ptr, int64_t rows, int64_t D, int64_t ld,
+                           int box_rows) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (fn == nullptr) return fail(LMS_ERR_CUDA, "cuTensorMapEncodeTiled not available from the driver");
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(LMS_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return LMS_OK;
+}
+
+}  // namespace
+
+namespace lms {
+int device_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return 148;
+    return sms;
+}
+}  // namespace lms
+
+extern "C" {
+
+const char* lms_version(void) { return "lms 0.1 (sm_103a)"; }
+
+const char* lms_last_error(void) { return g_last_error; }
+
+lms_status lms_tile_info(int32_t op, int64_t B, int64_t D, int64_t V, int32_t tile_v_req,
+                         int32_t* tile_v_out, int64_t* n_tiles_out, size_t* workspace_bytes_out,
+                         int32_t* path_out) {
+    Tiling t;
+    const lms_status st = make_tiling(op, B, D, V, tile_v_req, &t);
+    if (st != LMS_OK) return st;
+    if (tile_v_out) *tile_v_out = t.tile_v;
+    if (n_tiles_out) *n_tiles_out = t.n_tiles;
+    if (workspace_bytes_out) *workspace_bytes_out = t.workspace;
+    if (path_out) *path_out = t.path;
+    return LMS_OK;
+}
+
+size_t lms_workspace_bytes(int32_t op, int64_t B, int64_t D, int64_t V, int32_t tile_v_req) {
+    Tiling t;
+    return make_tiling(op, B, D, V, tile_v_req, &t) == LMS_OK ? t.workspace : 0;
+}
+
+lms_status lms_lmhead_sample(const void* H, int64_t ldh, const void* W, int64_t ldw, int64_t B,
+                             int64_t D, int64_t V, const lms_sample_params* params, int64_t* out,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+    g_last_error[0] = '\0';
+    if (H == nullptr || W == nullptr || out == nullptr)
+        return fail(LMS_ERR_INVALID_ARG, "H, W and out are required");
+    Tiling t;
+    lms_status st = make_tiling(LMS_OP_LMHEAD, B, D, V, params ? params->tile_v : 0, &t);
+    if (st != LMS_OK) return st;
+    if ((st = check_params(params, V)) != LMS_OK) return st;
+    if (D % 8 != 0) return fail(LMS_ERR_UNSUPPORTED, "D must be a multiple of 8 (D=%lld)", (long long)D);
+    if (D > 65536) return fail(LMS_ERR_UNSUPPORTED, "D must be <= 65536");
+    if (ldh < D || ldw < D || ldh % 8 != 0 || ldw % 8 != 0)
+        return fail(LMS_ERR_UNSUPPORTED, "ldh/ldw must be >= D and multiples of 8 elements");
+    if (reinterpret_cast<uintptr_t>(H) % 16 != 0 || reinterpret_cast<uintptr_t>(W) % 16 != 0)
+        return fail(LMS_ERR_UNSUPPORTED, "H and W must be 16-byte aligned");
+    if (workspace == nullptr || workspace_bytes < t.workspace)
+        return fail(LMS_ERR_WORKSPACE, "workspace of %zu bytes needed", t.workspace);
+    int32_t path = params->path == LMS_PATH_AUTO ? t.path : params->path;
+    if (path == LMS_PATH_GEMV && (B > LMS_GEMV_MAX_B || static_cast<size_t>(B) * D * 2 > 200 * 1024))
+        path = (params->path == LMS_PATH_GEMV) ? -1 : LMS_PATH_TCGEN05;
+    if (path == -1) return fail(LMS_ERR_UNSUPPORTED, "GEMV path needs B <= %d and B*D*2 <= 200 KB", LMS_GEMV_MAX_B);
+    if (path != LMS_PATH_GEMV && path != LMS_PATH_TCGEN05)
+        return fail(LMS_ERR_INVALID_ARG, "unknown path %d", params->path);
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool wide = params->noise_mode == LMS_NOISE_WIDE53;
+    lms::SampleArgs a = make_args(params, B, V, t, workspace);
+    cudaError_t e;
+    if (path == LMS_PATH_GEMV) {
+        e = lms::launch_lmhead_gemv(static_cast<const uint16_t*>(H), ldh, static_cast<const uint16_t*>(W),
+                                    ldw, D, wide, a, s);
+        if (e != cudaSuccess) return cuda_fail(e, "GEMV Stage-1 launch");
+    } else {
+        CUtensorMap tmW;
+        if ((st = encode_bf16_map(&tmW, W, V, D, ldw, 128)) != LMS_OK) return st;
+        const uint32_t timeout_ms = params->timeout_ms ? params->timeout_ms : 2000u;
+        // Batches above 256 rows run as several launches of <= 256 rows (one MMA N each).
+        for (int64_t r0 = 0; r0 < B; r0 += kTcMaxBatchPerLaunch) {
+            const int64_t nb = (B - r0 < kTcMaxBatchPerLaunch) ? B - r0 : kTcMaxBatchPerLaunch;
+            const int n_pad = static_cast<int>(nb < 16 ? 16 : (nb + 15) / 16 * 16);
+            CUtensorMap tmH;
+            if ((st = encode_bf16_map(&tmH, H, B, D, ldh, n_pad)) != LMS_OK) return st;
+            lms::SampleArgs ac = a;
+            ac.B = nb;
+            ac.row0 = r0;
+            ac.cand_score = a.cand_score + r0 * t.n_tiles;
+            ac.cand_index = a.cand_index + r0 * t.n_tiles;
+            e = lms::launch_lmhead_tc(tmW, tmH, D, n_pad, wide, timeout_ms, params->debug_flags, ac, s);
+            if (e != cudaSuccess) return cuda_fail(e, "tcgen05 Stage-1 launch");
+        }
+    }
+    e = lms::launch_stage2(a.cand_score, a.cand_index, t.n_tiles, B, params->temperature, out,
+                           params->row_status, s);
+    if (e != cudaSuccess) return cuda_fail(e, "Stage-2 launch");
+    return LMS_OK;
+}
+
+lms_status lms_sample_from_logits(const void* logits, int32_t dtype, int64_t ld, int64_t B,
+                                  int64_t V, const lms_sample_params* params, int64_t* out,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+    g_last_error[0] = '\0';
+    if (logits == nullptr || out == nullptr) return fail(LMS_ERR_INVALID_ARG, "logits and out are required");
+    if (dtype != LMS_DTYPE_F32 && dtype != LMS_DTYPE_BF16)
+        return fail(LMS_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+    Tiling t;
+    lms_status st = make_tiling(LMS_OP_LOGITS, B, 0, V, params ? params->tile_v : 0, &t);
+    if (st != LMS_OK) return st;
+    if ((st = check_params(params, V)) != LMS_OK) return st;
+    if (ld != 0 && ld < V) return fail(LMS_ERR_INVALID_ARG, "ld must be 0 (broadcast) or >= V");
+    if (params->path != LMS_PATH_AUTO) return fail(LMS_ERR_INVALID_ARG, "path applies to the fused entry only");
+    if (params->debug_flags != 0) return fail(LMS_ERR_INVALID_ARG, "debug_flags apply to the fused entry only");
+    if (workspace == nullptr || workspace_bytes < t.workspace)
+        return fail(LMS_ERR_WORKSPACE, "workspace of %zu bytes needed", t.workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    lms::SampleArgs a = make_args(params, B, V, t, workspace);
+    cudaError_t e = lms::launch_logits_stage1(logits, dtype == LMS_DTYPE_BF16, ld, t.tile_v,
+                                              params->noise_mode == LMS_NOISE_WIDE53, a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "logits Stage-1 launch");
+    e = lms::launch_stage2(a.cand_score, a.cand_index, t.n_tiles, B, params->temperature, out,
+                           params->row_status, s);
+    if (e != cudaSuccess) return cuda_fail(e, "Stage-2 launch");
+    return LMS_OK;
+}
+
+lms_status lms_philox_fill_noise(void* out, int32_t kind, int32_t noise_mode, int64_t B, int64_t V,
+                                 const int64_t* seeds, const int64_t* positions, uint64_t base_seed,
+                                 uint64_t offset, void* stream) {
+    g_last_error[0] = '\0';
+    if (out == nullptr) return fail(LMS_ERR_INVALID_ARG, "out is required");
+    if (kind < LMS_NOISE_OUT_WORDS || kind > LMS_NOISE_OUT_GUMBEL)
+        return fail(LMS_ERR_INVALID_ARG, "unknown noise kind %d", kind);
+    if (noise_mode != LMS_NOISE_FP32 && noise_mode != LMS_NOISE_WIDE53)
+        return fail(LMS_ERR_INVALID_ARG, "unknown noise_mode %d", noise_mode);
+    if (B <= 0 || V <= 0 || V > kMaxV) return fail(LMS_ERR_INVALID_ARG, "need B > 0 and 0 < V < 2^31");
+    if (seeds != nullptr && positions == nullptr)
+        return fail(LMS_ERR_INVALID_ARG, "positions is required when seeds is given");
+    const size_t align = kind == LMS_NOISE_OUT_WORDS ? 16 : (kind == LMS_NOISE_OUT_UNIFORM ? 8 : 4);
+    if (reinterpret_cast<uintptr_t>(out) % align != 0)
+        return fail(LMS_ERR_UNSUPPORTED, "out must be %zu-byte aligned", align);
+    const cudaError_t e = lms::launch_noise_fill(out, kind, noise_mode == LMS_NOISE_WIDE53, B, V, seeds,
+                                                 positions, base_seed, offset, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "noise-fill launch");
+    return LMS_OK;
+}
+
+}  // extern "C"

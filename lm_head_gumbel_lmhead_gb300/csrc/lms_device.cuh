@@ -1,0 +1,200 @@
+// Device-side building blocks shared by the sampling kernels: the Philox4x32-10 generator, the
+// uniform -> exponential -> Gumbel noise in fp32, the per-row transform, and the
+// lexicographic (score, index) argmax.  Every kernel computes the noise through these
+// functions, so the noise-fill kernel tests exactly what the samplers use.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+namespace lms {
+
+// ---------------------------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",
+// SC'11): ten rounds of two 32x32->64-bit products whose high halves are xored with the other
+// two words and the round key; the key advances by the Weyl constants between rounds.
+// ---------------------------------------------------------------------------------------------
+constexpr uint32_t kPhiloxMulA = 0xD2511F53u;
+constexpr uint32_t kPhiloxMulB = 0xCD9E8D57u;
+constexpr uint32_t kWeylA = 0x9E3779B9u;
+constexpr uint32_t kWeylB = 0xBB67AE85u;
+
+struct Words { uint32_t w0, w1, w2, w3; };
+
+__device__ __forceinline__ Words philox4x32_10(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3,
+                                               uint32_t ka, uint32_t kb) {
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint64_t pa = static_cast<uint64_t>(kPhiloxMulA) * x0;
+        const uint64_t pb = static_cast<uint64_t>(kPhiloxMulB) * x2;
+        const uint32_t n0 = static_cast<uint32_t>(pb >> 32) ^ x1 ^ ka;
+        const uint32_t n2 = static_cast<uint32_t>(pa >> 32) ^ x3 ^ kb;
+        x1 = static_cast<uint32_t>(pb);
+        x3 = static_cast<uint32_t>(pa);
+        x0 = n0;
+        x2 = n2;
+        ka += kWeylA;
+        kb += kWeylB;
+    }
+    return {x0, x1, x2, x3};
+}
+
+// Per-row generator state: the key and the counter words that do not depend on v.
+struct RowKey {
+    uint32_t ka, kb;      // key
+    uint32_t c1, c2, c3;  // counter words 1..3 (word 0 is the vocabulary index)
+};
+
+// (request seed, absolute position) for seeded rows; (base_seed, offset, row) otherwise.
+__device__ __forceinline__ RowKey make_row_key(const int64_t* seeds, const int64_t* positions,
+                                               uint64_t base_seed, uint64_t offset, int64_t row) {
+    RowKey k;
+    if (seeds != nullptr && seeds[row] >= 0) {
+        const uint64_t s = static_cast<uint64_t>(seeds[row]);
+        const uint64_t p = static_cast<uint64_t>(positions[row]);
+        k.ka = static_cast<uint32_t>(s);
+        k.kb = static_cast<uint32_t>(s >> 32);
+        k.c1 = static_cast<uint32_t>(p);
+        k.c2 = static_cast<uint32_t>(p >> 32);
+        k.c3 = 0u;
+    } else {
+        k.ka = static_cast<uint32_t>(base_seed);
+        k.kb = static_cast<uint32_t>(base_seed >> 32);
+        k.c1 = static_cast<uint32_t>(offset);
+        k.c2 = static_cast<uint32_t>(offset >> 32);
+        k.c3 = 0x80000000u | static_cast<uint32_t>(row);
+    }
+    return k;
+}
+
+__device__ __forceinline__ Words row_words(const RowKey& k, uint32_t v) {
+    return philox4x32_10(v, k.c1, k.c2, k.c3, k.ka, k.kb);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Uniform -> E = -log u -> g = -log E, in fp32.
+//
+// u = (k + 1/2) / 2^m is written as n / 2^(m+1) with n = 2k + 1 odd.  Below one half, u itself
+// is formed (exact for m = 24; one rounding for m = 52) and E = -log u; above one half the
+// complement c = 1 - u = (2^(m+1) - n) / 2^(m+1) is formed from integers the same way and
+// E = -log1p(-c), so the tail (u -> 1, E -> 0, the largest g) keeps full relative precision:
+// E reaches 2^-25 (fp32 noise) and 2^-53 (wide noise) as the Megatron-LM PR's ranges require.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ float exponential_from_odd24(uint32_t n /* odd, < 2^25 */) {
+    // u = n / 2^25
+    if (n < (1u << 24)) {
+        return -__logf(static_cast<float>(n) * 0x1p-25f);
+    }
+    const float c = static_cast<float>((1u << 25) - n) * 0x1p-25f;  // exact: < 2^24, odd
+    return -log1pf(-c);
+}
+
+__device__ __forceinline__ float exponential_from_odd53(uint64_t n /* odd, < 2^53 */) {
+    // u = n / 2^53
+    if (n < (1ull << 52)) {
+        return -__logf(__ull2float_rn(n) * 0x1p-53f);
+    }
+    const float c = __ull2float_rn((1ull << 53) - n) * 0x1p-53f;
+    return -log1pf(-c);
+}
+
+__device__ __forceinline__ float exponential_fp32(const Words& w) {
+    return exponential_from_odd24(((w.w0 >> 8) << 1) | 1u);
+}
+
+__device__ __forceinline__ float exponential_wide(const Words& w) {
+    const uint64_t k = ((static_cast<uint64_t>(w.w1) << 32) | w.w0) >> 12;
+    return exponential_from_odd53((k << 1) | 1ull);
+}
+
+__device__ __forceinline__ float gumbel_from_exponential(float E) { return -__logf(E); }
+
+template <bool kWide>
+__device__ __forceinline__ float gumbel(const RowKey& k, uint32_t v) {
+    const Words w = row_words(k, v);
+    return gumbel_from_exponential(kWide ? exponential_wide(w) : exponential_fp32(w));
+}
+
+// ---------------------------------------------------------------------------------------------
+// Per-row parameters and the transform (bias before temperature; T == 0 greedy; mask -> -inf).
+// ---------------------------------------------------------------------------------------------
+enum RowFlags : uint32_t { kRowGreedy = 1u, kRowInvalid = 2u };
+
+struct RowParams {
+    RowKey key;
+    float inv_t;     // 1 / T for sampled rows
+    uint32_t flags;  // RowFlags
+};
+
+__device__ __forceinline__ RowParams make_row_params(const float* temperature, const int64_t* seeds,
+                                                     const int64_t* positions, uint64_t base_seed,
+                                                     uint64_t offset, int64_t row) {
+    RowParams p;
+    p.key = make_row_key(seeds, positions, base_seed, offset, row);
+    const float T = temperature ? temperature[row] : 1.0f;
+    p.flags = 0u;
+    p.inv_t = 1.0f;
+    if (!(T >= 0.0f)) {
+        p.flags = kRowInvalid;           // T < 0 or NaN
+    } else if (T == 0.0f) {
+        p.flags = kRowGreedy;
+    } else {
+        p.inv_t = 1.0f / T;
+    }
+    return p;
+}
+
+__device__ __forceinline__ bool allowed(const uint32_t* mask_row, uint32_t v) {
+    return mask_row == nullptr || ((__ldg(mask_row + (v >> 5)) >> (v & 31u)) & 1u);
+}
+
+// Perturbed score of one entry.  `y` is the raw logit, `bias` already looked up (0 if none).
+template <bool kWide>
+__device__ __forceinline__ float perturbed_score(const RowParams& p, uint32_t v, float y,
+                                                 float bias, bool is_allowed) {
+    if (!is_allowed) return -CUDART_INF_F;
+    const float t = y + bias;
+    float s;
+    if (p.flags & kRowGreedy) {
+        s = t;
+    } else {
+        s = t * p.inv_t + gumbel<kWide>(p.key, v);
+    }
+    return (s == s) ? s : -CUDART_INF_F;  // NaN counts as -inf
+}
+
+// ---------------------------------------------------------------------------------------------
+// Lexicographic argmax: larger score, then smaller index.  Index 0x7fffffff marks "nothing yet".
+// ---------------------------------------------------------------------------------------------
+constexpr int kNoIndex = 0x7fffffff;
+
+__device__ __forceinline__ bool better(float sa, int ia, float sb, int ib) {
+    return sa > sb || (sa == sb && ia < ib);
+}
+
+__device__ __forceinline__ void warp_argmax(float& s, int& i) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float so = __shfl_xor_sync(0xffffffffu, s, off);
+        const int io = __shfl_xor_sync(0xffffffffu, i, off);
+        if (better(so, io, s, i)) { s = so; i = io; }
+    }
+}
+
+// The candidate a tile reports: index -1 when nothing in the tile is above -inf.
+__device__ __forceinline__ int candidate_index(float s, int i) {
+    return (s > -CUDART_INF_F && i != kNoIndex) ? i : -1;
+}
+
+// Index written by a CTA whose device-side wait ran out of time.
+constexpr int kPoisonIndex = -2;
+
+// Programmatic dependent launch: let the dependent grid start launching / wait for the primary.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+}  // namespace lms

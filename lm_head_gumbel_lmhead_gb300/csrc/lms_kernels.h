@@ -1,0 +1,51 @@
+// Internal launch interface between the C-ABI layer (lms_api.cu) and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace lms {
+
+// Everything a sampling kernel needs besides its logits / GEMM operands.
+struct SampleArgs {
+    const float* temperature;
+    const int64_t* seeds;
+    const int64_t* positions;
+    const float* bias;
+    int64_t ld_bias;
+    const uint32_t* mask;
+    int64_t ld_mask;
+    uint64_t base_seed;
+    uint64_t offset;
+    int64_t B;        // rows in this launch
+    int64_t row0;     // global row index of the first row (unseeded rows are keyed by it)
+    int64_t V;
+    int64_t n_tiles;  // candidate columns per row in the workspace
+    float* cand_score;  // [B][n_tiles] (already offset to row0)
+    int* cand_index;    // [B][n_tiles]
+};
+
+cudaError_t launch_noise_fill(void* out, int kind, bool wide, int64_t B, int64_t V,
+                              const int64_t* seeds, const int64_t* positions, uint64_t base_seed,
+                              uint64_t offset, cudaStream_t stream);
+
+cudaError_t launch_logits_stage1(const void* logits, bool bf16, int64_t ld, int tile_v, bool wide,
+                                 const SampleArgs& a, cudaStream_t stream);
+
+cudaError_t launch_stage2(const float* cand_score, const int* cand_index, int64_t n_tiles,
+                          int64_t B, const float* temperature, int64_t* out, int32_t* row_status,
+                          cudaStream_t stream);
+
+cudaError_t launch_lmhead_gemv(const uint16_t* H, int64_t ldh, const uint16_t* W, int64_t ldw,
+                               int64_t D, bool wide, const SampleArgs& a, cudaStream_t stream);
+
+// The tcgen05 path.  tmW / tmH are TMA descriptors (bf16, 128-byte swizzle, boxes of 64 x 128
+// for W and 64 x n_pad for H).  B <= 256 per launch.
+cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int64_t D, int n_pad,
+                             bool wide, uint32_t timeout_ms, uint32_t debug_flags,
+                             const SampleArgs& a, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace lms

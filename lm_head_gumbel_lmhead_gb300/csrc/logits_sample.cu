@@ -1,0 +1,124 @@
+// Stage 1 of the Gumbel race over materialised logits: one CTA per (row, tile of tile_v
+// entries), the noise generated in registers, one (score, index) candidate per CTA.
+// (Megatron-LM PR 8370, "Cost": a fused kernel that generates the noise in registers and reduces
+// each row in place, with several blocks per row; FlashSampling steps 2-6 over a logits tile.)
+#include <cuda_bf16.h>
+
+#include "lms_device.cuh"
+#include "lms_kernels.h"
+
+namespace lms {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <typename T>
+__device__ __forceinline__ float to_float(T x);
+template <>
+__device__ __forceinline__ float to_float<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_float<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// kVec consecutive entries per load (16 bytes when the rows are 16-byte aligned, else 1).
+template <typename T, int kVec>
+struct VecLoad {
+    __device__ __forceinline__ static void load(const T* p, float (&y)[kVec]) {
+        if constexpr (kVec == 1) {
+            y[0] = to_float<T>(p[0]);
+        } else {
+            const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p));
+            const T* e = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) y[j] = to_float<T>(e[j]);
+        }
+    }
+};
+
+template <typename T, int kVec, bool kWide>
+__global__ void __launch_bounds__(kThreads) logits_stage1_kernel(const T* __restrict__ logits,
+                                                                 int64_t ld, int tile_v,
+                                                                 SampleArgs a) {
+    const int64_t cta = blockIdx.x;
+    const int64_t b = cta / a.n_tiles;             // local row
+    const int64_t t = cta - b * a.n_tiles;         // tile
+    const int64_t row = a.row0 + b;
+    const RowParams p = make_row_params(a.temperature, a.seeds, a.positions, a.base_seed,
+                                        a.offset, row);
+    float best_s = -CUDART_INF_F;
+    int best_i = kNoIndex;
+    if (!(p.flags & kRowInvalid)) {
+        const T* y_row = logits + row * ld;
+        const float* bias_row = a.bias ? a.bias + row * a.ld_bias : nullptr;
+        const uint32_t* mask_row = a.mask ? a.mask + row * a.ld_mask : nullptr;
+        const int64_t v0 = t * tile_v;
+        const int64_t v_end = (v0 + tile_v < a.V) ? v0 + tile_v : a.V;
+        // chunk c covers entries [v0 + c*kVec, v0 + c*kVec + kVec); chunks are strided by the
+        // CTA so that each thread visits its entries in increasing v (strict '>' then keeps
+        // the smallest index among equal scores within the thread).
+        for (int64_t v = v0 + static_cast<int64_t>(threadIdx.x) * kVec; v < v_end;
+             v += static_cast<int64_t>(kThreads) * kVec) {
+            float y[kVec];
+            if (v + kVec <= v_end) {
+                VecLoad<T, kVec>::load(y_row + v, y);
+            } else {
+#pragma unroll
+                for (int j = 0; j < kVec; ++j) y[j] = (v + j < v_end) ? to_float<T>(y_row[v + j]) : 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) {
+                const int64_t vj = v + j;
+                if (vj < v_end) {
+                    const uint32_t vv = static_cast<uint32_t>(vj);
+                    const float bias = bias_row ? __ldg(bias_row + vj) : 0.0f;
+                    const float s = perturbed_score<kWide>(p, vv, y[j], bias, allowed(mask_row, vv));
+                    if (s > best_s) { best_s = s; best_i = static_cast<int>(vv); }
+                }
+            }
+        }
+    }
+    // Block argmax: shuffles within warps, then across the warps through shared memory.
+    warp_argmax(best_s, best_i);
+    __shared__ float sh_s[kThreads / 32];
+    __shared__ int sh_i[kThreads / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) { sh_s[warp] = best_s; sh_i[warp] = best_i; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int w = 1; w < kThreads / 32; ++w)
+            if (better(sh_s[w], sh_i[w], best_s, best_i)) { best_s = sh_s[w]; best_i = sh_i[w]; }
+        a.cand_score[b * a.n_tiles + t] = best_s;
+        a.cand_index[b * a.n_tiles + t] = candidate_index(best_s, best_i);
+    }
+    pdl_launch_dependents();
+}
+
+template <typename T, int kVec>
+cudaError_t launch_typed(const void* logits, int64_t ld, int tile_v, bool wide, const SampleArgs& a,
+                         cudaStream_t stream) {
+    const int64_t grid = a.B * a.n_tiles;
+    const T* y = static_cast<const T*>(logits);
+    if (wide) {
+        logits_stage1_kernel<T, kVec, true><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(y, ld, tile_v, a);
+    } else {
+        logits_stage1_kernel<T, kVec, false><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(y, ld, tile_v, a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_logits_stage1(const void* logits, bool bf16, int64_t ld, int tile_v, bool wide,
+                                 const SampleArgs& a, cudaStream_t stream) {
+    const size_t esize = bf16 ? 2 : 4;
+    const bool aligned = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) &&
+                         ((static_cast<size_t>(ld) * esize) % 16 == 0);
+    if (bf16) {
+        return aligned ? launch_typed<__nv_bfloat16, 8>(logits, ld, tile_v, wide, a, stream)
+                       : launch_typed<__nv_bfloat16, 1>(logits, ld, tile_v, wide, a, stream);
+    }
+    return aligned ? launch_typed<float, 4>(logits, ld, tile_v, wide, a, stream)
+                   : launch_typed<float, 1>(logits, ld, tile_v, wide, a, stream);
+}
+
+}  // namespace lms

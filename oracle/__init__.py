@@ -62,6 +62,10 @@ def _load():
             lib.orc_lmhead_sample.restype = ctypes.c_int
             lib.orc_lmhead_scores_at.argtypes = [P, i64, P, i64, i64, i64, i64, P, P, P, P, i64,
                                                  P, i64, u64, u64, i32, i64, P, P, P]
+            lib.orc_lmhead_sample_rows.argtypes = [P, i64, P, i64, i64, i64, i64, P, i64, P, P,
+                                                   P, P, i64, P, i64, u64, u64, i32, i64, P, P,
+                                                   P, P, P, P, i32]
+            lib.orc_lmhead_sample_rows.restype = ctypes.c_int
             lib.orc_uniform.argtypes = [ctypes.c_uint32, ctypes.c_uint32, i32]
             lib.orc_uniform.restype = ctypes.c_double
             _lib = lib
@@ -192,6 +196,32 @@ def lmhead_sample(H_bits, W_bits, *, temperature=None, seeds=None, positions=Non
         _ptr(H), D, _ptr(W), D, B, D, V, _ptr(T), _ptr(seeds_a), _ptr(pos_a), _ptr(bias_a),
         ld_bias, _ptr(mask_a), ld_mask, base_seed, offset, int(bool(wide)), tile_v,
         *[_ptr(o) for o in outs], threads or default_threads())
+    if rc != 0:
+        raise MemoryError("oracle could not allocate the fp64 logits")
+    return RowResult(*outs)
+
+
+def lmhead_sample_rows(H_bits, W_bits, rows, *, temperature=None, seeds=None, positions=None,
+                       bias=None, mask=None, base_seed=0, offset=0, wide=False, tile_v=128,
+                       threads=None) -> RowResult:
+    """The fused path's result for chosen batch rows of a B-row problem (each row keeps its own
+    parameters and its batch index), for sampled checks at full size."""
+    H, W = _bits16(H_bits), _bits16(W_bits)
+    B, D = H.shape
+    V = W.shape[0]
+    rows = _c(rows, np.int64)
+    n = rows.shape[0]
+    T = _c(temperature, np.float64)
+    bias_a = _c(bias, np.float64)
+    ld_bias = 0 if bias_a is None or bias_a.ndim == 1 else bias_a.shape[1]
+    mask_a = _c(mask, np.uint32)
+    ld_mask = 0 if mask_a is None or mask_a.ndim == 1 else mask_a.shape[1]
+    seeds_a, pos_a = _c(seeds, np.int64), _c(positions, np.int64)
+    outs = _row_outputs(n, V, tile_v, False)
+    rc = _load().orc_lmhead_sample_rows(
+        _ptr(H), D, _ptr(W), D, B, D, V, _ptr(rows), n, _ptr(T), _ptr(seeds_a), _ptr(pos_a),
+        _ptr(bias_a), ld_bias, _ptr(mask_a), ld_mask, base_seed, offset, int(bool(wide)), tile_v,
+        *[_ptr(o) for o in outs[:6]], threads or default_threads())
     if rc != 0:
         raise MemoryError("oracle could not allocate the fp64 logits")
     return RowResult(*outs)

@@ -168,6 +168,9 @@ typedef struct {
     int64_t* out; int32_t* status; double* top1; double* top2;
     double* tile_max; int64_t* tile_idx;   /* [B][n_tiles] when tile_v > 0 */
     double* scores;                /* optional [B][V] perturbed scores */
+    const int64_t* rows;           /* optional: evaluate only these batch rows; output slot i and
+                                      y row i belong to batch row rows[i] (n_rows of them) */
+    int64_t n_rows;
 } orc_rows_args;
 
 /* Perturbed score s for row b, column v, given the (untransformed) logit y. */
@@ -194,24 +197,26 @@ static double orc_score(const orc_rows_args* a, int64_t b, int64_t v, double y) 
     return s;
 }
 
-static void orc_one_row(const orc_rows_args* a, int64_t b, const double* yrow) {
+/* Row b of the batch, its logits yrow, its outputs at slot o (o == b unless a subset of rows
+ * is evaluated). */
+static void orc_one_row(const orc_rows_args* a, int64_t b, int64_t o, const double* yrow) {
     int64_t V = a->V;
     double T = a->T ? a->T[b] : 1.0;
     int64_t nt = a->tile_v > 0 ? (V + a->tile_v - 1) / a->tile_v : 0;
     if (isnan(T) || T < 0.0) {                 /* invalid temperature: rejected per row */
-        a->out[b] = -1; a->status[b] = 2;
-        if (a->top1) a->top1[b] = -INFINITY;
-        if (a->top2) a->top2[b] = -INFINITY;
-        for (int64_t t = 0; t < nt; ++t) { a->tile_max[b * nt + t] = -INFINITY; a->tile_idx[b * nt + t] = -1; }
-        if (a->scores) for (int64_t v = 0; v < V; ++v) a->scores[b * V + v] = -INFINITY;
+        a->out[o] = -1; a->status[o] = 2;
+        if (a->top1) a->top1[o] = -INFINITY;
+        if (a->top2) a->top2[o] = -INFINITY;
+        for (int64_t t = 0; t < nt; ++t) { a->tile_max[o * nt + t] = -INFINITY; a->tile_idx[o * nt + t] = -1; }
+        if (a->scores) for (int64_t v = 0; v < V; ++v) a->scores[o * V + v] = -INFINITY;
         return;
     }
     double best = -INFINITY, second = -INFINITY;
     int64_t arg = -1;
-    for (int64_t t = 0; t < nt; ++t) { a->tile_max[b * nt + t] = -INFINITY; a->tile_idx[b * nt + t] = -1; }
+    for (int64_t t = 0; t < nt; ++t) { a->tile_max[o * nt + t] = -INFINITY; a->tile_idx[o * nt + t] = -1; }
     for (int64_t v = 0; v < V; ++v) {
         double s = orc_score(a, b, v, yrow[v]);
-        if (a->scores) a->scores[b * V + v] = s;
+        if (a->scores) a->scores[o * V + v] = s;
         if (s > -INFINITY) {
             if (arg < 0 || s > best) {         /* strict '>' keeps the smallest index on ties */
                 second = best; best = s; arg = v;
@@ -220,36 +225,40 @@ static void orc_one_row(const orc_rows_args* a, int64_t b, const double* yrow) {
             }
             if (nt > 0) {
                 int64_t t = v / a->tile_v;
-                if (a->tile_idx[b * nt + t] < 0 || s > a->tile_max[b * nt + t]) {
-                    a->tile_max[b * nt + t] = s; a->tile_idx[b * nt + t] = v;
+                if (a->tile_idx[o * nt + t] < 0 || s > a->tile_max[o * nt + t]) {
+                    a->tile_max[o * nt + t] = s; a->tile_idx[o * nt + t] = v;
                 }
             }
         }
     }
-    a->out[b] = arg;
-    a->status[b] = arg < 0 ? 1 : 0;
-    if (a->top1) a->top1[b] = best;
-    if (a->top2) a->top2[b] = second;
+    a->out[o] = arg;
+    a->status[o] = arg < 0 ? 1 : 0;
+    if (a->top1) a->top1[o] = best;
+    if (a->top2) a->top2[o] = second;
 }
 
 typedef struct { const orc_rows_args* a; int64_t b0, b1; } orc_rows_job;
 
 static void* orc_rows_worker(void* p) {
     const orc_rows_job* j = (const orc_rows_job*)p;
-    for (int64_t b = j->b0; b < j->b1; ++b) orc_one_row(j->a, b, j->a->y + b * j->a->ld_y);
+    for (int64_t i = j->b0; i < j->b1; ++i) {
+        int64_t b = j->a->rows ? j->a->rows[i] : i;
+        orc_one_row(j->a, b, i, j->a->y + i * j->a->ld_y);
+    }
     return NULL;
 }
 
 static void orc_run_rows(const orc_rows_args* a, int nthreads) {
+    int64_t n = a->rows ? a->n_rows : a->B;
     if (nthreads < 1) nthreads = 1;
-    if (nthreads > a->B) nthreads = (int)(a->B > 0 ? a->B : 1);
+    if (nthreads > n) nthreads = (int)(n > 0 ? n : 1);
     pthread_t th[256];
     orc_rows_job jobs[256];
     if (nthreads > 256) nthreads = 256;
     for (int i = 0; i < nthreads; ++i) {
         jobs[i].a = a;
-        jobs[i].b0 = a->B * i / nthreads;
-        jobs[i].b1 = a->B * (i + 1) / nthreads;
+        jobs[i].b0 = n * i / nthreads;
+        jobs[i].b1 = n * (i + 1) / nthreads;
         pthread_create(&th[i], NULL, orc_rows_worker, &jobs[i]);
     }
     for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
@@ -264,7 +273,7 @@ void orc_sample_from_logits(const double* y, int64_t ld_y, int64_t B, int64_t V,
                             double* tile_max, int64_t* tile_idx, double* scores, int nthreads) {
     orc_rows_args a = {y, ld_y, B, V, T, seeds, positions, bias, ld_bias, mask, ld_mask,
                        base_seed, offset, wide, tile_v, out, status, top1, top2,
-                       tile_max, tile_idx, scores};
+                       tile_max, tile_idx, scores, NULL, 0};
     orc_run_rows(&a, nthreads);
 }
 
@@ -283,6 +292,7 @@ static double orc_bf16(uint16_t h) {
 typedef struct {
     const uint16_t* H; int64_t ldh; const uint16_t* W; int64_t ldw;
     int64_t B, D, V; double* y; int64_t v0, v1;
+    const int64_t* rows;   /* NULL: all B rows; else y row i is H row rows[i] (B of them) */
 } orc_gemm_job;
 
 static void* orc_gemm_worker(void* p) {
@@ -291,29 +301,35 @@ static void* orc_gemm_worker(void* p) {
     double* wrow = (double*)malloc(sizeof(double) * (size_t)j->D);
     for (int64_t v = j->v0; v < j->v1; ++v) {
         for (int64_t d = 0; d < j->D; ++d) wrow[d] = orc_bf16(j->W[v * j->ldw + d]);
-        for (int64_t b = 0; b < j->B; ++b) {
+        for (int64_t i = 0; i < j->B; ++i) {
+            int64_t b = j->rows ? j->rows[i] : i;
             double acc = 0.0;
             for (int64_t d = 0; d < j->D; ++d) acc += orc_bf16(j->H[b * j->ldh + d]) * wrow[d];
-            j->y[b * j->V + v] = acc;
+            j->y[i * j->V + v] = acc;
         }
     }
     free(hrow); free(wrow);
     return NULL;
 }
 
-/* y [B][V] = sum_d H[b][d] * W[v][d], accumulated in fp64 in increasing d. */
-void orc_lmhead_logits(const uint16_t* H, int64_t ldh, const uint16_t* W, int64_t ldw, int64_t B,
-                       int64_t D, int64_t V, double* y, int nthreads) {
+static void orc_gemm(const uint16_t* H, int64_t ldh, const uint16_t* W, int64_t ldw, int64_t B,
+                     int64_t D, int64_t V, double* y, const int64_t* rows, int nthreads) {
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;
     pthread_t th[256];
     orc_gemm_job jobs[256];
     for (int i = 0; i < nthreads; ++i) {
-        orc_gemm_job j = {H, ldh, W, ldw, B, D, V, y, V * i / nthreads, V * (i + 1) / nthreads};
+        orc_gemm_job j = {H, ldh, W, ldw, B, D, V, y, V * i / nthreads, V * (i + 1) / nthreads, rows};
         jobs[i] = j;
         pthread_create(&th[i], NULL, orc_gemm_worker, &jobs[i]);
     }
     for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+}
+
+/* y [B][V] = sum_d H[b][d] * W[v][d], accumulated in fp64 in increasing d. */
+void orc_lmhead_logits(const uint16_t* H, int64_t ldh, const uint16_t* W, int64_t ldw, int64_t B,
+                       int64_t D, int64_t V, double* y, int nthreads) {
+    orc_gemm(H, ldh, W, ldw, B, D, V, y, NULL, nthreads);
 }
 
 /* The fused path's result: logits in fp64, then the same per-row race. */
@@ -326,7 +342,7 @@ int orc_lmhead_sample(const uint16_t* H, int64_t ldh, const uint16_t* W, int64_t
                       int nthreads) {
     double* y = (double*)malloc(sizeof(double) * (size_t)(B * V));
     if (!y) return 1;
-    orc_lmhead_logits(H, ldh, W, ldw, B, D, V, y, nthreads);
+    orc_gemm(H, ldh, W, ldw, B, D, V, y, NULL, nthreads);
     orc_sample_from_logits(y, V, B, V, T, seeds, positions, bias, ld_bias, mask, ld_mask,
                            base_seed, offset, wide, tile_v, out, status, top1, top2, tile_max,
                            tile_idx, scores, nthreads);
@@ -344,7 +360,8 @@ void orc_lmhead_scores_at(const uint16_t* H, int64_t ldh, const uint16_t* W, int
                           uint64_t offset, int wide, int64_t n, const int64_t* bs,
                           const int64_t* vs, double* s_out) {
     orc_rows_args a = {NULL, 0, B, V, T, seeds, positions, bias, ld_bias, mask, ld_mask,
-                       base_seed, offset, wide, 0, NULL, NULL, NULL, NULL, NULL, NULL, NULL};
+                       base_seed, offset, wide, 0, NULL, NULL, NULL, NULL, NULL, NULL, NULL,
+                       NULL, 0};
     for (int64_t i = 0; i < n; ++i) {
         int64_t b = bs[i], v = vs[i];
         double Tb = T ? T[b] : 1.0;
@@ -353,4 +370,25 @@ void orc_lmhead_scores_at(const uint16_t* H, int64_t ldh, const uint16_t* W, int
         for (int64_t d = 0; d < D; ++d) acc += orc_bf16(H[b * ldh + d]) * orc_bf16(W[v * ldw + d]);
         s_out[i] = orc_score(&a, b, v, acc);
     }
+}
+
+/* The fused path's result for a subset of the batch: rows[i] (i < n_rows) are batch rows of the
+ * full B-row problem (their own temperature, seed, position, bias and mask rows, and row index
+ * for unseeded keys); outputs are [n_rows] / [n_rows][n_tiles]. */
+int orc_lmhead_sample_rows(const uint16_t* H, int64_t ldh, const uint16_t* W, int64_t ldw,
+                           int64_t B, int64_t D, int64_t V, const int64_t* rows, int64_t n_rows,
+                           const double* T, const int64_t* seeds, const int64_t* positions,
+                           const double* bias, int64_t ld_bias, const uint32_t* mask,
+                           int64_t ld_mask, uint64_t base_seed, uint64_t offset, int wide,
+                           int64_t tile_v, int64_t* out, int32_t* status, double* top1,
+                           double* top2, double* tile_max, int64_t* tile_idx, int nthreads) {
+    double* y = (double*)malloc(sizeof(double) * (size_t)(n_rows * V));
+    if (!y) return 1;
+    orc_gemm(H, ldh, W, ldw, n_rows, D, V, y, rows, nthreads);
+    orc_rows_args a = {y, V, B, V, T, seeds, positions, bias, ld_bias, mask, ld_mask,
+                       base_seed, offset, wide, tile_v, out, status, top1, top2,
+                       tile_max, tile_idx, NULL, rows, n_rows};
+    orc_run_rows(&a, nthreads);
+    free(y);
+    return 0;
 }

@@ -1,0 +1,117 @@
+"""The C ABI without a GPU: the library loads, exports every function include/lms.h declares,
+and rejects bad arguments on the host before anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import lm_head_gumbel_lmhead_gb300 as lms
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "lms.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lms_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from lm_head_gumbel_lmhead_gb300 import build
+    build.build()
+    return lms.lib()
+
+
+def test_every_declared_function_is_exported(L):
+    names = _declared()
+    assert "lms_lmhead_sample" in names and "lms_sample_from_logits" in names
+    assert "lms_philox_fill_noise" in names
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in lms.h but not exported"
+
+
+def test_version_and_empty_error(L):
+    assert lms.version().startswith("lms")
+
+
+def test_params_struct_matches_header_size(L):
+    # pointers/int64 x9, 4 x int32, pointer, 2 x uint32 = 72 + 16 + 8 + 8
+    assert ctypes.sizeof(lms.SampleParams) == 104
+
+
+def test_tile_info(L):
+    tv, nt, ws, path = lms.tile_info(lms.OP_LMHEAD, 64, 4096, 151936)
+    assert tv == 128 and nt == 1187 and path == lms.PATH_TCGEN05
+    cand = 64 * 1187 * 4
+    assert ws == 2 * ((cand + 255) // 256 * 256)
+    assert lms.tile_info(lms.OP_LMHEAD, 1, 4096, 151936)[3] == lms.PATH_GEMV
+    tv, nt, _, _ = lms.tile_info(lms.OP_LOGITS, 8192, 0, 131072)
+    assert tv == 8192 and nt == 16
+    tv, nt, _, _ = lms.tile_info(lms.OP_LOGITS, 1, 0, 131072)
+    assert tv == 1024 and nt == 128
+    assert lms.tile_info(lms.OP_LOGITS, 3, 0, 1000, 256)[:2] == (256, 4)
+    assert lms.workspace_bytes(lms.OP_LMHEAD, 0, 4096, 100) == 0
+
+
+@pytest.mark.parametrize("args,status", [
+    ((lms.OP_LMHEAD, 0, 64, 100, 0), lms.LMS_ERR_INVALID_ARG),
+    ((lms.OP_LMHEAD, 4, 0, 100, 0), lms.LMS_ERR_INVALID_ARG),
+    ((lms.OP_LMHEAD, 4, 64, 2**31, 0), lms.LMS_ERR_INVALID_ARG),
+    ((lms.OP_LMHEAD, 4, 64, 100, 64), lms.LMS_ERR_UNSUPPORTED),
+    ((lms.OP_LOGITS, 4, 0, 100, 300), lms.LMS_ERR_UNSUPPORTED),
+    ((lms.OP_LOGITS, 4, 0, 100, 128), lms.LMS_ERR_UNSUPPORTED),
+    ((7, 4, 0, 100, 0), lms.LMS_ERR_INVALID_ARG),
+])
+def test_tile_info_rejects(L, args, status):
+    with pytest.raises(lms.LmsError) as e:
+        lms.tile_info(*args)
+    assert e.value.status == status
+
+
+def _params(**kw):
+    p = lms.SampleParams()
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+FAKE = ctypes.c_void_p(0x100000)   # a 16-byte aligned non-null address; never dereferenced
+
+
+@pytest.mark.parametrize("kw,call_kw,status", [
+    (dict(), dict(H=None), lms.LMS_ERR_INVALID_ARG),
+    (dict(noise_mode=5), dict(), lms.LMS_ERR_INVALID_ARG),
+    (dict(seeds=0x1000), dict(), lms.LMS_ERR_INVALID_ARG),           # seeds without positions
+    (dict(reserved=1), dict(), lms.LMS_ERR_INVALID_ARG),
+    (dict(debug_flags=8), dict(), lms.LMS_ERR_INVALID_ARG),
+    (dict(bias=0x1000, ld_bias=10), dict(), lms.LMS_ERR_INVALID_ARG),
+    (dict(), dict(D=60), lms.LMS_ERR_UNSUPPORTED),                    # D % 8 != 0
+    (dict(), dict(ldh=70), lms.LMS_ERR_UNSUPPORTED),
+    (dict(), dict(H=ctypes.c_void_p(0x100008)), lms.LMS_ERR_UNSUPPORTED),
+    (dict(), dict(ws_bytes=16), lms.LMS_ERR_WORKSPACE),
+    (dict(path=lms.PATH_GEMV), dict(B=9), lms.LMS_ERR_UNSUPPORTED),
+    (dict(path=9), dict(), lms.LMS_ERR_INVALID_ARG),
+])
+def test_lmhead_host_validation(L, kw, call_kw, status):
+    c = dict(H=FAKE, ldh=64, W=FAKE, ldw=64, B=4, D=64, V=1000, out=FAKE, ws=FAKE, ws_bytes=1 << 20)
+    c.update(call_kw)
+    p = _params(**kw)
+    st = L.lms_lmhead_sample(c["H"], c["ldh"], c["W"], c["ldw"], c["B"], c["D"], c["V"],
+                             ctypes.byref(p), c["out"], c["ws"], c["ws_bytes"], None)
+    assert st == status, L.lms_last_error()
+    assert L.lms_last_error()
+
+
+def test_logits_and_noise_host_validation(L):
+    p = _params()
+    assert L.lms_sample_from_logits(FAKE, 7, 0, 4, 100, ctypes.byref(p), FAKE, FAKE, 1 << 20, None) == lms.LMS_ERR_INVALID_ARG
+    assert L.lms_sample_from_logits(FAKE, 0, 50, 4, 100, ctypes.byref(p), FAKE, FAKE, 1 << 20, None) == lms.LMS_ERR_INVALID_ARG
+    assert L.lms_sample_from_logits(FAKE, 0, 0, 4, 100, ctypes.byref(p), FAKE, FAKE, 8, None) == lms.LMS_ERR_WORKSPACE
+    p2 = _params(debug_flags=1)
+    assert L.lms_sample_from_logits(FAKE, 0, 0, 4, 100, ctypes.byref(p2), FAKE, FAKE, 1 << 20, None) == lms.LMS_ERR_INVALID_ARG
+    assert L.lms_philox_fill_noise(None, 0, 0, 4, 100, None, None, 0, 0, None) == lms.LMS_ERR_INVALID_ARG
+    assert L.lms_philox_fill_noise(FAKE, 9, 0, 4, 100, None, None, 0, 0, None) == lms.LMS_ERR_INVALID_ARG
+    assert L.lms_philox_fill_noise(FAKE, 0, 0, 0, 100, None, None, 0, 0, None) == lms.LMS_ERR_INVALID_ARG
+    assert L.lms_philox_fill_noise(ctypes.c_void_p(0x100008), 0, 0, 4, 100, None, None, 0, 0, None) == lms.LMS_ERR_UNSUPPORTED

@@ -1,0 +1,65 @@
+"""Host-side logic of bench.py: the max-over-ranks reduction across replicas (gloo, world size
+2, CPU), the reference arm's JSON line, and the algorithmic byte count."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE="2", LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    import torch.distributed as dist
+    bench.init_dist("gloo")
+    v = bench.max_over_ranks(10.0 + 5 * rank)
+    bench.barrier()
+    q.put((rank, v))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_worker, args=(r, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in ps)
+    for p in ps:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == {0: 15.0, 1: 15.0}
+
+
+def test_reference_arm_prints_contract_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3", "--batch", "4", "--D", "256", "--V", "4096",
+                        "--ref-vslice", "1024"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "us/step" and line["value"] > 0
+    assert line["higher_is_better"] is False
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_algorithmic_bytes_qwen_b64():
+    sys.path.insert(0, ROOT)
+    import bench
+    b = bench.algorithmic_bytes(64, 4096, 151936, 1187)
+    assert b == 151936 * 4096 * 2 + 64 * 4096 * 2 + 2 * 64 * 1187 * 8 + 64 * 28
+    assert abs(b / 1e9 - 1.2464) < 1e-3

@@ -1,0 +1,197 @@
+"""sample_from_logits on the GPU against the oracle, and the laws the pages fix:
+  * parity (indices, statuses, per-tile candidates) on fp32 and bf16 logits, ragged tiles,
+    bias, masks, greedy / invalid rows, seeded and unseeded rows, both noise modes;
+  * the tail rate on the Megatron-LM PR's rows [0, -D, ..., -D], V = 131072, against the
+    closed form inside the two-sided 1e-6 Poisson interval ("Tests"), wide noise at
+    r = 1e-7 / 1e-8 / 1e-9; fp32 noise falls below the interval at r = 1e-9 (non-vacuity);
+  * chi-square on a 16-token row (1M draws, 15 dof) for both modes, seeded and unseeded;
+  * seeded draws are invariant to batch position.
+"""
+import numpy as np
+import pytest
+import torch
+from scipy import stats
+
+import lm_head_gumbel_lmhead_gb300 as lms
+import oracle
+from lm_head_gumbel_lmhead_gb300 import workloads
+from parity import check_rows, check_tiles
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda")
+
+
+def run_gpu(logits, B=None, tile_v=0, **kw):
+    dev_kw = {k: (torch.from_numpy(np.ascontiguousarray(v)).to(DEV) if isinstance(v, np.ndarray) else v)
+              for k, v in kw.items()}
+    if "temperature" in dev_kw and dev_kw["temperature"] is not None:
+        dev_kw["temperature"] = dev_kw["temperature"].float()
+    if "bias" in dev_kw and dev_kw["bias"] is not None:
+        dev_kw["bias"] = dev_kw["bias"].float()
+    if "mask" in dev_kw and dev_kw["mask"] is not None:
+        dev_kw["mask"] = dev_kw["mask"].view(torch.int32) if dev_kw["mask"].dtype == torch.int32 else \
+            dev_kw["mask"].to(torch.int64).to(torch.int32)
+    Bn = B if B is not None else logits.shape[0]
+    V = logits.shape[-1]
+    tv, nt, ws_bytes, _ = lms.tile_info(lms.OP_LOGITS, Bn, 0, V, tile_v)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=DEV)
+    status = torch.empty(Bn, dtype=torch.int32, device=DEV)
+    out = lms.sample_from_logits(logits, B=B, tile_v=tile_v, workspace=ws, row_status=status, **dev_kw)
+    torch.cuda.synchronize()
+    cs, ci = lms.split_workspace(ws, Bn, nt)
+    return out.cpu().numpy(), status.cpu().numpy(), cs.cpu().numpy(), ci.cpu().numpy(), tv
+
+
+def oracle_kw(kw):
+    o = dict(kw)
+    if o.get("mask") is not None:
+        o["mask"] = np.asarray(o["mask"]).view(np.uint32)
+    return o
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("wide", [False, True])
+@pytest.mark.parametrize("tile_v", [0, 256, 2048])
+def test_parity_mixed_rows(dtype, wide, tile_v):
+    rng = np.random.default_rng(1)
+    B, V = 23, 5003
+    logits = workloads.logits_normal(B, V, std=2.0, seed=3, dtype=dtype)
+    y64 = logits.double().numpy()
+    T = rng.uniform(0.3, 1.5, B).astype(np.float32)
+    T[[0, 9]] = 0.0          # greedy
+    T[4] = -1.0              # invalid
+    T[7] = np.nan            # invalid
+    seeds = (np.arange(B) * 31 + 7).astype(np.int64)
+    seeds[[2, 11, 12, 20]] = -1
+    pos = (np.arange(B) * 1001).astype(np.int64)
+    bias = (rng.standard_normal((B, V)) * 0.5).astype(np.float32)
+    bias[3, :100] = -np.inf
+    allowed = rng.random((B, V)) < 0.4
+    allowed[5] = False       # all masked
+    allowed[:B // 2] = True
+    allowed[5] = False
+    mask = workloads.pack_allow_bits(torch.from_numpy(allowed)).numpy()
+    kw = dict(temperature=T, seeds=seeds, positions=pos, bias=bias, mask=mask, base_seed=99,
+              offset=5, wide=wide)
+    out, st, cs, ci, tv = run_gpu(logits.to(DEV), tile_v=tile_v, **kw)
+    orc = oracle.sample_from_logits(y64, tile_v=tv, want_scores=True,
+                                    **oracle_kw({**kw, "temperature": T.astype(np.float64),
+                                                 "bias": bias.astype(np.float64)}))
+    score_of = lambda i, v: orc.scores[i, v]
+    check_rows(out, st, orc, score_of)
+    check_tiles(cs, ci, orc, score_of)
+    assert list(st[[4, 5, 7]]) == [2, 1, 2]
+
+
+def test_broadcast_row_and_unaligned_rows():
+    V = 1537
+    row = workloads.logits_normal(1, V, seed=9)[0]
+    B = 300
+    seeds = np.arange(B, dtype=np.int64)
+    out, st, _, _, _ = run_gpu(row.to(DEV), B=B, seeds=seeds, positions=seeds * 3)
+    orc = oracle.sample_from_logits(row.double().numpy(), B=B, seeds=seeds, positions=seeds * 3,
+                                    want_scores=True)
+    check_rows(out, st, orc, lambda i, v: orc.scores[i, v])
+    # rows whose stride breaks 16-byte alignment take the scalar-load kernel
+    big = workloads.logits_normal(7, V + 1, seed=10).to(DEV)
+    sub = big[:, 1:]
+    out2, st2, _, _, _ = run_gpu(sub, base_seed=4)
+    orc2 = oracle.sample_from_logits(sub.double().cpu().numpy(), base_seed=4, want_scores=True)
+    check_rows(out2, st2, orc2, lambda i, v: orc2.scores[i, v])
+
+
+def _miss_interval(V, r, draws):
+    p = (V - 1) * r / (1 + (V - 1) * r)
+    mu = draws * p
+    return mu, stats.poisson.ppf(5e-7, mu), stats.poisson.isf(5e-7, mu)
+
+
+def _tail_misses(r, draws, wide, seeded, chunk=8192, V=131072):
+    row = workloads.tail_row(V, r).to(DEV)
+    misses = 0
+    done = 0
+    ci = 0
+    while done < draws:
+        n = min(chunk, draws - done)
+        if seeded:
+            seeds = torch.full((n,), 1234, dtype=torch.int64, device=DEV)
+            pos = torch.arange(done, done + n, dtype=torch.int64, device=DEV)
+            out = lms.sample_from_logits(row, B=n, seeds=seeds, positions=pos, wide=wide)
+        else:
+            out = lms.sample_from_logits(row, B=n, base_seed=1234, offset=ci, wide=wide)
+        misses += int((out != 0).sum().item())
+        done += n
+        ci += 1
+    return misses
+
+
+@pytest.mark.parametrize("seeded", [True, False])
+@pytest.mark.parametrize("r,draws", [(1e-7, 200_000), (1e-8, 1_000_000), (1e-9, 1_000_000),
+                                     (1e-9, 262_144)])
+def test_wide_noise_tail_rate(r, draws, seeded):
+    misses = _tail_misses(r, draws, True, seeded)
+    mu, lo, hi = _miss_interval(131072, r, draws)
+    assert lo <= misses <= hi, (misses, mu, lo, hi)
+
+
+@pytest.mark.parametrize("seeded", [True, False])
+def test_fp32_noise_misses_the_far_tail(seeded):
+    misses = _tail_misses(1e-9, 262_144, False, seeded)
+    mu, lo, hi = _miss_interval(131072, 1e-9, 262_144)
+    assert misses < lo, (misses, mu, lo)
+
+
+def test_tail_draws_match_oracle():
+    V, r, n = 131072, 1e-7, 24
+    row = workloads.tail_row(V, r)
+    seeds = np.full(n, 1234, np.int64)
+    pos = np.arange(n, dtype=np.int64) * 5003
+    for wide in (False, True):
+        out, st, _, _, _ = run_gpu(row.to(DEV), B=n, seeds=seeds, positions=pos, wide=wide)
+        orc = oracle.sample_from_logits(row.double().numpy(), B=n, seeds=seeds, positions=pos,
+                                        wide=wide, want_scores=True)
+        check_rows(out, st, orc, lambda i, v: orc.scores[i, v])
+
+
+ROW16 = np.array([1.2, -0.3, 0.0, 2.1, -1.7, 0.4, 0.9, -2.5, 1.6, -0.8, 0.05, 1.1, -1.2, 0.7,
+                  -0.1, 0.3], np.float32)
+
+
+@pytest.mark.parametrize("wide", [False, True])
+@pytest.mark.parametrize("seeded", [True, False])
+def test_chi_square_16_tokens(wide, seeded):
+    n = 1_000_000
+    row = torch.from_numpy(ROW16).to(DEV)
+    if seeded:
+        out = lms.sample_from_logits(row, B=n, seeds=torch.full((n,), 1234, dtype=torch.int64, device=DEV),
+                                     positions=torch.arange(n, device=DEV), wide=wide)
+    else:
+        out = lms.sample_from_logits(row, B=n, base_seed=1234, offset=3, wide=wide)
+    counts = np.bincount(out.cpu().numpy(), minlength=16).astype(np.float64)
+    p = np.exp(ROW16.astype(np.float64) - ROW16.max())
+    p /= p.sum()
+    stat = ((counts - n * p) ** 2 / (n * p)).sum()
+    assert stat < stats.chi2.isf(1e-6, 15)
+
+
+@pytest.mark.parametrize("wide", [False, True])
+def test_seeded_rows_batch_position_invariant(wide):
+    B, V = 16, 20_000
+    logits = workloads.logits_normal(B, V, seed=12).to(DEV)
+    T = torch.full((B,), 0.7, device=DEV)
+    seeds = torch.arange(B, dtype=torch.int64, device=DEV) + 100
+    seeds[1::3] = -1
+    pos = torch.arange(B, dtype=torch.int64, device=DEV) * 7
+    full = lms.sample_from_logits(logits, temperature=T, seeds=seeds, positions=pos, wide=wide, base_seed=5)
+    perm = torch.randperm(B, generator=torch.Generator().manual_seed(0)).to(DEV)
+    pr = lms.sample_from_logits(logits[perm].contiguous(), temperature=T[perm].contiguous(),
+                                seeds=seeds[perm].contiguous(), positions=pos[perm].contiguous(),
+                                wide=wide, base_seed=5)
+    seeded = (seeds[perm] >= 0)
+    assert torch.equal(pr[seeded], full[perm][seeded])
+    for b in range(0, B, 3):
+        one = lms.sample_from_logits(logits[b:b + 1], temperature=T[b:b + 1], seeds=seeds[b:b + 1],
+                                     positions=pos[b:b + 1], wide=wide)
+        assert one.item() == full[b].item()
+    again = lms.sample_from_logits(logits, temperature=T, seeds=seeds, positions=pos, wide=wide, base_seed=5)
+    assert torch.equal(again, full)

@@ -226,3 +226,25 @@ def test_seeded_rows_are_batch_position_invariant():
     outs = {int(oracle.sample_from_logits(np.zeros(V), B=1, base_seed=3, offset=o).out[0])
             for o in range(8)}
     assert len(outs) > 4
+
+
+def test_row_subset_equals_full_batch():
+    rng = np.random.default_rng(10)
+    B, D, V = 9, 64, 700
+    H = torch.from_numpy(rng.standard_normal((B, D)).astype(np.float32)).to(torch.bfloat16)
+    W = torch.from_numpy(rng.standard_normal((V, D)).astype(np.float32)).to(torch.bfloat16)
+    T = rng.uniform(0.3, 1.2, B); T[2] = 0.0
+    seeds = np.arange(B) + 50; seeds[[1, 5]] = -1
+    pos = np.arange(B) * 3
+    bias = rng.standard_normal((B, V))
+    allowed = rng.random((B, V)) < 0.5
+    mask = workloads.pack_allow_bits(torch.from_numpy(allowed)).numpy().view(np.uint32)
+    kw = dict(temperature=T, seeds=seeds, positions=pos, bias=bias, mask=mask, base_seed=8,
+              offset=2, wide=True)
+    full = oracle.lmhead_sample(H, W, tile_v=128, **kw)
+    rows = np.array([7, 1, 5, 2])
+    sub = oracle.lmhead_sample_rows(H, W, rows, tile_v=128, **kw)
+    assert (sub.out == full.out[rows]).all()
+    assert (sub.status == full.status[rows]).all()
+    assert (sub.tile_idx == full.tile_idx[rows]).all()
+    assert np.array_equal(sub.tile_max, full.tile_max[rows])
