@@ -151,6 +151,23 @@ lms_status lms_sample_from_logits(const void* logits, int32_t dtype, int64_t ld,
                                   int64_t V, const lms_sample_params* params, int64_t* out,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
+/* Allocation-free variant of lms_lmhead_sample for callers that cannot allocate device memory:
+ * code that runs inside a device-memory allocator or a pool's callback, code that must not take
+ * the allocator's lock, or an embedding that hands this library only fixed buffers.  The pages
+ * have no counterpart of this call; it changes where the scratch lives, not what is computed.
+ * Arguments and results are those of lms_lmhead_sample without the workspace: the Stage-1
+ * candidates go to a 4 MiB file-scope device array that is part of the library image (every
+ * GPU that loads the library holds it until the process exits), so B * ceil(V / 128) must be
+ * <= 524288; larger calls return LMS_ERR_WORKSPACE before any launch.  Calls no cudaMalloc,
+ * cudaFree or allocating library routine.  The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress, with that device current): make that first call before
+ * any stream capture.  Every call shares the array and leaves its candidates in it; nothing in
+ * it has to start at zero (each call writes every candidate it reads), but calls whose kernels
+ * overlap on the GPU (concurrent streams or threads) race on it: serialise them. */
+lms_status lms_lmhead_sample_noalloc(const void* H, int64_t ldh, const void* W, int64_t ldw,
+                                     int64_t B, int64_t D, int64_t V,
+                                     const lms_sample_params* params, int64_t* out, void* stream);
+
 /* Noise grid [B][V] as the sampling kernels compute it, for testing and debugging
  * (Megatron-LM PR 8370, "Tests": the noise replays bit-exactly; the words are the bit-exact
  * surface).  kind selects the output (lms_noise_kind; element sizes 16, 8, 4, 4 bytes);

@@ -89,6 +89,9 @@ def lib() -> ctypes.CDLL:
             L.lms_sample_from_logits.argtypes = [P, i32, i64, i64, i64, ctypes.POINTER(SampleParams),
                                                  P, P, sz, P]
             L.lms_sample_from_logits.restype = i32
+            L.lms_lmhead_sample_noalloc.argtypes = [P, i64, P, i64, i64, i64, i64,
+                                                    ctypes.POINTER(SampleParams), P, P]
+            L.lms_lmhead_sample_noalloc.restype = i32
             L.lms_philox_fill_noise.argtypes = [P, i32, i32, i64, i64, P, P, u64, u64, P]
             L.lms_philox_fill_noise.restype = i32
             _lib = L
@@ -215,6 +218,29 @@ def lmhead_sample(H: torch.Tensor, W: torch.Tensor, *, temperature=None, seeds=N
     _check(lib().lms_lmhead_sample(_ptr(H), H.stride(0), _ptr(W), W.stride(0), B, D, V,
                                    ctypes.byref(p), _ptr(out), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def lmhead_sample_noalloc(H: torch.Tensor, W: torch.Tensor, *, temperature=None, seeds=None,
+                          positions=None, bias=None, mask=None, base_seed: int = 0,
+                          offset: int = 0, wide: bool = False, path: int = PATH_AUTO, out=None,
+                          row_status=None, stream=None) -> torch.Tensor:
+    """lmhead_sample without a workspace, for callers that cannot allocate device memory: the
+    Stage-1 candidates go to the library's fixed 4 MiB device array (B * ceil(V/128) <= 524288).
+    Calls that overlap on the GPU share that array and race; serialise them.  `out` (and
+    `row_status`) are still the caller's: pass preallocated tensors to allocate nothing."""
+    if H.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise TypeError("H and W must be bfloat16")
+    if H.dim() != 2 or W.dim() != 2 or H.shape[1] != W.shape[1] or W.device != H.device:
+        raise ValueError("H must be [B, D] and W [V, D] on one device")
+    B, D = H.shape
+    V = W.shape[0]
+    p = _params(B, H.device, temperature, seeds, positions, bias, mask, base_seed, offset, wide, 0,
+                path, row_status, 0, 0)
+    if out is None:
+        out = torch.empty(B, dtype=torch.int64, device=H.device)
+    _check(lib().lms_lmhead_sample_noalloc(_ptr(H), H.stride(0), _ptr(W), W.stride(0), B, D, V,
+                                           ctypes.byref(p), _ptr(out), _stream(stream)))
     return out
 
 

@@ -162,6 +162,8 @@ lms_status encode_bf16_map(CUtensorMap* tm, const void* ptr, int64_t rows, int64
 }  // namespace
 
 namespace lms {
+void set_last_error(const char* msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+
 int device_sm_count() {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;

@@ -48,4 +48,7 @@ cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int
 
 int device_sm_count();
 
+// Sets the thread-local message that lms_last_error() returns.
+void set_last_error(const char* msg);
+
 }  // namespace lms
