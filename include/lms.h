@@ -69,7 +69,7 @@ typedef enum {
 } lms_noise_kind;
 typedef enum { LMS_OP_LMHEAD = 0, LMS_OP_LOGITS = 1 } lms_op;
 typedef enum {
-    LMS_PATH_AUTO = 0,            /* pick by batch size                                        */
+    LMS_PATH_AUTO = 0,            /* the library's choice (currently tcgen05 for every B)      */
     LMS_PATH_GEMV = 1,            /* CUDA-core dot products (B <= LMS_GEMV_MAX_B)                */
     LMS_PATH_TCGEN05 = 2          /* TMA -> shared memory -> tcgen05.mma -> TMEM accumulators  */
 } lms_path;

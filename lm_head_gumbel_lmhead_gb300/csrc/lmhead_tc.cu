@@ -11,10 +11,11 @@
 //   warp 1      allocates TMEM; one lane issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32) with
 //               "swap-AB": M = 128 vocabulary rows of W, N = n_pad batch rows of H, K = 16 per
 //               instruction, into one of two TMEM accumulators [128 lanes x n_pad columns].
-//   warps 2..   epilogue (4 or 8 warps): tcgen05.ld the accumulator (thread = one vocabulary row,
+//   warps 2..   epilogue (kEpilogueWarps, a multiple of 4): tcgen05.ld the accumulator (thread = one vocabulary row,
 //               registers = batch columns), apply bias / mask / temperature, run Philox and the
-//               noise per element, reduce the argmax over the 128 rows with warp shuffles and
-//               shared memory, write one candidate per batch row.
+//               noise per element, reduce the argmax over the 128 rows (16 columns at a time
+//               across the 32 lanes, then across the 4 lane quadrants in shared memory), write
+//               one candidate per batch row.
 // The double-buffered accumulator lets the epilogue of tile i overlap the loads and MMAs of
 // tile i+1.  Every mbarrier wait is bounded in time; a CTA whose wait runs out flags the error,
 // drains its in-flight copies and MMAs, poisons its remaining candidates (index -2, reported
@@ -32,6 +33,13 @@ constexpr int kTileV = 128;                       // tcgen05 M
 constexpr int kBK = 64;                           // K elements per stage (one 128-byte row)
 constexpr int kWStageBytes = kTileV * kBK * 2;    // 16 KB
 constexpr int kMaxStages = 12;
+#ifndef LMS_TC_EPILOGUE_WARPS
+#define LMS_TC_EPILOGUE_WARPS 16
+#endif
+// Epilogue warps: a multiple of 4 (each TMEM lane quadrant gets the same number of warps, which
+// split the batch columns between them).
+constexpr int kEpilogueWarps = LMS_TC_EPILOGUE_WARPS;
+static_assert(kEpilogueWarps % 4 == 0, "epilogue warps come in groups of four");
 constexpr uint32_t kEpiBarrierId = 1;
 
 struct TcParams {
@@ -387,24 +395,30 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
             for (int cc = col_group; cc < n_chunks; cc += kColGroups) {
                 uint32_t acc[16];
                 tmem_load_16(t_row + 16u * cc, acc);
+                float s[16];
+                int ix[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int b = cc * 16 + j;
+                    s[j] = -CUDART_INF_F;
+                    ix[j] = static_cast<int>(v);
                     if (b < B) {
                         const RowParams p = rows[b];
-                        float s = -CUDART_INF_F;
                         if (v_ok && !(p.flags & kRowInvalid)) {
                             const int64_t row = a.row0 + b;
                             const float bias = a.bias ? __ldg(a.bias + row * a.ld_bias + v) : 0.0f;
                             const uint32_t* mrow = a.mask ? a.mask + row * a.ld_mask : nullptr;
-                            s = perturbed_score<kWide>(p, static_cast<uint32_t>(v),
-                                                       __uint_as_float(acc[j]), bias,
-                                                       allowed(mrow, static_cast<uint32_t>(v)));
+                            s[j] = perturbed_score<kWide>(p, static_cast<uint32_t>(v),
+                                                          __uint_as_float(acc[j]), bias,
+                                                          allowed(mrow, static_cast<uint32_t>(v)));
                         }
-                        int idx = static_cast<int>(v);
-                        warp_argmax(s, idx);
-                        if (lane == 0) { red_s[quad * n_pad + b] = s; red_i[quad * n_pad + b] = idx; }
                     }
+                }
+                warp_argmax_16_columns(s, ix, lane);
+                const int c = cc * 16 + (lane >> 1);
+                if ((lane & 1) == 0 && c < B) {
+                    red_s[quad * n_pad + c] = s[0];
+                    red_i[quad * n_pad + c] = ix[0];
                 }
             }
             // The accumulator buffer is free for the MMA of tile i+2.
@@ -474,12 +488,8 @@ cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int
     const size_t smem = L.total + 1024;
     int sms = device_sm_count();
     int grid = static_cast<int>(a.n_tiles < sms ? a.n_tiles : sms);
-    if (n_pad <= 64) {
-        return wide ? launch_variant<4, true>(tmW, tmH, prm, smem, grid, stream)
-                    : launch_variant<4, false>(tmW, tmH, prm, smem, grid, stream);
-    }
-    return wide ? launch_variant<8, true>(tmW, tmH, prm, smem, grid, stream)
-                : launch_variant<8, false>(tmW, tmH, prm, smem, grid, stream);
+    return wide ? launch_variant<kEpilogueWarps, true>(tmW, tmH, prm, smem, grid, stream)
+                : launch_variant<kEpilogueWarps, false>(tmW, tmH, prm, smem, grid, stream);
 }
 
 }  // namespace lms

@@ -120,10 +120,11 @@ __device__ __forceinline__ float gumbel(const RowKey& k, uint32_t v) {
 // ---------------------------------------------------------------------------------------------
 enum RowFlags : uint32_t { kRowGreedy = 1u, kRowInvalid = 2u };
 
-struct RowParams {
+struct __align__(16) RowParams {
     RowKey key;
     float inv_t;     // 1 / T for sampled rows
     uint32_t flags;  // RowFlags
+    uint32_t pad;
 };
 
 __device__ __forceinline__ RowParams make_row_params(const float* temperature, const int64_t* seeds,
@@ -133,6 +134,7 @@ __device__ __forceinline__ RowParams make_row_params(const float* temperature, c
     p.key = make_row_key(seeds, positions, base_seed, offset, row);
     const float T = temperature ? temperature[row] : 1.0f;
     p.flags = 0u;
+    p.pad = 0u;
     p.inv_t = 1.0f;
     if (!(T >= 0.0f)) {
         p.flags = kRowInvalid;           // T < 0 or NaN
@@ -179,6 +181,40 @@ __device__ __forceinline__ void warp_argmax(float& s, int& i) {
         const int io = __shfl_xor_sync(0xffffffffu, i, off);
         if (better(so, io, s, i)) { s = so; i = io; }
     }
+}
+
+// Argmax of 16 columns across the 32 lanes of a warp at once ("transposed" reduction): lane l
+// holds scores s[j] / indices ix[j] of its own row for columns j = 0..15.  Four halving rounds
+// (shuffle offsets 16, 8, 4, 2) each keep half of the columns in every lane, combined with the
+// partner lane's values for the same columns; a last xor-1 round finishes.  On return s[0] /
+// ix[0] of lane l hold the result for column (l >> 1) & 15 over all 32 rows.  16 shuffle pairs
+// instead of 16 x 5 for column-by-column reductions.
+template <int kN>
+__device__ __forceinline__ void halve_columns(float (&s)[16], int (&ix)[16], int lane) {
+    constexpr int kH = kN / 2;
+    const bool upper = (lane & kN) != 0;
+#pragma unroll
+    for (int j = 0; j < kH; ++j) {
+        const float keep_s = upper ? s[j + kH] : s[j];
+        const int keep_i = upper ? ix[j + kH] : ix[j];
+        const float send_s = upper ? s[j] : s[j + kH];
+        const int send_i = upper ? ix[j] : ix[j + kH];
+        const float rs = __shfl_xor_sync(0xffffffffu, send_s, kN);
+        const int ri = __shfl_xor_sync(0xffffffffu, send_i, kN);
+        const bool take = better(rs, ri, keep_s, keep_i);
+        s[j] = take ? rs : keep_s;
+        ix[j] = take ? ri : keep_i;
+    }
+}
+
+__device__ __forceinline__ void warp_argmax_16_columns(float (&s)[16], int (&ix)[16], int lane) {
+    halve_columns<16>(s, ix, lane);
+    halve_columns<8>(s, ix, lane);
+    halve_columns<4>(s, ix, lane);
+    halve_columns<2>(s, ix, lane);
+    const float rs = __shfl_xor_sync(0xffffffffu, s[0], 1);
+    const int ri = __shfl_xor_sync(0xffffffffu, ix[0], 1);
+    if (better(rs, ri, s[0], ix[0])) { s[0] = rs; ix[0] = ri; }
 }
 
 // The candidate a tile reports: index -1 when nothing in the tile is above -inf.

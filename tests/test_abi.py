@@ -46,7 +46,7 @@ def test_tile_info(L):
     assert tv == 128 and nt == 1187 and path == lms.PATH_TCGEN05
     cand = 64 * 1187 * 4
     assert ws == 2 * ((cand + 255) // 256 * 256)
-    assert lms.tile_info(lms.OP_LMHEAD, 1, 4096, 151936)[3] == lms.PATH_GEMV
+    assert lms.tile_info(lms.OP_LMHEAD, 1, 4096, 151936)[3] == lms.PATH_TCGEN05
     tv, nt, _, _ = lms.tile_info(lms.OP_LOGITS, 8192, 0, 131072)
     assert tv == 8192 and nt == 16
     tv, nt, _, _ = lms.tile_info(lms.OP_LOGITS, 1, 0, 131072)
