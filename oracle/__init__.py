@@ -94,16 +94,30 @@ def philox4x32(ctr, key, rounds: int = 10) -> np.ndarray:
     return out
 
 
-def uniform(w0: int, w1: int, wide: bool) -> float:
-    """The midpoint uniform (k + 1/2) / 2^m from one (fp32 noise) or two (wide) Philox words."""
-    return _load().orc_uniform(int(w0) & 0xFFFFFFFF, int(w1) & 0xFFFFFFFF, int(bool(wide)))
+def uniform(lo: int, hi: int, wide: bool) -> float:
+    """The midpoint uniform (k + 1/2) / 2^m from an entry's word (fp32 noise: k = lo >> 8) or
+    two words (wide noise: k = ((hi << 32) | lo) >> 12)."""
+    return _load().orc_uniform(int(lo) & 0xFFFFFFFF, int(hi) & 0xFFFFFFFF, int(bool(wide)))
+
+
+def entry_words(call_words, v, wide: bool):
+    """The (lo, hi) words vocabulary entry v takes from its call's four words: fp32 noise uses
+    word v & 3 of call v >> 2; wide noise words 2(v & 1), 2(v & 1) + 1 of call v >> 1."""
+    w = np.asarray(call_words)
+    v = np.asarray(v)
+    if wide:
+        j = 2 * (v & 1)
+        return np.take_along_axis(w, j[..., None], -1)[..., 0], np.take_along_axis(w, (j + 1)[..., None], -1)[..., 0]
+    return np.take_along_axis(w, (v & 3)[..., None], -1)[..., 0], np.zeros_like(w[..., 0])
 
 
 def noise(B, V, seeds, positions, base_seed, offset, wide):
-    """Noise grid [B, V]: Philox words [B,V,4], u, E = -log u, g = -log E (fp64).
+    """Noise grid [B, V]: the four words of the Philox call each entry draws from [B,V,4], u,
+    E = -log u, g = -log E (fp64).
 
     Keyed by (request seed, absolute position, vocabulary index) for seeded rows, as in the
-    Megatron-LM PR ("The change"); unseeded rows by (base_seed, offset, row)."""
+    Megatron-LM PR ("The change"); unseeded rows by (base_seed, offset, row).  A call serves
+    four consecutive entries (fp32 noise) or two (wide noise)."""
     seeds = _c(seeds, np.int64)
     positions = _c(positions, np.int64)
     words = np.empty((B, V, 4), np.uint32)

@@ -26,12 +26,16 @@
  * Readings where the pages leave a step open (each is also listed with the design notes):
  *   - Philox variant: Philox4x32 with 10 rounds (the pages say "Philox" and "two words ... the
  *     other three", i.e. four 32-bit words per call).
- *   - Key and counter: seeded row  -> key = (seed lo, seed hi), counter = (v, pos lo, pos hi, 0);
+ *   - Key and counter: seeded row  -> key = (seed lo, seed hi), counter = (n, pos lo, pos hi, 0);
  *                      unseeded row -> key = (base_seed lo, base_seed hi),
- *                                      counter = (v, offset lo, offset hi, 0x80000000 | b).
- *   - fp32 noise uses word 0: k = w0 >> 8 (24 bits), u = (k + 1/2) / 2^24.
- *     wide noise uses words 0 and 1: k = ((w1 << 32) | w0) >> 12 (52 bits), u = (k + 1/2) / 2^52.
- *     Both u are exact in fp64.  E = -log(u), g = -log(E).
+ *                                      counter = (n, offset lo, offset hi, 0x80000000 | b).
+ *     One call gives four words and serves consecutive vocabulary entries: with fp32 noise the
+ *     entry v uses word (v & 3) of the call n = v >> 2; with wide noise it uses words 2(v & 1)
+ *     and 2(v & 1) + 1 of the call n = v >> 1.  The variate stays a function of (seed, position,
+ *     v) alone, as the Megatron-LM PR requires, and no generated word is dropped.
+ *   - fp32 noise: k = w >> 8 (the top 24 bits of the entry's word), u = (k + 1/2) / 2^24.
+ *     wide noise: k = ((hi << 32) | lo) >> 12 (the top 52 bits of the entry's two words, lo the
+ *     first), u = (k + 1/2) / 2^52.  Both u are exact in fp64.  E = -log(u), g = -log(E).
  *   - Transform: masked -> -inf; T == 0 -> greedy, s = y + bias (no noise); otherwise
  *     s = (y + bias) / T + g.  T < 0 or NaN -> the row is invalid (status 2, index -1).
  *     A NaN score counts as -inf.
@@ -90,18 +94,38 @@ void orc_philox4x32_many(int64_t n, const uint32_t* ctr, const uint32_t* key, in
     for (int64_t i = 0; i < n; ++i) orc_philox4x32(ctr + 4 * i, key + 2 * i, rounds, out + 4 * i);
 }
 
-/* (request seed, absolute position, vocabulary index) -> (key, counter) [MLM "The change"];
+/* (request seed, absolute position, call index n) -> (key, counter) [MLM "The change"];
  * unseeded rows are keyed by (base_seed, offset, row) instead [SDO "Randomness"]. */
 void orc_key_counter(int seeded, int64_t seed, int64_t pos, uint64_t base_seed, uint64_t offset,
-                     int64_t row, uint32_t v, uint32_t ctr[4], uint32_t key[2]) {
+                     int64_t row, uint32_t n, uint32_t ctr[4], uint32_t key[2]) {
     if (seeded) {
         uint64_t s = (uint64_t)seed, p = (uint64_t)pos;
         key[0] = (uint32_t)s; key[1] = (uint32_t)(s >> 32);
-        ctr[0] = v; ctr[1] = (uint32_t)p; ctr[2] = (uint32_t)(p >> 32); ctr[3] = 0u;
+        ctr[0] = n; ctr[1] = (uint32_t)p; ctr[2] = (uint32_t)(p >> 32); ctr[3] = 0u;
     } else {
         key[0] = (uint32_t)base_seed; key[1] = (uint32_t)(base_seed >> 32);
-        ctr[0] = v; ctr[1] = (uint32_t)offset; ctr[2] = (uint32_t)(offset >> 32);
+        ctr[0] = n; ctr[1] = (uint32_t)offset; ctr[2] = (uint32_t)(offset >> 32);
         ctr[3] = 0x80000000u | (uint32_t)row;
+    }
+}
+
+/* The Philox call that vocabulary entry v draws from, and the word(s) it uses:
+ * fp32 noise -> call n = v >> 2, word (v & 3); wide noise -> call n = v >> 1, words 2(v & 1)
+ * (low half) and 2(v & 1) + 1 (high half).  Writes the call's four words to `call` and the
+ * entry's words to lo / hi (hi is unused for fp32 noise). */
+void orc_entry_words(int seeded, int64_t seed, int64_t pos, uint64_t base_seed, uint64_t offset,
+                     int64_t row, uint32_t v, int wide, uint32_t call[4], uint32_t* lo,
+                     uint32_t* hi) {
+    uint32_t ctr[4], key[2];
+    uint32_t n = wide ? (v >> 1) : (v >> 2);
+    orc_key_counter(seeded, seed, pos, base_seed, offset, row, n, ctr, key);
+    orc_philox4x32(ctr, key, 10, call);
+    if (wide) {
+        *lo = call[2 * (v & 1u)];
+        *hi = call[2 * (v & 1u) + 1];
+    } else {
+        *lo = call[v & 3u];
+        *hi = 0u;
     }
 }
 
@@ -109,13 +133,14 @@ void orc_key_counter(int seeded, int64_t seed, int64_t pos, uint64_t base_seed, 
 /* Uniform and noise [MLM "Problem", "The change"; FS step 3]                                  */
 /* ------------------------------------------------------------------------------------------ */
 
-/* The midpoint uniform: u = (k + 1/2) / 2^m, exact in fp64 (m = 24 or 52). */
-double orc_uniform(uint32_t w0, uint32_t w1, int wide) {
+/* The midpoint uniform u = (k + 1/2) / 2^m, exact in fp64, from the entry's word(s):
+ * fp32 noise: k = lo >> 8 (m = 24); wide noise: k = ((hi << 32) | lo) >> 12 (m = 52). */
+double orc_uniform(uint32_t lo, uint32_t hi, int wide) {
     if (wide) {
-        uint64_t k = ((((uint64_t)w1) << 32) | (uint64_t)w0) >> 12;
+        uint64_t k = ((((uint64_t)hi) << 32) | (uint64_t)lo) >> 12;
         return ldexp((double)k + 0.5, -52);
     } else {
-        uint32_t k = w0 >> 8;
+        uint32_t k = lo >> 8;
         return ldexp((double)k + 0.5, -24);
     }
 }
@@ -127,7 +152,7 @@ double orc_gumbel(double u) { return -log(-log(u)); }
 static int row_is_seeded(const int64_t* seeds, int64_t b) { return seeds != NULL && seeds[b] >= 0; }
 
 /* Noise for a [B][V] grid, any of the outputs may be NULL:
- *   words [B][V][4] uint32, u [B][V], E [B][V], g [B][V] (fp64). */
+ *   words [B][V][4] uint32 (the four words of the call entry v draws from), u, E, g [B][V]. */
 void orc_noise_fill(int64_t B, int64_t V, const int64_t* seeds, const int64_t* positions,
                     uint64_t base_seed, uint64_t offset, int wide, uint32_t* words, double* u,
                     double* E, double* g) {
@@ -135,12 +160,11 @@ void orc_noise_fill(int64_t B, int64_t V, const int64_t* seeds, const int64_t* p
         int seeded = row_is_seeded(seeds, b);
         int64_t seed = seeded ? seeds[b] : 0, pos = seeded ? positions[b] : 0;
         for (int64_t v = 0; v < V; ++v) {
-            uint32_t ctr[4], key[2], w[4];
-            orc_key_counter(seeded, seed, pos, base_seed, offset, b, (uint32_t)v, ctr, key);
-            orc_philox4x32(ctr, key, 10, w);
+            uint32_t w[4], lo, hi;
+            orc_entry_words(seeded, seed, pos, base_seed, offset, b, (uint32_t)v, wide, w, &lo, &hi);
             int64_t i = b * V + v;
             if (words) memcpy(words + 4 * i, w, sizeof w);
-            double uu = orc_uniform(w[0], w[1], wide);
+            double uu = orc_uniform(lo, hi, wide);
             if (u) u[i] = uu;
             if (E) E[i] = orc_exponential(uu);
             if (g) g[i] = orc_gumbel(uu);
@@ -187,11 +211,10 @@ static double orc_score(const orc_rows_args* a, int64_t b, int64_t v, double y) 
         s = t;                                 /* greedy: no noise [SK step 3] */
     } else {
         int seeded = row_is_seeded(a->seeds, b);
-        uint32_t ctr[4], key[2], w[4];
-        orc_key_counter(seeded, seeded ? a->seeds[b] : 0, seeded ? a->positions[b] : 0,
-                        a->base_seed, a->offset, b, (uint32_t)v, ctr, key);
-        orc_philox4x32(ctr, key, 10, w);
-        s = t / T + orc_gumbel(orc_uniform(w[0], w[1], a->wide));
+        uint32_t w[4], lo, hi;
+        orc_entry_words(seeded, seeded ? a->seeds[b] : 0, seeded ? a->positions[b] : 0,
+                        a->base_seed, a->offset, b, (uint32_t)v, a->wide, w, &lo, &hi);
+        s = t / T + orc_gumbel(orc_uniform(lo, hi, a->wide));
     }
     if (isnan(s)) s = -INFINITY;
     return s;

@@ -92,8 +92,37 @@ def test_noise_is_consistent_with_words():
     pos = np.array([0, 0, 2**33 + 1], np.int64)
     for wide in (False, True):
         words, u, E, g = oracle.noise(B, V, seeds, pos, 77, 3, wide)
-        for b, v in [(0, 0), (1, 100), (2, 256)]:
-            w = words[b, v]
-            assert u[b, v] == oracle.uniform(int(w[0]), int(w[1]), wide)
+        for b, v in [(0, 0), (1, 100), (2, 256), (0, 3), (1, 5)]:
+            lo, hi = oracle.entry_words(words[b, v], v, wide)
+            assert u[b, v] == oracle.uniform(int(lo), int(hi), wide)
             assert E[b, v] == -math.log(u[b, v])
             assert g[b, v] == -math.log(E[b, v])
+
+
+@pytest.mark.parametrize("wide", [False, True])
+def test_each_call_serves_consecutive_entries_without_dropping_words(wide):
+    # fp32 noise: entries 4n..4n+3 share call n and use its four words once each; wide noise:
+    # entries 2n, 2n+1 share call n and use words (0, 1) and (2, 3).  The call is Philox at
+    # counter word 0 = n with the row's key -- the same (seed, position, v) keying for every v.
+    B, V = 2, 64
+    seeds = np.array([11, -1], np.int64)
+    pos = np.array([2**35 + 7, 0], np.int64)
+    words, u, _, _ = oracle.noise(B, V, seeds, pos, 5, 9, wide)
+    per = 2 if wide else 4
+    for b in range(B):
+        for n in range(V // per):
+            group = words[b, per * n: per * (n + 1)]
+            assert (group == group[0]).all()
+            used = []
+            for v in range(per * n, per * (n + 1)):
+                lo, hi = oracle.entry_words(words[b, v], v, wide)
+                used += [int(lo)] + ([int(hi)] if wide else [])
+            assert sorted(used) == sorted(int(x) for x in group[0])
+        # the call itself: Philox4x32-10 at counter (n, pos lo, pos hi, 0) with key = seed
+        if seeds[b] >= 0:
+            n = 3
+            ctr = np.array([[n, pos[b] & 0xFFFFFFFF, pos[b] >> 32, 0]], np.uint64).astype(np.uint32)
+            key = np.array([[seeds[b] & 0xFFFFFFFF, seeds[b] >> 32]], np.uint64).astype(np.uint32)
+            assert (oracle.philox4x32(ctr, key)[0] == words[b, per * n]).all()
+        # neighbouring entries get different uniforms
+        assert len(set(u[b].tolist())) == V
