@@ -32,10 +32,8 @@ __global__ void __launch_bounds__(kThreads) lmhead_gemv_kernel(const uint16_t* _
                                                                int64_t ldw, int D, SampleArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     uint16_t* h_s = reinterpret_cast<uint16_t*>(smem_raw);                 // [B][D]
-    __shared__ float y_s[kB][kTileV];
+    __shared__ __align__(16) float y_s[kB][kTileV];
     __shared__ RowParams p_s[kB];
-    __shared__ float red_s[kB][kTileV / 32];
-    __shared__ int red_i[kB][kTileV / 32];
 
     const int B = static_cast<int>(a.B);
     const int tile = blockIdx.x;
@@ -101,35 +99,42 @@ __global__ void __launch_bounds__(kThreads) lmhead_gemv_kernel(const uint16_t* _
     }
     __syncthreads();
 
-    // Steps 2-5: transform, noise, per-row argmax over the tile's 128 entries.
-    // Thread (warp, lane) handles entry r = 32 * (warp % 4) + lane for rows b = warp / 4, +2, ...
-    const int r = 32 * (warp & 3) + lane;
-    const int64_t v = v_tile0 + r;
-    for (int b = warp >> 2; b < B; b += kWarps / 4) {
+    // Steps 2-6: transform, noise, argmax over the tile's 128 entries, one candidate per row.
+    // Warp w takes batch row b = w (B <= 8 = warps); lane l the four consecutive entries
+    // 4l .. 4l + 3, which one Philox call covers (fp32 noise; two calls for wide noise).
+    for (int b = warp; b < B; b += kWarps) {
         const RowParams p = p_s[b];
-        float s = -CUDART_INF_F;
-        if (v < a.V && !(p.flags & kRowInvalid)) {
+        const int r0 = 4 * lane;
+        const int64_t v0 = v_tile0 + r0;
+        float best_s = -CUDART_INF_F;
+        int best_i = kNoIndex;
+        if (v0 < a.V && !(p.flags & kRowInvalid)) {
+            float g[4];
+            if (p.flags & kRowGreedy) {
+                g[0] = g[1] = g[2] = g[3] = 0.0f;
+            } else {
+                gumbel_run<kWide, 4>(p.key, static_cast<uint32_t>(v0), g);
+            }
             const int64_t row = a.row0 + b;
-            const float bias = a.bias ? __ldg(a.bias + row * a.ld_bias + v) : 0.0f;
-            const uint32_t* mrow = a.mask ? a.mask + row * a.ld_mask : nullptr;
-            s = perturbed_score<kWide>(p, static_cast<uint32_t>(v), y_s[b][r], bias,
-                                       allowed(mrow, static_cast<uint32_t>(v)));
-        }
-        int i = static_cast<int>(v);
-        warp_argmax(s, i);
-        if (lane == 0) { red_s[b][warp & 3] = s; red_i[b][warp & 3] = i; }
-    }
-    __syncthreads();
-    // Step 6: one candidate per row for this tile.
-    if (threadIdx.x < B) {
-        const int b = threadIdx.x;
-        float s = red_s[b][0];
-        int i = red_i[b][0];
+            const float* brow = a.bias ? a.bias + row * a.ld_bias : nullptr;
+            const uint32_t mword = a.mask ? (__ldg(a.mask + row * a.ld_mask + (v0 >> 5)) >> (v0 & 31)) : 0xfu;
+            const float4 y = *reinterpret_cast<const float4*>(&y_s[b][r0]);
+            const float yv[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-        for (int q = 1; q < 4; ++q)
-            if (better(red_s[b][q], red_i[b][q], s, i)) { s = red_s[b][q]; i = red_i[b][q]; }
-        a.cand_score[b * a.n_tiles + tile] = s;
-        a.cand_index[b * a.n_tiles + tile] = candidate_index(s, i);
+            for (int e = 0; e < 4; ++e) {
+                const int64_t v = v0 + e;
+                if (v < a.V) {
+                    const float bias = brow ? __ldg(brow + v) : 0.0f;
+                    const float sc = perturb(p, yv[e], bias, (mword >> e) & 1u, g[e]);
+                    if (sc > best_s) { best_s = sc; best_i = static_cast<int>(v); }
+                }
+            }
+        }
+        warp_argmax(best_s, best_i);
+        if (lane == 0) {
+            a.cand_score[b * a.n_tiles + tile] = best_s;
+            a.cand_index[b * a.n_tiles + tile] = candidate_index(best_s, best_i);
+        }
     }
     pdl_launch_dependents();
 }

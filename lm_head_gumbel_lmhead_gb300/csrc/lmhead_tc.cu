@@ -166,14 +166,12 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         : "memory");
 }
 
-// 32 TMEM lanes x 16 consecutive 32-bit columns -> 16 registers per thread (lane = thread).
-__device__ __forceinline__ void tmem_load_16(uint32_t taddr, uint32_t (&r)[16]) {
+// 32 TMEM lanes x 8 consecutive 32-bit columns -> 8 registers per thread (lane = thread).
+__device__ __forceinline__ void tmem_load_8(uint32_t taddr, uint32_t (&r)[8]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
+          "=r"(r[7])
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -195,6 +193,25 @@ __device__ __forceinline__ bool epi_barrier_and(int threads, bool flag) {
         : "r"(flag ? 1u : 0u), "r"(kEpiBarrierId), "r"(threads)
         : "memory");
     return r != 0;
+}
+
+// (score, index) as one 64-bit key whose unsigned order is the lexicographic order "larger
+// score, then smaller index": the score's bits mapped to a monotone unsigned integer in the high
+// half (-0 folded onto +0 first; scores are never NaN here), the complemented index in the low
+// half.  Key 0 is below every real candidate.
+__device__ __forceinline__ unsigned long long pack_candidate(float s, int idx) {
+    const uint32_t f = __float_as_uint(s + 0.0f);
+    const uint32_t ord = (f & 0x80000000u) ? ~f : (f | 0x80000000u);
+    return (static_cast<unsigned long long>(ord) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(idx));
+}
+
+__device__ __forceinline__ float unpack_score(unsigned long long key) {
+    const uint32_t ord = static_cast<uint32_t>(key >> 32);
+    return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7fffffffu) : ~ord);
+}
+
+__device__ __forceinline__ int unpack_index(unsigned long long key) {
+    return static_cast<int>(~static_cast<uint32_t>(key));
 }
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA with the 128-byte
@@ -219,17 +236,22 @@ __host__ __device__ constexpr uint32_t mma_idesc_bf16(int n, int m) {
 // ------------------------------------------------------------------------------------------
 // Shared-memory layout (offsets from a 1024-byte aligned base)
 // ------------------------------------------------------------------------------------------
+// Per epilogue warp: an 8-column x 32-row transpose tile, rows padded to 36 floats so that both
+// the row-wise stores and the 16-byte column-wise loads are free of bank conflicts.
+constexpr int kTrStride = 36;
+constexpr uint32_t kTrWarpBytes = 8 * kTrStride * 4;
+
 struct SmemLayout {
-    uint32_t stages_off, bars_off, misc_off, rows_off, red_s_off, red_i_off, total;
-    __host__ __device__ SmemLayout(int stages, uint32_t stage_bytes, int n_pad) {
+    uint32_t stages_off, bars_off, misc_off, rows_off, red_off, tr_off, total;
+    __host__ __device__ SmemLayout(int stages, uint32_t stage_bytes, int n_pad, int epi_warps) {
         stages_off = 0;
         bars_off = stages * stage_bytes;
         // full[S], empty[S], acc_full[2], acc_empty[2], drain
         misc_off = bars_off + (2 * stages + 5) * 8;
         rows_off = (misc_off + 16 + 15) & ~15u;   // misc: tmem slot, error flag
-        red_s_off = rows_off + n_pad * static_cast<uint32_t>(sizeof(RowParams));
-        red_i_off = red_s_off + 4 * n_pad * 4;
-        total = red_i_off + 4 * n_pad * 4;
+        red_off = rows_off + n_pad * static_cast<uint32_t>(sizeof(RowParams));
+        tr_off = red_off + n_pad * 8;
+        total = tr_off + epi_warps * kTrWarpBytes;
     }
 };
 
@@ -241,7 +263,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
     uint8_t* base = smem_raw + (base_addr - raw_addr);
-    const SmemLayout L(prm.stages, prm.stage_bytes, prm.n_pad);
+    const SmemLayout L(prm.stages, prm.stage_bytes, prm.n_pad, kEpiWarps);
 
     const SampleArgs& a = prm.a;
     const int S = prm.stages;
@@ -259,8 +281,8 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.misc_off);
     volatile int* err = reinterpret_cast<volatile int*>(base + L.misc_off + 4);
     RowParams* rows = reinterpret_cast<RowParams*>(base + L.rows_off);
-    float* red_s = reinterpret_cast<float*>(base + L.red_s_off);   // [4][n_pad]
-    int* red_i = reinterpret_cast<int*>(base + L.red_i_off);       // [4][n_pad]
+    // per batch column: the best (score, index) of the tile so far, as one ordered 64-bit key
+    unsigned long long* red = reinterpret_cast<unsigned long long*>(base + L.red_off);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -280,9 +302,11 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmH)) : "memory");
     }
-    for (int b = threadIdx.x; b < B; b += blockDim.x)
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
         rows[b] = make_row_params(a.temperature, a.seeds, a.positions, a.base_seed, a.offset,
                                   a.row0 + b);
+        red[b] = 0ull;
+    }
     if (warp == 1) tmem_alloc(base_addr + L.misc_off, prm.tmem_cols);
     tc_fence_before_sync();
     __syncthreads();
@@ -369,7 +393,13 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
         const int quad = warp & 3;                       // TMEM lanes 32*quad .. 32*quad+31
         const int col_group = (warp - 2) >> 2;           // which column chunks this warp takes
         constexpr int kColGroups = kEpiWarps / 4;
-        const int n_chunks = (B + 15) / 16;
+        const int n_chunks = (B + 7) / 8;                // 8-column chunks
+        float* tr = reinterpret_cast<float*>(base + L.tr_off + (warp - 2) * kTrWarpBytes);
+        // After the transpose, thread (lane) owns column (lane & 7) of the chunk and the eight
+        // consecutive rows 8 * (lane >> 3) .. + 7 of this quadrant: two Philox calls (fp32
+        // noise) or four (wide noise) cover them.
+        const int my_col = lane & 7;
+        const int my_r0 = (lane >> 3) * 8;
         int i = 0;
         bool ok = true;
         for (int64_t tile = blockIdx.x; tile < nt; tile += gridDim.x, ++i) {
@@ -387,39 +417,58 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
                 continue;
             }
             tc_fence_after_sync();
-            const int r = 32 * quad + lane;
-            const int64_t v = tile * kTileV + r;
-            const bool v_ok = v < a.V;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) +
                                    static_cast<uint32_t>(ab * n_pad);
+            const int64_t v0 = tile * kTileV + 32 * quad + my_r0;   // a multiple of 8
             for (int cc = col_group; cc < n_chunks; cc += kColGroups) {
-                uint32_t acc[16];
-                tmem_load_16(t_row + 16u * cc, acc);
-                float s[16];
-                int ix[16];
+                uint32_t acc[8];
+                tmem_load_8(t_row + 8u * cc, acc);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int b = cc * 16 + j;
-                    s[j] = -CUDART_INF_F;
-                    ix[j] = static_cast<int>(v);
-                    if (b < B) {
-                        const RowParams p = rows[b];
-                        if (v_ok && !(p.flags & kRowInvalid)) {
-                            const int64_t row = a.row0 + b;
-                            const float bias = a.bias ? __ldg(a.bias + row * a.ld_bias + v) : 0.0f;
-                            const uint32_t* mrow = a.mask ? a.mask + row * a.ld_mask : nullptr;
-                            s[j] = perturbed_score<kWide>(p, static_cast<uint32_t>(v),
-                                                          __uint_as_float(acc[j]), bias,
-                                                          allowed(mrow, static_cast<uint32_t>(v)));
+                for (int j = 0; j < 8; ++j) tr[j * kTrStride + lane] = __uint_as_float(acc[j]);
+                __syncwarp();
+                float y[8];
+                const float4 y0 = *reinterpret_cast<const float4*>(tr + my_col * kTrStride + my_r0);
+                const float4 y1 = *reinterpret_cast<const float4*>(tr + my_col * kTrStride + my_r0 + 4);
+                __syncwarp();
+                y[0] = y0.x; y[1] = y0.y; y[2] = y0.z; y[3] = y0.w;
+                y[4] = y1.x; y[5] = y1.y; y[6] = y1.z; y[7] = y1.w;
+                const int b = cc * 8 + my_col;
+                float best_s = -CUDART_INF_F;
+                int best_i = kNoIndex;
+                if (b < B && v0 < a.V) {
+                    const RowParams p = rows[b];
+                    if (!(p.flags & kRowInvalid)) {
+                        float g[8];
+                        if (p.flags & kRowGreedy) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) g[e] = 0.0f;
+                        } else {
+                            gumbel_run<kWide, 8>(p.key, static_cast<uint32_t>(v0), g);
+                        }
+                        const int64_t row = a.row0 + b;
+                        const float* brow = a.bias ? a.bias + row * a.ld_bias : nullptr;
+                        // the eight entries share one mask word (v0 is a multiple of 8)
+                        const uint32_t mword =
+                            a.mask ? (__ldg(a.mask + row * a.ld_mask + (v0 >> 5)) >> (v0 & 31)) : 0xffu;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int64_t v = v0 + e;
+                            if (v < a.V) {
+                                const float bias = brow ? __ldg(brow + v) : 0.0f;
+                                const float sc = perturb(p, y[e], bias, (mword >> e) & 1u, g[e]);
+                                if (sc > best_s) { best_s = sc; best_i = static_cast<int>(v); }
+                            }
                         }
                     }
                 }
-                warp_argmax_16_columns(s, ix, lane);
-                const int c = cc * 16 + (lane >> 1);
-                if ((lane & 1) == 0 && c < B) {
-                    red_s[quad * n_pad + c] = s[0];
-                    red_i[quad * n_pad + c] = ix[0];
+                // the four threads holding this column (lanes c, c + 8, c + 16, c + 24)
+#pragma unroll
+                for (int off = 8; off <= 16; off <<= 1) {
+                    const float so = __shfl_xor_sync(0xffffffffu, best_s, off);
+                    const int io = __shfl_xor_sync(0xffffffffu, best_i, off);
+                    if (better(so, io, best_s, best_i)) { best_s = so; best_i = io; }
                 }
+                if (lane < 8 && b < B) atomicMax(red + b, pack_candidate(best_s, best_i));
             }
             // The accumulator buffer is free for the MMA of tile i+2.
             tc_fence_before_sync();
@@ -427,16 +476,11 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
             if (lane == 0) mbar_arrive(acce_bar(ab));
             epi_barrier(epi_threads);
             for (int b = epi_tid; b < B; b += epi_threads) {
-                float s = red_s[b];
-                int idx = red_i[b];
-#pragma unroll
-                for (int q = 1; q < 4; ++q)
-                    if (better(red_s[q * n_pad + b], red_i[q * n_pad + b], s, idx)) {
-                        s = red_s[q * n_pad + b];
-                        idx = red_i[q * n_pad + b];
-                    }
+                const unsigned long long key = red[b];
+                red[b] = 0ull;                       // ready for the next tile
+                const float s = unpack_score(key);
                 a.cand_score[b * nt + tile] = s;
-                a.cand_index[b * nt + tile] = candidate_index(s, idx);
+                a.cand_index[b * nt + tile] = candidate_index(s, unpack_index(key));
             }
             epi_barrier(epi_threads);
         }
@@ -474,7 +518,7 @@ cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int
     prm.n_pad = n_pad;
     prm.stage_bytes = static_cast<uint32_t>(kWStageBytes + n_pad * kBK * 2);
     const uint32_t budget = 227u * 1024u - 1024u;   // opt-in maximum minus alignment slack
-    const SmemLayout fixed(0, prm.stage_bytes, n_pad);
+    const SmemLayout fixed(0, prm.stage_bytes, n_pad, kEpilogueWarps);
     int stages = static_cast<int>((budget - fixed.total - (2 * kMaxStages + 5) * 8) / prm.stage_bytes);
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return cudaErrorInvalidValue;
@@ -484,7 +528,7 @@ cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int
     prm.tmem_cols = cols;
     prm.timeout_ns = static_cast<uint64_t>(timeout_ms) * 1000000ull;
     prm.debug_flags = debug_flags;
-    const SmemLayout L(stages, prm.stage_bytes, n_pad);
+    const SmemLayout L(stages, prm.stage_bytes, n_pad, kEpilogueWarps);
     const size_t smem = L.total + 1024;
     int sms = device_sm_count();
     int grid = static_cast<int>(a.n_tiles < sms ? a.n_tiles : sms);

@@ -67,52 +67,106 @@ __device__ __forceinline__ RowKey make_row_key(const int64_t* seeds, const int64
     return k;
 }
 
-__device__ __forceinline__ Words row_words(const RowKey& k, uint32_t v) {
-    return philox4x32_10(v, k.c1, k.c2, k.c3, k.ka, k.kb);
+// One Philox call of a row: counter (n, c1, c2, c3) under the row's key.  With fp32 noise the
+// call n serves the four vocabulary entries 4n..4n+3 (entry v takes word v & 3); with wide noise
+// it serves 2n and 2n+1 (entry v takes words 2(v & 1) and 2(v & 1) + 1, low half first).  The
+// variate of an entry is therefore a function of (seed, position, v) alone, and no word is
+// dropped.
+__device__ __forceinline__ Words row_call(const RowKey& k, uint32_t n) {
+    return philox4x32_10(n, k.c1, k.c2, k.c3, k.ka, k.kb);
 }
 
 // ---------------------------------------------------------------------------------------------
 // Uniform -> E = -log u -> g = -log E, in fp32.
 //
 // u = (k + 1/2) / 2^m is written as n / 2^(m+1) with n = 2k + 1 odd.  Below one half, u itself
-// is formed (exact for m = 24; one rounding for m = 52) and E = -log u; above one half the
+// is formed (exact for m = 24; one rounding for m = 52) and E = -log u.  Above one half the
 // complement c = 1 - u = (2^(m+1) - n) / 2^(m+1) is formed from integers the same way and
-// E = -log1p(-c), so the tail (u -> 1, E -> 0, the largest g) keeps full relative precision:
-// E reaches 2^-25 (fp32 noise) and 2^-53 (wide noise) as the Megatron-LM PR's ranges require.
+// E = -log(1 - c) is evaluated from c, so the tail (u -> 1, E -> 0, the largest g) keeps full
+// relative precision: E reaches 2^-25 (fp32 noise) and 2^-53 (wide noise), the ranges the
+// Megatron-LM PR gives.
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ float exponential_from_odd24(uint32_t n /* odd, < 2^25 */) {
-    // u = n / 2^25
-    if (n < (1u << 24)) {
-        return -__logf(static_cast<float>(n) * 0x1p-25f);
-    }
-    const float c = static_cast<float>((1u << 25) - n) * 0x1p-25f;  // exact: < 2^24, odd
-    return -log1pf(-c);
+
+// -log(1 - c) for 0 < c <= 1/2 with relative error about 2^-22: the series
+// -log(1 - c) = 2 atanh(z) = 2 (z + z^3/3 + z^5/5 + ...), z = c / (2 - c) <= 1/3, summed to
+// z^15/15 (the first omitted term is below z * 2^-29 for z <= 1/3).
+__device__ __forceinline__ float neg_log_one_minus(float c) {
+    const float z = __fdividef(c, 2.0f - c);
+    const float z2 = z * z;
+    float p = 1.0f / 15.0f;
+    p = fmaf(p, z2, 1.0f / 13.0f);
+    p = fmaf(p, z2, 1.0f / 11.0f);
+    p = fmaf(p, z2, 1.0f / 9.0f);
+    p = fmaf(p, z2, 1.0f / 7.0f);
+    p = fmaf(p, z2, 1.0f / 5.0f);
+    p = fmaf(p, z2, 1.0f / 3.0f);
+    p = fmaf(p, z2, 1.0f);
+    return 2.0f * z * p;
 }
 
-__device__ __forceinline__ float exponential_from_odd53(uint64_t n /* odd, < 2^53 */) {
-    // u = n / 2^53
-    if (n < (1ull << 52)) {
-        return -__logf(__ull2float_rn(n) * 0x1p-53f);
-    }
-    const float c = __ull2float_rn((1ull << 53) - n) * 0x1p-53f;
-    return -log1pf(-c);
+// E from the entry's word, fp32 noise: n = 2 (w >> 8) + 1, u = n / 2^25.
+__device__ __forceinline__ float exponential_fp32(uint32_t w) {
+    const uint32_t n = ((w >> 8) << 1) | 1u;
+    const float lower = -__logf(static_cast<float>(n) * 0x1p-25f);                       // u < 1/2
+    const float upper = neg_log_one_minus(static_cast<float>((1u << 25) - n) * 0x1p-25f); // c <= 1/2
+    return n < (1u << 24) ? lower : upper;
 }
 
-__device__ __forceinline__ float exponential_fp32(const Words& w) {
-    return exponential_from_odd24(((w.w0 >> 8) << 1) | 1u);
+// A 53-bit odd integer to fp32 (one rounding of the low part, then one of the sum).
+__device__ __forceinline__ float odd53_to_float(uint64_t n) {
+    return fmaf(static_cast<float>(static_cast<uint32_t>(n >> 32)), 0x1p32f,
+                static_cast<float>(static_cast<uint32_t>(n)));
 }
 
-__device__ __forceinline__ float exponential_wide(const Words& w) {
-    const uint64_t k = ((static_cast<uint64_t>(w.w1) << 32) | w.w0) >> 12;
-    return exponential_from_odd53((k << 1) | 1ull);
+// E from the entry's two words, wide noise: n = 2 k + 1 with k = ((hi << 32) | lo) >> 12,
+// u = n / 2^53.
+__device__ __forceinline__ float exponential_wide(uint32_t lo, uint32_t hi) {
+    const uint64_t k = ((static_cast<uint64_t>(hi) << 32) | lo) >> 12;
+    const uint64_t n = (k << 1) | 1ull;
+    const float lower = -__logf(odd53_to_float(n) * 0x1p-53f);
+    const float upper = neg_log_one_minus(odd53_to_float((1ull << 53) - n) * 0x1p-53f);
+    return n < (1ull << 52) ? lower : upper;
 }
 
 __device__ __forceinline__ float gumbel_from_exponential(float E) { return -__logf(E); }
 
+// Gumbel noise of one entry (a whole call per entry: for kernels that visit entries one by one).
 template <bool kWide>
-__device__ __forceinline__ float gumbel(const RowKey& k, uint32_t v) {
-    const Words w = row_words(k, v);
-    return gumbel_from_exponential(kWide ? exponential_wide(w) : exponential_fp32(w));
+__device__ __forceinline__ float gumbel_one(const RowKey& k, uint32_t v) {
+    if (kWide) {
+        const Words w = row_call(k, v >> 1);
+        const bool second = v & 1u;
+        return gumbel_from_exponential(exponential_wide(second ? w.w2 : w.w0, second ? w.w3 : w.w1));
+    }
+    const Words w = row_call(k, v >> 2);
+    const uint32_t j = v & 3u;
+    const uint32_t word = j == 0 ? w.w0 : j == 1 ? w.w1 : j == 2 ? w.w2 : w.w3;
+    return gumbel_from_exponential(exponential_fp32(word));
+}
+
+// Gumbel noise of kN consecutive entries v0 .. v0 + kN - 1 from kN / 4 calls (fp32 noise) or
+// kN / 2 calls (wide noise).  v0 must be a multiple of 4 (fp32) or 2 (wide), kN of the same.
+template <bool kWide, int kN>
+__device__ __forceinline__ void gumbel_run(const RowKey& k, uint32_t v0, float (&g)[kN]) {
+    if constexpr (kWide) {
+        static_assert(kN % 2 == 0, "wide noise: entries come in pairs");
+#pragma unroll
+        for (int c = 0; c < kN / 2; ++c) {
+            const Words w = row_call(k, (v0 >> 1) + c);
+            g[2 * c] = gumbel_from_exponential(exponential_wide(w.w0, w.w1));
+            g[2 * c + 1] = gumbel_from_exponential(exponential_wide(w.w2, w.w3));
+        }
+    } else {
+        static_assert(kN % 4 == 0, "fp32 noise: entries come in fours");
+#pragma unroll
+        for (int c = 0; c < kN / 4; ++c) {
+            const Words w = row_call(k, (v0 >> 2) + c);
+            g[4 * c] = gumbel_from_exponential(exponential_fp32(w.w0));
+            g[4 * c + 1] = gumbel_from_exponential(exponential_fp32(w.w1));
+            g[4 * c + 2] = gumbel_from_exponential(exponential_fp32(w.w2));
+            g[4 * c + 3] = gumbel_from_exponential(exponential_fp32(w.w3));
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -150,19 +204,22 @@ __device__ __forceinline__ bool allowed(const uint32_t* mask_row, uint32_t v) {
     return mask_row == nullptr || ((__ldg(mask_row + (v >> 5)) >> (v & 31u)) & 1u);
 }
 
-// Perturbed score of one entry.  `y` is the raw logit, `bias` already looked up (0 if none).
+// Perturbed score of one entry from its raw logit y, bias (0 if none), mask bit and noise g
+// (ignored on greedy rows).  Bias before temperature; NaN counts as -inf.
+__device__ __forceinline__ float perturb(const RowParams& p, float y, float bias, bool is_allowed,
+                                         float g) {
+    const float t = y + bias;
+    const float s = (p.flags & kRowGreedy) ? t : fmaf(t, p.inv_t, g);
+    return (is_allowed && s == s) ? s : -CUDART_INF_F;
+}
+
+// The same for one entry visited on its own (computes its Philox call).
 template <bool kWide>
 __device__ __forceinline__ float perturbed_score(const RowParams& p, uint32_t v, float y,
                                                  float bias, bool is_allowed) {
     if (!is_allowed) return -CUDART_INF_F;
-    const float t = y + bias;
-    float s;
-    if (p.flags & kRowGreedy) {
-        s = t;
-    } else {
-        s = t * p.inv_t + gumbel<kWide>(p.key, v);
-    }
-    return (s == s) ? s : -CUDART_INF_F;  // NaN counts as -inf
+    const float g = (p.flags & kRowGreedy) ? 0.0f : gumbel_one<kWide>(p.key, v);
+    return perturb(p, y, bias, true, g);
 }
 
 // ---------------------------------------------------------------------------------------------

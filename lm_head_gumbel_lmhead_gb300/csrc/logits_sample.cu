@@ -19,22 +19,23 @@ __device__ __forceinline__ float to_float<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ float to_float<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
 
-// kVec consecutive entries per load (16 bytes when the rows are 16-byte aligned, else 1).
-template <typename T, int kVec>
-struct VecLoad {
-    __device__ __forceinline__ static void load(const T* p, float (&y)[kVec]) {
-        if constexpr (kVec == 1) {
-            y[0] = to_float<T>(p[0]);
-        } else {
-            const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p));
-            const T* e = reinterpret_cast<const T*>(&raw);
+// A unit of kUnit consecutive entries per thread and iteration (a multiple of 4, so that whole
+// Philox calls cover it): one 16-byte load when the row is 16-byte aligned, else scalar loads.
+template <typename T, int kUnit, bool kVector>
+__device__ __forceinline__ void load_unit(const T* p, int64_t n_valid, float (&y)[kUnit]) {
+    if (kVector && n_valid >= kUnit) {
+        static_assert(kUnit * sizeof(T) == 16 || !kVector, "vector units are 16 bytes");
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p));
+        const T* e = reinterpret_cast<const T*>(&raw);
 #pragma unroll
-            for (int j = 0; j < kVec; ++j) y[j] = to_float<T>(e[j]);
-        }
+        for (int j = 0; j < kUnit; ++j) y[j] = to_float<T>(e[j]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < kUnit; ++j) y[j] = (j < n_valid) ? to_float<T>(p[j]) : 0.0f;
     }
-};
+}
 
-template <typename T, int kVec, bool kWide>
+template <typename T, int kUnit, bool kVector, bool kWide>
 __global__ void __launch_bounds__(kThreads) logits_stage1_kernel(const T* __restrict__ logits,
                                                                  int64_t ld, int tile_v,
                                                                  SampleArgs a) {
@@ -50,27 +51,28 @@ __global__ void __launch_bounds__(kThreads) logits_stage1_kernel(const T* __rest
         const T* y_row = logits + row * ld;
         const float* bias_row = a.bias ? a.bias + row * a.ld_bias : nullptr;
         const uint32_t* mask_row = a.mask ? a.mask + row * a.ld_mask : nullptr;
-        const int64_t v0 = t * tile_v;
-        const int64_t v_end = (v0 + tile_v < a.V) ? v0 + tile_v : a.V;
-        // chunk c covers entries [v0 + c*kVec, v0 + c*kVec + kVec); chunks are strided by the
-        // CTA so that each thread visits its entries in increasing v (strict '>' then keeps
-        // the smallest index among equal scores within the thread).
-        for (int64_t v = v0 + static_cast<int64_t>(threadIdx.x) * kVec; v < v_end;
-             v += static_cast<int64_t>(kThreads) * kVec) {
-            float y[kVec];
-            if (v + kVec <= v_end) {
-                VecLoad<T, kVec>::load(y_row + v, y);
-            } else {
+        const int64_t v_tile = t * tile_v;
+        const int64_t v_end = (v_tile + tile_v < a.V) ? v_tile + tile_v : a.V;
+        // Units are strided by the CTA so that each thread visits its entries in increasing v
+        // (strict '>' then keeps the smallest index among equal scores within the thread).
+        for (int64_t v0 = v_tile + static_cast<int64_t>(threadIdx.x) * kUnit; v0 < v_end;
+             v0 += static_cast<int64_t>(kThreads) * kUnit) {
+            float y[kUnit];
+            load_unit<T, kUnit, kVector>(y_row + v0, v_end - v0, y);
+            float g[kUnit];
+            if (p.flags & kRowGreedy) {
 #pragma unroll
-                for (int j = 0; j < kVec; ++j) y[j] = (v + j < v_end) ? to_float<T>(y_row[v + j]) : 0.0f;
+                for (int j = 0; j < kUnit; ++j) g[j] = 0.0f;
+            } else {
+                gumbel_run<kWide, kUnit>(p.key, static_cast<uint32_t>(v0), g);
             }
 #pragma unroll
-            for (int j = 0; j < kVec; ++j) {
-                const int64_t vj = v + j;
-                if (vj < v_end) {
-                    const uint32_t vv = static_cast<uint32_t>(vj);
-                    const float bias = bias_row ? __ldg(bias_row + vj) : 0.0f;
-                    const float s = perturbed_score<kWide>(p, vv, y[j], bias, allowed(mask_row, vv));
+            for (int j = 0; j < kUnit; ++j) {
+                const int64_t v = v0 + j;
+                if (v < v_end) {
+                    const uint32_t vv = static_cast<uint32_t>(v);
+                    const float bias = bias_row ? __ldg(bias_row + v) : 0.0f;
+                    const float s = perturb(p, y[j], bias, allowed(mask_row, vv), g[j]);
                     if (s > best_s) { best_s = s; best_i = static_cast<int>(vv); }
                 }
             }
@@ -93,15 +95,15 @@ __global__ void __launch_bounds__(kThreads) logits_stage1_kernel(const T* __rest
     pdl_launch_dependents();
 }
 
-template <typename T, int kVec>
+template <typename T, int kUnit, bool kVector>
 cudaError_t launch_typed(const void* logits, int64_t ld, int tile_v, bool wide, const SampleArgs& a,
                          cudaStream_t stream) {
     const int64_t grid = a.B * a.n_tiles;
     const T* y = static_cast<const T*>(logits);
     if (wide) {
-        logits_stage1_kernel<T, kVec, true><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(y, ld, tile_v, a);
+        logits_stage1_kernel<T, kUnit, kVector, true><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(y, ld, tile_v, a);
     } else {
-        logits_stage1_kernel<T, kVec, false><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(y, ld, tile_v, a);
+        logits_stage1_kernel<T, kUnit, kVector, false><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(y, ld, tile_v, a);
     }
     return cudaGetLastError();
 }
@@ -114,11 +116,11 @@ cudaError_t launch_logits_stage1(const void* logits, bool bf16, int64_t ld, int 
     const bool aligned = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) &&
                          ((static_cast<size_t>(ld) * esize) % 16 == 0);
     if (bf16) {
-        return aligned ? launch_typed<__nv_bfloat16, 8>(logits, ld, tile_v, wide, a, stream)
-                       : launch_typed<__nv_bfloat16, 1>(logits, ld, tile_v, wide, a, stream);
+        return aligned ? launch_typed<__nv_bfloat16, 8, true>(logits, ld, tile_v, wide, a, stream)
+                       : launch_typed<__nv_bfloat16, 4, false>(logits, ld, tile_v, wide, a, stream);
     }
-    return aligned ? launch_typed<float, 4>(logits, ld, tile_v, wide, a, stream)
-                   : launch_typed<float, 1>(logits, ld, tile_v, wide, a, stream);
+    return aligned ? launch_typed<float, 4, true>(logits, ld, tile_v, wide, a, stream)
+                   : launch_typed<float, 4, false>(logits, ld, tile_v, wide, a, stream);
 }
 
 }  // namespace lms

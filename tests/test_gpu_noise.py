@@ -66,7 +66,8 @@ def test_noise_extremes_keep_the_tail(wide):
     idx = torch.cat([torch.topk(flat, 16).indices, torch.topk(-flat, 16).indices]).cpu().numpy()
     words = lms.philox_fill_noise(B, V, kind="words", **kw).view(-1, 4)[torch.from_numpy(idx).to(dev)]
     w = _u32(words)
-    ref = np.array([-math.log(oracle.uniform(int(a), int(b), wide)) for a, b in w[:, :2]])
+    lo, hi = oracle.entry_words(w, idx % V, wide)
+    ref = np.array([-math.log(oracle.uniform(int(a), int(b), wide)) for a, b in zip(lo, hi)])
     got = flat[torch.from_numpy(idx).to(dev)].cpu().numpy().astype(np.float64)
     assert np.all(np.abs(got - ref) <= E_RTOL * ref)
     lo_bound = 2.0 ** -53 if wide else 2.0 ** -25
@@ -96,7 +97,8 @@ def test_replay_under_contention_and_single_row_equals_batched(rows):
         one = lms.philox_fill_noise(1, V, kind="words", wide=True, seeds=sd[b:b + 1],
                                     positions=pd[b:b + 1], base_seed=3)
         assert torch.equal(one[0], ref[b])
-    # the fp32 stream uses word 0 only and is unchanged by the wide option
-    g32 = lms.philox_fill_noise(B, V, kind="uniform", wide=False, seeds=sd, positions=pd, base_seed=3)
-    w0 = _u32(ref[..., 0]).astype(np.float64)
-    assert np.array_equal(g32.cpu().numpy(), (np.floor(w0 / 256) * 2 + 1) * 2.0 ** -25)
+    # the fp32 stream: entry v takes the top 24 bits of word v & 3 of its call
+    w32 = _u32(lms.philox_fill_noise(B, V, kind="words", wide=False, seeds=sd, positions=pd, base_seed=3))
+    u32 = lms.philox_fill_noise(B, V, kind="uniform", wide=False, seeds=sd, positions=pd, base_seed=3)
+    lo, _ = oracle.entry_words(w32, np.arange(V)[None, :].repeat(B, 0), False)
+    assert np.array_equal(u32.cpu().numpy(), (np.floor(lo.astype(np.float64) / 256) * 2 + 1) * 2.0 ** -25)
