@@ -1,20 +1,38 @@
 """Benchmark: µs per fused LM-head + Gumbel-max decode sample step on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--batch B] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--batch B]
+                    [--impl reference]
 
-One step is one pass of the whole hot path over one batch: the fused Stage 1 (LM-head GEMM on
-the tensor cores, transform, Philox noise, per-tile argmax; the [B, V] logits never reach
-memory) and Stage 2 (per-row reduction of the tile candidates), both through the C ABI
-``lms_lmhead_sample``.  The workload is the Qwen3-8B-shaped decode batch (D = 4096,
-V = 151936, bf16 W ~ N(0, 0.02), H RMS-normalised N(0, 1), T = 0.7, per-row seeds, positions =
-step), B = 64 by default: W (1.24 GB) is far larger than L2, so no flush is needed between steps.
+One step is one pass of the whole hot path over one batch. For the fused workloads that means the
+fused Stage 1 and then Stage 2, both through the C ABI ``lms_lmhead_sample``:
 
-Prints one JSON line.  `value` is µs per step (lower is better), `roofline` the achieved HBM
-bandwidth of the step against the measured copy bandwidth, `e2e` the same metric with the
-step's inputs copied from pinned host memory and the tokens copied back inside the timed
-region, `cpu_baseline` the CPU oracle on a bounded slice of the same workload.  With
-``--impl reference`` the CPU oracle itself is timed as the reference arm.
-Multi-GPU (torchrun): every rank runs an independent replica; rank 0 prints the max over ranks.
+- Stage 1 runs the LM-head GEMM on the tensor cores, applies the transform, draws the Philox
+  noise and takes the per-tile argmax. The [B, V] logits never reach memory.
+- Stage 2 reduces each row's tile candidates to one token.
+
+Workloads (synthetic, seeded; the shapes of the FlashSampling page's measurements):
+
+- ``qwen3-8b`` (default; B = 64): D = 4096, V = 151936. W is bf16 ~ N(0, 0.02) and H is
+  RMS-normalised N(0, 1). Noise is fp32, T = 0.7 with per-row seeds, and positions = step.
+- ``llama3-hetero`` (B = 64): D = 4096, V = 128256. Rows mix T ~ U[0.3, 1.2] with 8 greedy
+  rows. It adds an fp32 bias and a 90% -inf mask on half the rows.
+- ``large-vocab`` (B in 128/256/512): D = 8192, V = 262144, wide noise.
+- ``logits``: ``lms_sample_from_logits`` over materialised N(0, 4) logits, V = 131072.
+- ``noise``: ``lms_philox_fill_noise`` of Gumbel noise, B x V float32.
+
+Every input is larger than L2 (the fused workloads stream W of 1.05–4.3 GB), so no flush is needed.
+
+The script prints one JSON line:
+
+- `value`: µs per step (lower is better).
+- `roofline`: the step's algorithmic bytes (or flops, where the tensor floor dominates) over its
+  event time, against ``MEASURED_PEAKS.json``.
+- `e2e`: the same metric with the step's inputs copied from pinned host memory and the tokens
+  copied back, inside the timed region.
+- `cpu_baseline`: the CPU oracle on a bounded slice of the same workload.
+
+With ``--impl reference`` the CPU oracle itself is timed as the reference arm. Under torchrun every
+rank runs an independent replica, and rank 0 prints the max over ranks.
 """
 from __future__ import annotations
 
@@ -37,6 +55,7 @@ METRIC = "µs per decode sample step & achieved HBM GB/s vs peak, fused LM-head+
 UNIT = "us/step"
 TC_SOURCES = ["lm_head_gumbel_lmhead_gb300/csrc/lmhead_tc.cu",
               "lm_head_gumbel_lmhead_gb300/csrc/lms_device.cuh"]
+FUSED = ("qwen3-8b", "llama3-hetero", "large-vocab")
 
 
 def kernel_source_hash() -> str:
@@ -53,27 +72,37 @@ def measured_peaks() -> dict:
         with open(p) as f:
             d = json.load(f)
         return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
                 "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
 
 
-def recorded_traffic():
+def recorded_traffic(workload: str, B: int):
     """DRAM bytes per launch of the fused kernel from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
+    for this workload on the current kernel source (else None)."""
     p = os.path.join(ROOT, "profiles", "lmhead_tc_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    if d.get("kernel_source_hash") != kernel_source_hash():
+    rec = d.get(f"{workload}/B={B}")
+    if rec is None or rec.get("kernel_source_hash") != kernel_source_hash():
         return None
-    return d
+    return rec
 
 
-def algorithmic_bytes(B: int, D: int, V: int, n_tiles: int) -> int:
-    """Bytes the method must move per step: W once, H once, the Stage-1 candidates written and
-    read back, the per-row parameters (T, seed, position) and the tokens."""
-    return V * D * 2 + B * D * 2 + 2 * B * n_tiles * 8 + B * 20 + B * 8
+def algorithmic_bytes(B: int, D: int, V: int, n_tiles: int, bias: bool = False,
+                      mask: bool = False) -> int:
+    """Bytes the fused method must move per step: W once, H once, the Stage-1 candidates written
+    and read back, the per-row parameters (T, seed, position), the tokens, and the optional bias
+    and mask rows."""
+    b = V * D * 2 + B * D * 2 + 2 * B * n_tiles * 8 + B * 20 + B * 8
+    if bias:
+        b += B * V * 4
+    if mask:
+        b += B * ((V + 31) // 32) * 4
+    return b
 
 
 # ------------------------------------------------------------------------------------------
@@ -156,16 +185,54 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------------
+# workloads
+# ------------------------------------------------------------------------------------------
+def make_workload(name: str, B: int, D: int, V: int):
+    from lm_head_gumbel_lmhead_gb300 import workloads
+    if name == "qwen3-8b":
+        return workloads.qwen3_8b(B, D=D or 4096, V=V or 151936)
+    if name == "llama3-hetero":
+        return workloads.llama3_hetero(B, D=D or 4096, V=V or 128256)
+    if name == "large-vocab":
+        return workloads.large_vocab(B, D=D or 8192, V=V or 262144)
+    raise ValueError(name)
+
+
+def default_batch(name: str) -> int:
+    return {"large-vocab": 256, "logits": 64, "noise": 64}.get(name, 64)
+
+
+# ------------------------------------------------------------------------------------------
 # the CPU oracle timed on a bounded slice (cpu_baseline leg and --impl reference)
 # ------------------------------------------------------------------------------------------
+def _orc_kw(w, v_slice):
+    mask = None if w.mask is None else w.mask.numpy().view("uint32")
+    bias = None if w.bias is None else w.bias[:, :v_slice].double().numpy()
+    if mask is not None:
+        mask = mask[:, : (v_slice + 31) // 32]
+    return dict(temperature=w.temperature.double().numpy(), seeds=w.seeds.numpy(),
+                positions=w.positions.numpy(), bias=bias, mask=mask, base_seed=w.base_seed,
+                offset=w.offset, wide=w.noise_mode == 1)
+
+
 def oracle_sample_time(w, v_slice: int, threads: int):
     """Seconds for the oracle's fused path on all B rows over the first v_slice vocabulary
     rows; scaled linearly to the full vocabulary by the caller."""
     import oracle
     W = w.W[:v_slice].contiguous()
     t0 = time.perf_counter()
-    oracle.lmhead_sample(w.H, W, temperature=w.temperature.double().numpy(), seeds=w.seeds.numpy(),
-                         positions=w.positions.numpy(), tile_v=128, threads=threads)
+    oracle.lmhead_sample(w.H, W, tile_v=128, threads=threads, **_orc_kw(w, v_slice))
+    return time.perf_counter() - t0
+
+
+def oracle_logits_time(logits, v_slice: int, threads: int):
+    import oracle
+    import numpy as np
+    B = logits.shape[0]
+    y = logits[:, :v_slice].double().numpy()
+    t0 = time.perf_counter()
+    oracle.sample_from_logits(y, temperature=np.full(B, 0.7), seeds=np.arange(B) + 1000,
+                              positions=np.zeros(B, np.int64), threads=threads)
     return time.perf_counter() - t0
 
 
@@ -187,10 +254,13 @@ def run_reference(args):
     rank, ws = init_dist("gloo")
     if rank != 0:
         return
-    from lm_head_gumbel_lmhead_gb300 import workloads
-    w = workloads.qwen3_8b(args.batch, D=args.D, V=args.V)
+    if args.workload not in FUSED:
+        print(json.dumps({"impl": "reference", "unavailable":
+                          f"the reference arm times the oracle's fused path; workload {args.workload} has none"}))
+        return
+    w = make_workload(args.workload, args.batch, args.D, args.V)
     threads = os.cpu_count() or 1
-    v_slice = args.ref_vslice
+    v_slice = min(args.ref_vslice, w.V)
     for _ in range(args.warmup):
         oracle_sample_time(w, min(v_slice, 512), threads)
     times = [oracle_sample_time(w, v_slice, threads) for _ in range(args.steps)]
@@ -199,8 +269,8 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "D": w.D, "V": w.V, "noise": "fp32",
-                       "parallelism": "replicas"},
+            "config": {"workload": w.name, "B": w.B, "D": w.D, "V": w.V,
+                       "noise": "wide53" if w.noise_mode else "fp32", "parallelism": "replicas"},
             "cpu_baseline": {"value": us, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": f"each step: B={w.B} rows x first {v_slice} of {w.V} "
                                        f"vocabulary rows, scaled linearly to the full vocabulary"},
@@ -211,6 +281,26 @@ def run_reference(args):
 # ------------------------------------------------------------------------------------------
 # the GPU arm
 # ------------------------------------------------------------------------------------------
+def _time_steps(step, n_warm, n_steps, dev, stream, first_index=0):
+    import torch
+    for i in range(n_warm):
+        step(first_index + i)
+    torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps + 1)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    ev[0].record(stream)
+    for k in range(n_steps):
+        step(first_index + n_warm + k)
+        ev[k + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    barrier()
+    per_ms = [ev[k].elapsed_time(ev[k + 1]) for k in range(n_steps)]
+    return ev[0].elapsed_time(ev[n_steps]) / n_steps, per_ms, t0, t1
+
+
 def run_gpu(args):
     import torch
 
@@ -221,106 +311,162 @@ def run_gpu(args):
     _, _, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    B, D, V = args.batch, args.D, args.V
-    w = workloads.qwen3_8b(B, D=D, V=V)
-    H, W = w.H.to(dev), w.W.to(dev)
-    T, seeds = w.temperature.to(dev), w.seeds.to(dev)
-    n_steps = args.warmup + args.steps
-    # positions = step: one row of positions per step, made before timing
-    pos_all = torch.arange(n_steps, dtype=torch.int64, device=dev)[:, None].expand(n_steps, B).contiguous()
-    tv, nt, ws_bytes, path = lms.tile_info(lms.OP_LMHEAD, B, D, V)
-    workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    out = torch.empty(B, dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = (1 + (B - 1) // 256 if path == lms.PATH_TCGEN05 else 1) + 1
+    n_steps = args.warmup + args.steps
+    peaks = measured_peaks()
+    B = args.batch
+    extra = {}
+    sampler = None
 
-    def step(i):
-        lms.lmhead_sample(H, W, temperature=T, seeds=seeds, positions=pos_all[i], out=out,
-                          workspace=workspace)
+    if args.workload in FUSED:
+        w = make_workload(args.workload, B, args.D, args.V)
+        D, V = w.D, w.V
+        H, W = w.H.to(dev), w.W.to(dev)
+        T, seeds = w.temperature.to(dev), w.seeds.to(dev)
+        bias = None if w.bias is None else w.bias.to(dev)
+        mask = None if w.mask is None else w.mask.to(dev)
+        # positions advance with the step: one row per step, made before timing
+        pos_all = (w.positions[None, :] + torch.arange(n_steps)[:, None]).contiguous().to(dev)
+        tv, nt, ws_bytes, path = lms.tile_info(lms.OP_LMHEAD, B, D, V)
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        out = torch.empty(B, dtype=torch.int64, device=dev)
+        wide = w.noise_mode == 1
+        kw = dict(temperature=T, seeds=seeds, bias=bias, mask=mask, base_seed=w.base_seed,
+                  offset=w.offset, wide=wide, out=out, workspace=workspace)
+        launches_per_step = (1 + (B - 1) // 256 if path == lms.PATH_TCGEN05 else 1) + 1
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize(dev)
-    sampler = ClockSampler(local) if rank == 0 else None
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    barrier()
-    torch.cuda.synchronize(dev)
-    t0 = time.time()
-    ev[0].record(stream)
-    for k in range(args.steps):
-        step(args.warmup + k)
-        ev[k + 1].record(stream)
-    torch.cuda.synchronize(dev)
-    t1 = time.time()
-    barrier()
-    per_step_ms = [ev[k].elapsed_time(ev[k + 1]) for k in range(args.steps)]
-    total_ms = ev[0].elapsed_time(ev[args.steps])
+        def step(i):
+            lms.lmhead_sample(H, W, positions=pos_all[i], **kw)
+
+        alg = algorithmic_bytes(B, D, V, nt, bias is not None, mask is not None)
+        flops = 2 * B * V * D
+        config = {"workload": w.name, "B": B, "D": D, "V": V, "noise": "wide53" if wide else "fp32",
+                  "path": {1: "gemv", 2: "tcgen05"}[path], "tile_v": tv,
+                  "l2": "inputs larger than L2 (W is %.2f GB), no flush" % (V * D * 2 / 1e9)}
+        kernel = "lmhead_tc_kernel + stage2_kernel (one step, CUDA events)"
+    elif args.workload == "logits":
+        V = args.V or 131072
+        D = 0
+        dt = torch.bfloat16 if args.logits_dtype == "bf16" else torch.float32
+        logits = workloads.logits_normal(B, V, std=2.0, seed=5, dtype=dt).to(dev)
+        T = torch.full((B,), 0.7, device=dev)
+        seeds = 1000 + torch.arange(B, dtype=torch.int64, device=dev)
+        pos_all = torch.arange(n_steps, dtype=torch.int64)[:, None].expand(n_steps, B).contiguous().to(dev)
+        tv, nt, ws_bytes, _ = lms.tile_info(lms.OP_LOGITS, B, 0, V)
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        out = torch.empty(B, dtype=torch.int64, device=dev)
+        launches_per_step = 2
+
+        def step(i):
+            lms.sample_from_logits(logits, temperature=T, seeds=seeds, positions=pos_all[i], out=out,
+                                   workspace=workspace)
+
+        alg = B * V * logits.element_size() + 2 * B * nt * 8 + B * 28
+        flops = 0
+        config = {"workload": f"sample_from_logits B={B} V={V} {args.logits_dtype} logits ~ N(0, 4)",
+                  "B": B, "V": V, "noise": "fp32", "tile_v": tv,
+                  "l2": "inputs %s L2 (%.0f MB)" % ("larger than" if alg > 130e6 else "within", alg / 1e6)}
+        kernel = "logits_stage1_kernel + stage2_kernel (one step, CUDA events)"
+    elif args.workload == "noise":
+        V = args.V or 151936
+        D = 0
+        seeds = 1000 + torch.arange(B, dtype=torch.int64, device=dev)
+        pos_all = torch.arange(n_steps, dtype=torch.int64)[:, None].expand(n_steps, B).contiguous().to(dev)
+        g = torch.empty(B, V, dtype=torch.float32, device=dev)
+        launches_per_step = 1
+
+        def step(i):
+            lms.philox_fill_noise(B, V, kind="gumbel", seeds=seeds, positions=pos_all[i], out=g)
+
+        alg = B * V * 4 + B * 16
+        flops = 0
+        config = {"workload": f"philox_fill_noise gumbel B={B} V={V}", "B": B, "V": V,
+                  "noise": "fp32", "l2": "output %.0f MB" % (alg / 1e6)}
+        kernel = "noise_fill_kernel (one launch per step)"
+    else:
+        raise SystemExit(f"unknown workload {args.workload}")
+
+    if rank == 0:
+        sampler = ClockSampler(local)
+    avg_ms, per_ms, t0, t1 = _time_steps(step, args.warmup, args.steps, dev, stream)
     clocks = sampler.stop(t0, t1) if sampler else None
-    ms_per_step = max_over_ranks(total_ms / args.steps, dev)
+    ms_per_step = max_over_ranks(avg_ms, dev)
     us = ms_per_step * 1e3
 
-    # e2e: the step's inputs from pinned host memory, the tokens back to pinned host memory
-    H_h = w.H.pin_memory()
-    T_h, seeds_h = w.temperature.pin_memory(), w.seeds.pin_memory()
-    pos_h = pos_all.cpu().pin_memory()
-    out_h = torch.empty(B, dtype=torch.int64).pin_memory()
-    H_d, T_d, s_d = torch.empty_like(H), torch.empty_like(T), torch.empty_like(seeds)
-    p_d = torch.empty(B, dtype=torch.int64, device=dev)
+    e2e = None
+    if args.workload in FUSED:
+        # e2e: the step's per-request inputs from pinned host memory, the tokens back to pinned
+        # host memory; W is a resident weight.
+        host = {"H": w.H, "T": w.temperature, "seeds": w.seeds}
+        if w.bias is not None:
+            host["bias"] = w.bias
+        if w.mask is not None:
+            host["mask"] = w.mask
+        host = {k: v.pin_memory() for k, v in host.items()}
+        pos_h = pos_all.cpu().pin_memory()
+        devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+        p_d = torch.empty(B, dtype=torch.int64, device=dev)
+        out_h = torch.empty(B, dtype=torch.int64).pin_memory()
 
-    def e2e_step(i):
-        H_d.copy_(H_h, non_blocking=True)
-        T_d.copy_(T_h, non_blocking=True)
-        s_d.copy_(seeds_h, non_blocking=True)
-        p_d.copy_(pos_h[i], non_blocking=True)
-        lms.lmhead_sample(H_d, W, temperature=T_d, seeds=s_d, positions=p_d, out=out,
-                          workspace=workspace)
-        out_h.copy_(out, non_blocking=True)
+        def e2e_step(i):
+            for k, v in host.items():
+                devb[k].copy_(v, non_blocking=True)
+            p_d.copy_(pos_h[i], non_blocking=True)
+            lms.lmhead_sample(devb["H"], W, temperature=devb["T"], seeds=devb["seeds"], positions=p_d,
+                              bias=devb.get("bias"), mask=devb.get("mask"), base_seed=w.base_seed,
+                              offset=w.offset, wide=wide, out=out, workspace=workspace)
+            out_h.copy_(out, non_blocking=True)
 
-    for i in range(args.warmup):
-        e2e_step(i)
-    torch.cuda.synchronize(dev)
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for k in range(args.steps):
-        e2e_step(args.warmup + k)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
-    e2e_us = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev) * 1e3
-    h2d = B * D * 2 + B * 4 + B * 8 + B * 8
-    d2h = B * 8
+        e2e_ms, _, _, _ = _time_steps(e2e_step, args.warmup, args.steps, dev, stream)
+        e2e = {"value": round(max_over_ranks(e2e_ms, dev) * 1e3, 2), "unit": UNIT,
+               "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()) + B * 8,
+               "d2h_bytes_per_step": B * 8}
 
     if rank != 0:
         return
-    peaks = measured_peaks()
-    alg = algorithmic_bytes(B, D, V, nt)
-    achieved = alg / (us * 1e-6) / 1e9
-    traffic = recorded_traffic()
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
-                "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)",
-                "kernel": "lmhead_tc_kernel + stage2_kernel (one step, CUDA events)",
-                "algorithmic_bytes": alg}
+    achieved_gbs = alg / (us * 1e-6) / 1e9
+    t_hbm = alg / (peaks["hbm_gbs"] * 1e9)
+    t_tensor = flops / (peaks["bf16_tflops"] * 1e12) if flops else 0.0
+    if t_tensor > t_hbm:
+        tf = flops / (us * 1e-6) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+                    "peak_source": peaks["source"] + " (MEASURED_PEAKS.json bf16_tflops, burst cuBLAS)",
+                    "algorithmic_flops": flops}
+    else:
+        roofline = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(achieved_gbs / peaks["hbm_gbs"], 4),
+                    "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)",
+                    "algorithmic_bytes": alg}
+    traffic = recorded_traffic(args.workload, B) if args.workload in FUSED else None
+    roofline["traffic"] = traffic["dram_bytes_per_launch"] if traffic else None
+    roofline["kernel"] = kernel
     line = {"metric": METRIC, "value": round(us, 2), "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": w.name, "B": B, "D": D, "V": V, "noise": "fp32",
-                       "path": {1: "gemv", 2: "tcgen05"}[path], "tile_v": tv,
-                       "l2": "inputs larger than L2 (W is %.2f GB), no flush" % (V * D * 2 / 1e9),
-                       "parallelism": "replicas" if ws > 1 else "single-gpu"},
-            "hbm_gbs": round(achieved, 1), "samples_per_s": round(B / (us * 1e-6), 1),
-            "p50_us": round(statistics.median(per_step_ms) * 1e3, 2),
-            "p10_us": round(sorted(per_step_ms)[len(per_step_ms) // 10] * 1e3, 2),
-            "p90_us": round(sorted(per_step_ms)[(len(per_step_ms) * 9) // 10] * 1e3, 2),
+            "config": dict(config, parallelism="replicas" if ws > 1 else "single-gpu"),
+            "hbm_gbs": round(achieved_gbs, 1), "samples_per_s": round(B / (us * 1e-6), 1),
+            "p50_us": round(statistics.median(per_ms) * 1e3, 2),
+            "p10_us": round(sorted(per_ms)[len(per_ms) // 10] * 1e3, 2),
+            "p90_us": round(sorted(per_ms)[(len(per_ms) * 9) // 10] * 1e3, 2),
             "roofline": roofline, "clocks": clocks,
-            "e2e": {"value": round(e2e_us, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps}
+    if flops:
+        line["tflops"] = round(flops / (us * 1e-6) / 1e12, 1)
+    if e2e is not None:
+        line["e2e"] = e2e
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        if args.workload in FUSED:
+            line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        elif args.workload == "logits":
+            threads = os.cpu_count() or 1
+            vs = min(V, 16384)
+            t = oracle_logits_time(logits.cpu(), vs, threads)
+            line["cpu_baseline"] = {"value": t / vs * V * 1e6, "unit": UNIT, "cores": threads,
+                                    "kind": "oracle",
+                                    "sample": f"B={B} rows x first {vs} of {V} logits, scaled linearly"}
+    line.update(extra)
     print(json.dumps(line), flush=True)
 
 
@@ -329,9 +475,12 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=25)
-    ap.add_argument("--batch", type=int, default=64)
-    ap.add_argument("--D", type=int, default=4096)
-    ap.add_argument("--V", type=int, default=151936)
+    ap.add_argument("--workload", default="qwen3-8b",
+                    choices=list(FUSED) + ["logits", "noise"])
+    ap.add_argument("--batch", type=int, default=0)
+    ap.add_argument("--D", type=int, default=0)
+    ap.add_argument("--V", type=int, default=0)
+    ap.add_argument("--logits-dtype", choices=["fp32", "bf16"], default="bf16")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -339,6 +488,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.batch <= 0:
+        args.batch = default_batch(args.workload)
     if args.impl == "reference":
         run_reference(args)
     else:
