@@ -71,7 +71,9 @@ typedef enum { LMS_OP_LMHEAD = 0, LMS_OP_LOGITS = 1 } lms_op;
 typedef enum {
     LMS_PATH_AUTO = 0,            /* the library's choice (currently tcgen05 for every B)      */
     LMS_PATH_GEMV = 1,            /* CUDA-core dot products (B <= LMS_GEMV_MAX_B)                */
-    LMS_PATH_TCGEN05 = 2          /* TMA -> shared memory -> tcgen05.mma -> TMEM accumulators  */
+    LMS_PATH_TCGEN05 = 2,         /* TMA -> shared memory -> tcgen05.mma -> TMEM accumulators  */
+    LMS_PATH_TCGEN05_PAIR = 3     /* the same on CTA pairs: tcgen05.mma.cta_group::2, M = 256;
+                                     each CTA streams half of H (for large batches)            */
 } lms_path;
 
 #define LMS_ROW_OK 0

@@ -26,7 +26,7 @@ LMS_OK, LMS_ERR_INVALID_ARG, LMS_ERR_UNSUPPORTED, LMS_ERR_WORKSPACE, LMS_ERR_CUD
 NOISE_FP32, NOISE_WIDE53 = 0, 1
 DTYPE_F32, DTYPE_BF16 = 0, 1
 OP_LMHEAD, OP_LOGITS = 0, 1
-PATH_AUTO, PATH_GEMV, PATH_TCGEN05 = 0, 1, 2
+PATH_AUTO, PATH_GEMV, PATH_TCGEN05, PATH_TCGEN05_PAIR = 0, 1, 2, 3
 NOISE_KINDS = {"words": 0, "uniform": 1, "exponential": 2, "gumbel": 3}
 ROW_OK, ROW_NO_CANDIDATE, ROW_BAD_TEMPERATURE, ROW_DEVICE_TIMEOUT = range(4)
 DEBUG_WITHHOLD_FIRST_LOAD = 1

@@ -25,13 +25,12 @@
 #include "lms.h"
 #include "lms_device.cuh"
 #include "lms_kernels.h"
+#include "tcgen05_common.cuh"
 
 namespace lms {
 namespace {
 
-constexpr int kTileV = 128;                       // tcgen05 M
-constexpr int kBK = 64;                           // K elements per stage (one 128-byte row)
-constexpr int kWStageBytes = kTileV * kBK * 2;    // 16 KB
+using namespace tc;
 constexpr int kMaxStages = 12;
 #ifndef LMS_TC_EPILOGUE_WARPS
 #define LMS_TC_EPILOGUE_WARPS 16
@@ -40,7 +39,6 @@ constexpr int kMaxStages = 12;
 // split the batch columns between them).
 constexpr int kEpilogueWarps = LMS_TC_EPILOGUE_WARPS;
 static_assert(kEpilogueWarps % 4 == 0, "epilogue warps come in groups of four");
-constexpr uint32_t kEpiBarrierId = 1;
 
 struct TcParams {
     SampleArgs a;
@@ -54,193 +52,8 @@ struct TcParams {
 };
 
 // ------------------------------------------------------------------------------------------
-// PTX wrappers
-// ------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-__device__ __forceinline__ uint64_t global_timer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Waits until the barrier phase of the given parity has completed.  Gives up (returns false)
-// when `timeout_ns` passes or, if `err` is non-null, when another role has flagged an error.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
-                                          const volatile int* err) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t deadline = global_timer_ns() + timeout_ns;
-    for (uint32_t spin = 1;; ++spin) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((spin & 31u) == 0u) {
-            if (err != nullptr && *err != 0) return false;
-            if (global_timer_ns() > deadline) return false;
-        }
-    }
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
-// 2-D tiled TMA load (box given by the descriptor) completing on an mbarrier.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y,
-                                            uint32_t bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before_sync() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tc_fence_after_sync() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate; issued by one thread.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrive once on `bar` when all tcgen05 operations issued so far by this thread have completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-
-// 32 TMEM lanes x 8 consecutive 32-bit columns -> 8 registers per thread (lane = thread).
-__device__ __forceinline__ void tmem_load_8(uint32_t taddr, uint32_t (&r)[8]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void epi_barrier(int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(kEpiBarrierId), "r"(threads) : "memory");
-}
-
-// Barrier over the epilogue warps that also ANDs a flag across them, so that every epilogue
-// thread takes the same branch after a bounded wait (no thread can be left at a barrier).
-__device__ __forceinline__ bool epi_barrier_and(int threads, bool flag) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred p, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"(flag ? 1u : 0u), "r"(kEpiBarrierId), "r"(threads)
-        : "memory");
-    return r != 0;
-}
-
-// (score, index) as one 64-bit key whose unsigned order is the lexicographic order "larger
-// score, then smaller index": the score's bits mapped to a monotone unsigned integer in the high
-// half (-0 folded onto +0 first; scores are never NaN here), the complemented index in the low
-// half.  Key 0 is below every real candidate.
-__device__ __forceinline__ unsigned long long pack_candidate(float s, int idx) {
-    const uint32_t f = __float_as_uint(s + 0.0f);
-    const uint32_t ord = (f & 0x80000000u) ? ~f : (f | 0x80000000u);
-    return (static_cast<unsigned long long>(ord) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(idx));
-}
-
-__device__ __forceinline__ float unpack_score(unsigned long long key) {
-    const uint32_t ord = static_cast<uint32_t>(key >> 32);
-    return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7fffffffu) : ~ord);
-}
-
-__device__ __forceinline__ int unpack_index(unsigned long long key) {
-    return static_cast<int>(~static_cast<uint32_t>(key));
-}
-
-// Shared-memory matrix descriptor for a K-major operand tile written by TMA with the 128-byte
-// swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), the leading
-// byte offset unused for this layout, descriptor version 1, layout code 2 = 128-byte swizzle.
-__device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>(1u) << 16;
-    d |= static_cast<uint64_t>(1024u >> 4) << 32;
-    d |= static_cast<uint64_t>(1u) << 46;
-    d |= static_cast<uint64_t>(2u) << 61;
-    return d;
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major, N and M.
-__host__ __device__ constexpr uint32_t mma_idesc_bf16(int n, int m) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
-           (static_cast<uint32_t>(m >> 4) << 24);
-}
-
-// ------------------------------------------------------------------------------------------
 // Shared-memory layout (offsets from a 1024-byte aligned base)
 // ------------------------------------------------------------------------------------------
-// Per epilogue warp: an 8-column x 32-row transpose tile, rows padded to 36 floats so that both
-// the row-wise stores and the 16-byte column-wise loads are free of bank conflicts.
-constexpr int kTrStride = 36;
-constexpr uint32_t kTrWarpBytes = 8 * kTrStride * 4;
-
 struct SmemLayout {
     uint32_t stages_off, bars_off, misc_off, rows_off, red_off, tr_off, total;
     __host__ __device__ SmemLayout(int stages, uint32_t stage_bytes, int n_pad, int epi_warps) {
@@ -392,14 +205,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
         const int epi_threads = 32 * kEpiWarps;
         const int quad = warp & 3;                       // TMEM lanes 32*quad .. 32*quad+31
         const int col_group = (warp - 2) >> 2;           // which column chunks this warp takes
-        constexpr int kColGroups = kEpiWarps / 4;
-        const int n_chunks = (B + 7) / 8;                // 8-column chunks
         float* tr = reinterpret_cast<float*>(base + L.tr_off + (warp - 2) * kTrWarpBytes);
-        // After the transpose, thread (lane) owns column (lane & 7) of the chunk and the eight
-        // consecutive rows 8 * (lane >> 3) .. + 7 of this quadrant: two Philox calls (fp32
-        // noise) or four (wide noise) cover them.
-        const int my_col = lane & 7;
-        const int my_r0 = (lane >> 3) * 8;
         int i = 0;
         bool ok = true;
         for (int64_t tile = blockIdx.x; tile < nt; tile += gridDim.x, ++i) {
@@ -419,57 +225,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
             tc_fence_after_sync();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) +
                                    static_cast<uint32_t>(ab * n_pad);
-            const int64_t v0 = tile * kTileV + 32 * quad + my_r0;   // a multiple of 8
-            for (int cc = col_group; cc < n_chunks; cc += kColGroups) {
-                uint32_t acc[8];
-                tmem_load_8(t_row + 8u * cc, acc);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) tr[j * kTrStride + lane] = __uint_as_float(acc[j]);
-                __syncwarp();
-                float y[8];
-                const float4 y0 = *reinterpret_cast<const float4*>(tr + my_col * kTrStride + my_r0);
-                const float4 y1 = *reinterpret_cast<const float4*>(tr + my_col * kTrStride + my_r0 + 4);
-                __syncwarp();
-                y[0] = y0.x; y[1] = y0.y; y[2] = y0.z; y[3] = y0.w;
-                y[4] = y1.x; y[5] = y1.y; y[6] = y1.z; y[7] = y1.w;
-                const int b = cc * 8 + my_col;
-                float best_s = -CUDART_INF_F;
-                int best_i = kNoIndex;
-                if (b < B && v0 < a.V) {
-                    const RowParams p = rows[b];
-                    if (!(p.flags & kRowInvalid)) {
-                        float g[8];
-                        if (p.flags & kRowGreedy) {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) g[e] = 0.0f;
-                        } else {
-                            gumbel_run<kWide, 8>(p.key, static_cast<uint32_t>(v0), g);
-                        }
-                        const int64_t row = a.row0 + b;
-                        const float* brow = a.bias ? a.bias + row * a.ld_bias : nullptr;
-                        // the eight entries share one mask word (v0 is a multiple of 8)
-                        const uint32_t mword =
-                            a.mask ? (__ldg(a.mask + row * a.ld_mask + (v0 >> 5)) >> (v0 & 31)) : 0xffu;
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int64_t v = v0 + e;
-                            if (v < a.V) {
-                                const float bias = brow ? __ldg(brow + v) : 0.0f;
-                                const float sc = perturb(p, y[e], bias, (mword >> e) & 1u, g[e]);
-                                if (sc > best_s) { best_s = sc; best_i = static_cast<int>(v); }
-                            }
-                        }
-                    }
-                }
-                // the four threads holding this column (lanes c, c + 8, c + 16, c + 24)
-#pragma unroll
-                for (int off = 8; off <= 16; off <<= 1) {
-                    const float so = __shfl_xor_sync(0xffffffffu, best_s, off);
-                    const int io = __shfl_xor_sync(0xffffffffu, best_i, off);
-                    if (better(so, io, best_s, best_i)) { best_s = so; best_i = io; }
-                }
-                if (lane < 8 && b < B) atomicMax(red + b, pack_candidate(best_s, best_i));
-            }
+            epilogue_tile_columns<kEpiWarps, kWide>(a, rows, red, tr, t_row, tile, quad, col_group, lane, B);
             // The accumulator buffer is free for the MMA of tile i+2.
             tc_fence_before_sync();
             __syncwarp();

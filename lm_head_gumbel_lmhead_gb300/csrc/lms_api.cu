@@ -222,7 +222,7 @@ lms_status lms_lmhead_sample(const void* H, int64_t ldh, const void* W, int64_t 
     if (path == LMS_PATH_GEMV && (B > LMS_GEMV_MAX_B || static_cast<size_t>(B) * D * 2 > 200 * 1024))
         path = (params->path == LMS_PATH_GEMV) ? -1 : LMS_PATH_TCGEN05;
     if (path == -1) return fail(LMS_ERR_UNSUPPORTED, "GEMV path needs B <= %d and B*D*2 <= 200 KB", LMS_GEMV_MAX_B);
-    if (path != LMS_PATH_GEMV && path != LMS_PATH_TCGEN05)
+    if (path != LMS_PATH_GEMV && path != LMS_PATH_TCGEN05 && path != LMS_PATH_TCGEN05_PAIR)
         return fail(LMS_ERR_INVALID_ARG, "unknown path %d", params->path);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -241,15 +241,19 @@ lms_status lms_lmhead_sample(const void* H, int64_t ldh, const void* W, int64_t 
         for (int64_t r0 = 0; r0 < B; r0 += kTcMaxBatchPerLaunch) {
             const int64_t nb = (B - r0 < kTcMaxBatchPerLaunch) ? B - r0 : kTcMaxBatchPerLaunch;
             const int n_pad = static_cast<int>(nb < 16 ? 16 : (nb + 15) / 16 * 16);
+            const bool pair = path == LMS_PATH_TCGEN05_PAIR;
             CUtensorMap tmH;
-            if ((st = encode_bf16_map(&tmH, H, B, D, ldh, n_pad)) != LMS_OK) return st;
+            if ((st = encode_bf16_map(&tmH, H, B, D, ldh, pair ? n_pad / 2 : n_pad)) != LMS_OK) return st;
             lms::SampleArgs ac = a;
             ac.B = nb;
             ac.row0 = r0;
             ac.cand_score = a.cand_score + r0 * t.n_tiles;
             ac.cand_index = a.cand_index + r0 * t.n_tiles;
-            e = lms::launch_lmhead_tc(tmW, tmH, D, n_pad, wide, timeout_ms, params->debug_flags, ac, s);
-            if (e != cudaSuccess) return cuda_fail(e, "tcgen05 Stage-1 launch");
+            e = pair ? lms::launch_lmhead_tc_pair(tmW, tmH, D, n_pad, wide, timeout_ms,
+                                                  params->debug_flags, ac, s)
+                     : lms::launch_lmhead_tc(tmW, tmH, D, n_pad, wide, timeout_ms,
+                                             params->debug_flags, ac, s);
+            if (e != cudaSuccess) return cuda_fail(e, pair ? "tcgen05 pair Stage-1 launch" : "tcgen05 Stage-1 launch");
         }
     }
     e = lms::launch_stage2(a.cand_score, a.cand_index, t.n_tiles, B, params->temperature, out,

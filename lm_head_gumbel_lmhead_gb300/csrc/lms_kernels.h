@@ -46,6 +46,11 @@ cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int
                              bool wide, uint32_t timeout_ms, uint32_t debug_flags,
                              const SampleArgs& a, cudaStream_t stream);
 
+// The CTA-pair tcgen05 path (cta_group::2, M = 256): tmH boxes are 64 x (n_pad / 2).
+cudaError_t launch_lmhead_tc_pair(const CUtensorMap& tmW, const CUtensorMap& tmH, int64_t D,
+                                  int n_pad, bool wide, uint32_t timeout_ms, uint32_t debug_flags,
+                                  const SampleArgs& a, cudaStream_t stream);
+
 int device_sm_count();
 
 // Sets the thread-local message that lms_last_error() returns.

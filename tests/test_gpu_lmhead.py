@@ -189,3 +189,43 @@ def test_timeout_reports_status_and_context_survives():
     assert (ci == -2).any()
     # the next call on the same context is correct
     full_parity(w, lms.PATH_TCGEN05)
+
+
+# ---- the CTA-pair tcgen05 path (cta_group::2, M = 256) ----
+@pytest.mark.parametrize("B,D,V,wide", [(1, 64, 1000, False), (17, 200, 1300, True),
+                                        (40, 512, 3000, False), (128, 256, 2000, True)])
+def test_tcgen05_pair_ragged(B, D, V, wide):
+    full_parity(_ragged(B, D, V, seed=B * 5 + D, wide=wide), lms.PATH_TCGEN05_PAIR)
+
+
+@pytest.mark.parametrize("B,D,V,wide", [(256, 128, 1500, True), (300, 192, 1300, False)])
+def test_tcgen05_pair_ragged_wide_batches(B, D, V, wide):
+    full_parity(_ragged(B, D, V, seed=B * 5 + D, wide=wide), lms.PATH_TCGEN05_PAIR)
+
+
+def test_tcgen05_pair_matches_single_cta_path():
+    # same accumulation (fp32, same K order per 128-row tile): bit-equal tokens and candidates
+    w = _ragged(96, 512, 5000, seed=21, features=True)
+    d = to_dev(w)
+    a = run_fused(w, d, lms.PATH_TCGEN05)
+    b = run_fused(w, d, lms.PATH_TCGEN05_PAIR)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    assert np.array_equal(a[3], b[3])
+
+
+def test_tcgen05_pair_timeout_reports_status():
+    w = _ragged(20, 256, 4000, seed=13, features=False)
+    d = to_dev(w)
+    out, st, _, ci = run_fused(w, d, lms.PATH_TCGEN05_PAIR, timeout_ms=20,
+                               debug_flags=lms.DEBUG_WITHHOLD_FIRST_LOAD)
+    assert (st == lms.ROW_DEVICE_TIMEOUT).all() and (out == -1).all()
+    full_parity(w, lms.PATH_TCGEN05_PAIR)
+
+
+@pytest.mark.parametrize("B", [64, 256])
+def test_qwen3_8b_shape_pair_sampled_rows(qwen_w, B):
+    w = qwen_w
+    sub = workloads.Workload(w.name, B, w.D, w.V, w.H[:B].contiguous(), w.W, w.temperature[:B],
+                             w.seeds[:B], w.positions[:B], None, None, w.noise_mode)
+    out, st, _ = sampled_parity(sub, [0, B // 2, B - 1], lms.PATH_TCGEN05_PAIR)
+    assert (st == 0).all()
