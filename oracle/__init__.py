@@ -66,6 +66,9 @@ def _load():
                                                    P, P, i64, P, i64, u64, u64, i32, i64, P, P,
                                                    P, P, P, P, i32]
             lib.orc_lmhead_sample_rows.restype = ctypes.c_int
+            lib.orc_sample_filtered.argtypes = [P, i64, i64, i64, P, P, P, P, i64, P, i64, u64, u64,
+                                                i32, P, P, P, i32, ctypes.c_double,
+                                                ctypes.c_double, P, P, P, i32]
             lib.orc_uniform.argtypes = [ctypes.c_uint32, ctypes.c_uint32, i32]
             lib.orc_uniform.restype = ctypes.c_double
             _lib = lib
@@ -260,3 +263,33 @@ def lmhead_scores_at(H_bits, W_bits, rows, cols, *, temperature=None, seeds=None
         ld_bias, _ptr(mask_a), ld_mask, base_seed, offset, int(bool(wide)), rows.shape[0],
         _ptr(rows), _ptr(cols), _ptr(s))
     return s
+
+
+def sample_filtered(logits, *, B=None, temperature=None, seeds=None, positions=None, bias=None,
+                    mask=None, base_seed=0, offset=0, wide=False, top_k=None, top_p=None,
+                    min_p=None, k_max=1024, p_shift=0.0, minp_scale=1.0, threads=None):
+    """Filtered race over materialised logits: top-k -> top-p -> min-p on t = (y + bias) / T,
+    then the Gumbel race over the kept tokens (spec-decode-ops "Semantics"; sampling-kernel
+    guide steps 6-8).  Returns (out, status, kept-set size).  p_shift / minp_scale move the
+    top-p / min-p thresholds, to find out which decisions sit on a floating-point boundary."""
+    y = np.asarray(logits, dtype=np.float64)
+    if y.ndim == 1:
+        ld_y, V = 0, y.shape[0]
+    else:
+        B = y.shape[0] if B is None else B
+        ld_y, V = y.shape[1], y.shape[1]
+    y = np.ascontiguousarray(y)
+    T = _c(temperature, np.float64)
+    bias_a = _c(bias, np.float64)
+    ld_bias = 0 if bias_a is None or bias_a.ndim == 1 else bias_a.shape[1]
+    mask_a = _c(mask, np.uint32)
+    ld_mask = 0 if mask_a is None or mask_a.ndim == 1 else mask_a.shape[1]
+    seeds_a, pos_a = _c(seeds, np.int64), _c(positions, np.int64)
+    tk, tp, mp = _c(top_k, np.int32), _c(top_p, np.float64), _c(min_p, np.float64)
+    out = np.empty(B, np.int64); status = np.empty(B, np.int32); kept = np.empty(B, np.int32)
+    _load().orc_sample_filtered(_ptr(y), ld_y, B, V, _ptr(T), _ptr(seeds_a), _ptr(pos_a),
+                                _ptr(bias_a), ld_bias, _ptr(mask_a), ld_mask, base_seed, offset,
+                                int(bool(wide)), _ptr(tk), _ptr(tp), _ptr(mp), int(k_max),
+                                float(p_shift), float(minp_scale), _ptr(out), _ptr(status),
+                                _ptr(kept), threads or default_threads())
+    return out, status, kept

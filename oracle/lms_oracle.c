@@ -415,3 +415,136 @@ int orc_lmhead_sample_rows(const uint16_t* H, int64_t ldh, const uint16_t* W, in
     free(y);
     return 0;
 }
+
+/* ------------------------------------------------------------------------------------------ */
+/* Filtered race: top-k -> top-p -> min-p, then the Gumbel race over the kept tokens           */
+/* [SDO "Semantics"; SK reasoning steps 6-8, "Correctness requirements"]                      */
+/* ------------------------------------------------------------------------------------------ */
+/* Readings (also listed with the design notes):
+ *   - t = (y + bias) / T as in the race (masked -> -inf); T == 0 rows are greedy (filters cannot
+ *     remove the top token, so the greedy token is the filtered one too).
+ *   - Sorted order: t descending, then v ascending.  top-k keeps the first k of that order
+ *     (1 <= top_k; values above k_max count as k_max; <= 0 or >= V = off).
+ *   - top-p (0 < top_p < 1) keeps the shortest prefix of the top-k set (or, with top-k off, of
+ *     the first k_max tokens) whose probability mass -- normalised over that set -- reaches
+ *     top_p, the crossing token included.
+ *   - min-p (0 < min_p <= 1) keeps p_i >= min_p * p_max, i.e. t_i - t_max >= log(min_p).
+ *   - Every filter keeps the top token.  The race over the kept set samples the softmax
+ *     renormalised to it (Gumbel-max over a subset). */
+
+typedef struct { double t; int64_t v; } orc_tv;
+
+static int orc_cmp_desc(const void* x, const void* y) {
+    const orc_tv* a = (const orc_tv*)x; const orc_tv* b = (const orc_tv*)y;
+    if (a->t > b->t) return -1;
+    if (a->t < b->t) return 1;
+    return (a->v < b->v) ? -1 : (a->v > b->v);
+}
+
+typedef struct {
+    const double* y; int64_t ld_y; int64_t B, V;
+    const double* T; const int64_t* seeds; const int64_t* positions;
+    const double* bias; int64_t ld_bias; const uint32_t* mask; int64_t ld_mask;
+    uint64_t base_seed, offset; int wide;
+    const int32_t* top_k; const double* top_p; const double* min_p; int32_t k_max;
+    double p_shift;      /* added to top_p (to probe the decision boundary) */
+    double minp_scale;   /* multiplies min_p (same) */
+    int64_t* out; int32_t* status; int32_t* kept;
+} orc_filt_args;
+
+static void orc_filtered_row(const orc_filt_args* f, int64_t b) {
+    int64_t V = f->V;
+    double T = f->T ? f->T[b] : 1.0;
+    if (isnan(T) || T < 0.0) { f->out[b] = -1; f->status[b] = 2; if (f->kept) f->kept[b] = 0; return; }
+    const double* yrow = f->y + b * f->ld_y;
+    orc_rows_args a = {NULL, 0, f->B, V, f->T, f->seeds, f->positions, f->bias, f->ld_bias, f->mask,
+                       f->ld_mask, f->base_seed, f->offset, f->wide, 0, NULL, NULL, NULL, NULL,
+                       NULL, NULL, NULL, NULL, 0};
+    /* transformed logits (no noise), -inf for masked / NaN */
+    orc_tv* tv = (orc_tv*)malloc(sizeof(orc_tv) * (size_t)V);
+    int64_t n_fin = 0;
+    for (int64_t v = 0; v < V; ++v) {
+        double t = -INFINITY;
+        int ok = 1;
+        if (f->mask) ok = (f->mask[b * f->ld_mask + (v >> 5)] >> (v & 31)) & 1u;
+        if (ok) {
+            double bias = f->bias ? f->bias[b * f->ld_bias + v] : 0.0;
+            t = (T == 0.0) ? yrow[v] + bias : (yrow[v] + bias) / T;
+            if (isnan(t)) t = -INFINITY;
+        }
+        tv[v].t = t; tv[v].v = v;
+        if (t > -INFINITY) ++n_fin;
+    }
+    if (n_fin == 0) { f->out[b] = -1; f->status[b] = 1; if (f->kept) f->kept[b] = 0; free(tv); return; }
+    qsort(tv, (size_t)V, sizeof(orc_tv), orc_cmp_desc);   /* -inf entries sort last */
+    int32_t k = f->top_k ? f->top_k[b] : 0;
+    int64_t kmax = f->k_max > 0 ? f->k_max : 1024;
+    double p = f->top_p ? f->top_p[b] + f->p_shift : 1.0;
+    double mp = f->min_p ? f->min_p[b] * f->minp_scale : 0.0;
+    int topk_on = k >= 1 && k < V;
+    int topp_on = f->top_p && f->top_p[b] > 0.0 && f->top_p[b] < 1.0;
+    int64_t n = n_fin;                                    /* kept prefix length */
+    if (topk_on) n = (k > kmax ? kmax : k) < n ? (k > kmax ? kmax : k) : n;
+    else if (topp_on && n > kmax) n = kmax;
+    if (topp_on) {
+        double z = 0.0;
+        for (int64_t i = 0; i < n; ++i) z += exp(tv[i].t - tv[0].t);
+        double c = 0.0;
+        int64_t m = n;
+        for (int64_t i = 0; i < n; ++i) {
+            c += exp(tv[i].t - tv[0].t) / z;
+            if (c >= p) { m = i + 1; break; }
+        }
+        n = m;
+    }
+    if (f->min_p && f->min_p[b] > 0.0) {
+        double thr = tv[0].t + log(mp);
+        int64_t m = 1;
+        while (m < n && tv[m].t >= thr) ++m;
+        n = m;
+    }
+    if (n < 1) n = 1;
+    /* race over the kept prefix */
+    double best = -INFINITY;
+    int64_t arg = -1;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t v = tv[i].v;
+        double s = orc_score(&a, b, v, yrow[v]);
+        if (arg < 0 || s > best || (s == best && v < arg)) { best = s; arg = v; }
+    }
+    f->out[b] = arg;
+    f->status[b] = 0;
+    if (f->kept) f->kept[b] = (int32_t)n;
+    free(tv);
+}
+
+typedef struct { const orc_filt_args* f; int64_t b0, b1; } orc_filt_job;
+
+static void* orc_filt_worker(void* p) {
+    const orc_filt_job* j = (const orc_filt_job*)p;
+    for (int64_t b = j->b0; b < j->b1; ++b) orc_filtered_row(j->f, b);
+    return NULL;
+}
+
+/* Filtered race over materialised logits y [B][ld_y] (ld_y == 0 broadcasts one row). */
+void orc_sample_filtered(const double* y, int64_t ld_y, int64_t B, int64_t V, const double* T,
+                         const int64_t* seeds, const int64_t* positions, const double* bias,
+                         int64_t ld_bias, const uint32_t* mask, int64_t ld_mask,
+                         uint64_t base_seed, uint64_t offset, int wide, const int32_t* top_k,
+                         const double* top_p, const double* min_p, int32_t k_max, double p_shift,
+                         double minp_scale, int64_t* out, int32_t* status, int32_t* kept,
+                         int nthreads) {
+    orc_filt_args f = {y, ld_y, B, V, T, seeds, positions, bias, ld_bias, mask, ld_mask,
+                       base_seed, offset, wide, top_k, top_p, min_p, k_max, p_shift, minp_scale,
+                       out, status, kept};
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > B) nthreads = (int)B;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t th[256];
+    orc_filt_job jobs[256];
+    for (int i = 0; i < nthreads; ++i) {
+        jobs[i].f = &f; jobs[i].b0 = B * i / nthreads; jobs[i].b1 = B * (i + 1) / nthreads;
+        pthread_create(&th[i], NULL, orc_filt_worker, &jobs[i]);
+    }
+    for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+}
