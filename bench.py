@@ -19,6 +19,8 @@ Workloads (synthetic, seeded; the shapes of the FlashSampling page's measurement
 - ``large-vocab`` (B in 128/256/512): D = 8192, V = 262144, wide noise.
 - ``logits``: ``lms_sample_from_logits`` over materialised N(0, 4) logits, V = 131072.
 - ``noise``: ``lms_philox_fill_noise`` of Gumbel noise, B x V float32.
+- ``filtered``: ``lms_sample_from_logits_filtered`` with top-k 50 and top-p 0.9 at T = 0.7 over
+  bf16 logits, V = 131072 (the Megatron-LM PR's filter settings).
 
 Every input is larger than L2 (the fused workloads stream W of 1.05–4.3 GB), so no flush is needed.
 
@@ -199,7 +201,7 @@ def make_workload(name: str, B: int, D: int, V: int):
 
 
 def default_batch(name: str) -> int:
-    return {"large-vocab": 256, "logits": 64, "noise": 64}.get(name, 64)
+    return {"large-vocab": 256, "logits": 64, "noise": 64, "filtered": 64}.get(name, 64)
 
 
 # ------------------------------------------------------------------------------------------
@@ -367,6 +369,28 @@ def run_gpu(args):
                   "B": B, "V": V, "noise": "fp32", "tile_v": tv,
                   "l2": "inputs %s L2 (%.0f MB)" % ("larger than" if alg > 130e6 else "within", alg / 1e6)}
         kernel = "logits_stage1_kernel + stage2_kernel (one step, CUDA events)"
+    elif args.workload == "filtered":
+        V = args.V or 131072
+        D = 0
+        logits = workloads.logits_normal(B, V, std=2.0, seed=6, dtype=torch.bfloat16).to(dev)
+        T = torch.full((B,), 0.7, device=dev)
+        seeds = 1000 + torch.arange(B, dtype=torch.int64, device=dev)
+        top_k = torch.full((B,), 50, dtype=torch.int32, device=dev)
+        top_p = torch.full((B,), 0.9, device=dev)
+        pos_all = torch.arange(n_steps, dtype=torch.int64)[:, None].expand(n_steps, B).contiguous().to(dev)
+        out = torch.empty(B, dtype=torch.int64, device=dev)
+        launches_per_step = 1
+
+        def step(i):
+            lms.sample_from_logits_filtered(logits, temperature=T, seeds=seeds, positions=pos_all[i],
+                                            top_k=top_k, top_p=top_p, out=out)
+
+        alg = B * V * 2 + B * 44
+        flops = 0
+        config = {"workload": f"filtered sample_from_logits top-k 50 top-p 0.9 T 0.7 B={B} V={V} bf16",
+                  "B": B, "V": V, "noise": "fp32",
+                  "l2": "inputs %s L2 (%.0f MB)" % ("larger than" if alg > 130e6 else "within", alg / 1e6)}
+        kernel = "filtered_race_kernel (one launch per step)"
     elif args.workload == "noise":
         V = args.V or 151936
         D = 0
@@ -476,7 +500,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=25)
     ap.add_argument("--workload", default="qwen3-8b",
-                    choices=list(FUSED) + ["logits", "noise"])
+                    choices=list(FUSED) + ["logits", "noise", "filtered"])
     ap.add_argument("--batch", type=int, default=0)
     ap.add_argument("--D", type=int, default=0)
     ap.add_argument("--V", type=int, default=0)

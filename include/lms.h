@@ -153,6 +153,34 @@ lms_status lms_sample_from_logits(const void* logits, int32_t dtype, int64_t ld,
                                   int64_t V, const lms_sample_params* params, int64_t* out,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
+/* Per-row filters for lms_sample_from_logits_filtered (all device arrays [B], each may be NULL).
+ * spec-decode-ops "Semantics" and the sampling-kernel guide, reasoning steps 6-8:
+ *   top_k  keep the k largest t = (y + bias) / T (ties: smaller index first).  Off when
+ *          top_k[b] <= 0 or >= V; values above k_max count as k_max.
+ *   top_p  keep the shortest prefix of that sorted set (or, with top-k off, of the first k_max
+ *          tokens) whose probability mass, normalised over the set, reaches top_p; the crossing
+ *          token is kept.  Off unless 0 < top_p[b] < 1.
+ *   min_p  keep p >= min_p * p_max, i.e. t - t_max >= log(min_p).  Off unless 0 < min_p[b] <= 1.
+ * Applied in this order; each keeps the top token.  The Gumbel race then runs over the kept
+ * tokens with the same noise as lms_sample_from_logits, which samples the softmax renormalised
+ * to them.  Greedy rows (T == 0) take the argmax. */
+typedef struct {
+    const int32_t* top_k;
+    const float* top_p;
+    const float* min_p;
+    int32_t k_max;              /* candidate bound for top-k / top-p, 1..1024; 0 = 1024 */
+    int32_t reserved;           /* must be 0 */
+} lms_filter_params;
+
+/* The filtered race over materialised logits [B][ld] (fp32 or bf16; ld == 0 broadcasts one row):
+ * one CTA per row selects (radix select), sorts (bitonic, in shared memory) and cuts the
+ * candidates, then races them.  out int64 [B] (-1 when row status != 0); no workspace.
+ * Requirements: 1 <= B < 2^31, 1 <= V < 2^31. */
+lms_status lms_sample_from_logits_filtered(const void* logits, int32_t dtype, int64_t ld, int64_t B,
+                                           int64_t V, const lms_sample_params* params,
+                                           const lms_filter_params* filters, int64_t* out,
+                                           void* stream);
+
 /* Allocation-free variant of lms_lmhead_sample for callers that cannot allocate device memory:
  * code that runs inside a device-memory allocator or a pool's callback, code that must not take
  * the allocator's lock, or an embedding that hands this library only fixed buffers.  The pages

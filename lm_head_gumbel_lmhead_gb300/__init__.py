@@ -62,6 +62,12 @@ class SampleParams(ctypes.Structure):
     ]
 
 
+class FilterParams(ctypes.Structure):
+    """Mirror of ``lms_filter_params``."""
+    _fields_ = [("top_k", ctypes.c_void_p), ("top_p", ctypes.c_void_p), ("min_p", ctypes.c_void_p),
+                ("k_max", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -92,6 +98,10 @@ def lib() -> ctypes.CDLL:
             L.lms_lmhead_sample_noalloc.argtypes = [P, i64, P, i64, i64, i64, i64,
                                                     ctypes.POINTER(SampleParams), P, P]
             L.lms_lmhead_sample_noalloc.restype = i32
+            L.lms_sample_from_logits_filtered.argtypes = [P, i32, i64, i64, i64,
+                                                          ctypes.POINTER(SampleParams),
+                                                          ctypes.POINTER(FilterParams), P, P]
+            L.lms_sample_from_logits_filtered.restype = i32
             L.lms_philox_fill_noise.argtypes = [P, i32, i32, i64, i64, P, P, u64, u64, P]
             L.lms_philox_fill_noise.restype = i32
             _lib = L
@@ -277,6 +287,44 @@ def sample_from_logits(logits: torch.Tensor, *, B: Optional[int] = None, tempera
     _check(lib().lms_sample_from_logits(_ptr(logits), dt, ld, B, V, ctypes.byref(p), _ptr(out),
                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
                                         _stream(stream)))
+    return out
+
+
+def sample_from_logits_filtered(logits: torch.Tensor, *, B: Optional[int] = None, top_k=None,
+                                top_p=None, min_p=None, k_max: int = 1024, temperature=None,
+                                seeds=None, positions=None, bias=None, mask=None,
+                                base_seed: int = 0, offset: int = 0, wide: bool = False, out=None,
+                                row_status=None, stream=None) -> torch.Tensor:
+    """The race over materialised logits after top-k -> top-p -> min-p filters (per-row [B]
+    tensors: top_k int32, top_p / min_p float32; None = off)."""
+    if logits.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("logits must be float32 or bfloat16")
+    if logits.dim() == 1:
+        if B is None:
+            raise ValueError("pass B for a broadcast row")
+        ld, V = 0, logits.shape[0]
+    else:
+        if logits.stride(1) != 1:
+            raise ValueError("logits must be row-major with unit inner stride")
+        B = logits.shape[0] if B is None else B
+        ld, V = logits.stride(0), logits.shape[1]
+    dev = logits.device
+    p = _params(B, dev, temperature, seeds, positions, bias, mask, base_seed, offset, wide, 0,
+                PATH_AUTO, row_status, 0, 0)
+    fp = FilterParams()
+    tk = _dev(top_k, torch.int32, "top_k", dev)
+    tp = _dev(top_p, torch.float32, "top_p", dev)
+    mp = _dev(min_p, torch.float32, "min_p", dev)
+    fp.top_k = tk.data_ptr() if tk is not None else None
+    fp.top_p = tp.data_ptr() if tp is not None else None
+    fp.min_p = mp.data_ptr() if mp is not None else None
+    fp.k_max = int(k_max)
+    fp.reserved = 0
+    if out is None:
+        out = torch.empty(B, dtype=torch.int64, device=dev)
+    dt = DTYPE_F32 if logits.dtype == torch.float32 else DTYPE_BF16
+    _check(lib().lms_sample_from_logits_filtered(_ptr(logits), dt, ld, B, V, ctypes.byref(p),
+                                                 ctypes.byref(fp), _ptr(out), _stream(stream)))
     return out
 
 

@@ -289,6 +289,53 @@ lms_status lms_sample_from_logits(const void* logits, int32_t dtype, int64_t ld,
     return LMS_OK;
 }
 
+lms_status lms_sample_from_logits_filtered(const void* logits, int32_t dtype, int64_t ld, int64_t B,
+                                           int64_t V, const lms_sample_params* params,
+                                           const lms_filter_params* filters, int64_t* out,
+                                           void* stream) {
+    g_last_error[0] = '\0';
+    if (logits == nullptr || out == nullptr || filters == nullptr)
+        return fail(LMS_ERR_INVALID_ARG, "logits, filters and out are required");
+    if (dtype != LMS_DTYPE_F32 && dtype != LMS_DTYPE_BF16)
+        return fail(LMS_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+    if (B <= 0 || V <= 0 || V > kMaxV || B > kMaxV)
+        return fail(LMS_ERR_INVALID_ARG, "need 0 < B < 2^31 and 0 < V < 2^31");
+    lms_status st = check_params(params, V);
+    if (st != LMS_OK) return st;
+    if (ld != 0 && ld < V) return fail(LMS_ERR_INVALID_ARG, "ld must be 0 (broadcast) or >= V");
+    if (params->path != LMS_PATH_AUTO || params->debug_flags != 0 || params->tile_v != 0)
+        return fail(LMS_ERR_INVALID_ARG, "path, tile_v and debug_flags do not apply to the filtered race");
+    if (filters->k_max < 0 || filters->k_max > 1024 || filters->reserved != 0)
+        return fail(LMS_ERR_INVALID_ARG, "k_max must be in [0, 1024] and reserved 0");
+    lms::FilterArgs f;
+    f.a.temperature = params->temperature;
+    f.a.seeds = params->seeds;
+    f.a.positions = params->positions;
+    f.a.bias = params->bias;
+    f.a.ld_bias = params->ld_bias;
+    f.a.mask = params->allow_mask;
+    f.a.ld_mask = params->ld_mask;
+    f.a.base_seed = params->base_seed;
+    f.a.offset = params->offset;
+    f.a.B = B;
+    f.a.row0 = 0;
+    f.a.V = V;
+    f.a.n_tiles = 0;
+    f.a.cand_score = nullptr;
+    f.a.cand_index = nullptr;
+    f.top_k = filters->top_k;
+    f.top_p = filters->top_p;
+    f.min_p = filters->min_p;
+    f.k_max = filters->k_max ? filters->k_max : 1024;
+    f.out = out;
+    f.row_status = params->row_status;
+    const cudaError_t e = lms::launch_filtered_race(logits, dtype == LMS_DTYPE_BF16, ld,
+                                                    params->noise_mode == LMS_NOISE_WIDE53, f,
+                                                    static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "filtered race launch");
+    return LMS_OK;
+}
+
 lms_status lms_philox_fill_noise(void* out, int32_t kind, int32_t noise_mode, int64_t B, int64_t V,
                                  const int64_t* seeds, const int64_t* positions, uint64_t base_seed,
                                  uint64_t offset, void* stream) {

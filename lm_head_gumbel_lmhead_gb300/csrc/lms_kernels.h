@@ -26,6 +26,20 @@ struct SampleArgs {
     int* cand_index;    // [B][n_tiles]
 };
 
+// The filtered race (one CTA per row; writes tokens and statuses directly).
+struct FilterArgs {
+    SampleArgs a;
+    const int32_t* top_k;
+    const float* top_p;
+    const float* min_p;
+    int k_max;
+    int64_t* out;
+    int32_t* row_status;
+};
+
+cudaError_t launch_filtered_race(const void* logits, bool bf16, int64_t ld, bool wide,
+                                 const FilterArgs& f, cudaStream_t stream);
+
 cudaError_t launch_noise_fill(void* out, int kind, bool wide, int64_t B, int64_t V,
                               const int64_t* seeds, const int64_t* positions, uint64_t base_seed,
                               uint64_t offset, cudaStream_t stream);

@@ -68,7 +68,7 @@ def _load():
             lib.orc_lmhead_sample_rows.restype = ctypes.c_int
             lib.orc_sample_filtered.argtypes = [P, i64, i64, i64, P, P, P, P, i64, P, i64, u64, u64,
                                                 i32, P, P, P, i32, ctypes.c_double,
-                                                ctypes.c_double, P, P, P, i32]
+                                                ctypes.c_double, P, P, P, P, P, i32]
             lib.orc_uniform.argtypes = [ctypes.c_uint32, ctypes.c_uint32, i32]
             lib.orc_uniform.restype = ctypes.c_double
             _lib = lib
@@ -267,11 +267,13 @@ def lmhead_scores_at(H_bits, W_bits, rows, cols, *, temperature=None, seeds=None
 
 def sample_filtered(logits, *, B=None, temperature=None, seeds=None, positions=None, bias=None,
                     mask=None, base_seed=0, offset=0, wide=False, top_k=None, top_p=None,
-                    min_p=None, k_max=1024, p_shift=0.0, minp_scale=1.0, threads=None):
+                    min_p=None, k_max=1024, p_shift=0.0, minp_scale=1.0, threads=None,
+                    want_top2=False):
     """Filtered race over materialised logits: top-k -> top-p -> min-p on t = (y + bias) / T,
     then the Gumbel race over the kept tokens (spec-decode-ops "Semantics"; sampling-kernel
-    guide steps 6-8).  Returns (out, status, kept-set size).  p_shift / minp_scale move the
-    top-p / min-p thresholds, to find out which decisions sit on a floating-point boundary."""
+    guide steps 6-8).  Returns (out, status, kept-set size[, top1, top2]): top1 / top2 are the
+    two best perturbed scores of the kept set.  p_shift / minp_scale move the top-p / min-p
+    thresholds, to find out which decisions sit on a floating-point boundary."""
     y = np.asarray(logits, dtype=np.float64)
     if y.ndim == 1:
         ld_y, V = 0, y.shape[0]
@@ -287,9 +289,12 @@ def sample_filtered(logits, *, B=None, temperature=None, seeds=None, positions=N
     seeds_a, pos_a = _c(seeds, np.int64), _c(positions, np.int64)
     tk, tp, mp = _c(top_k, np.int32), _c(top_p, np.float64), _c(min_p, np.float64)
     out = np.empty(B, np.int64); status = np.empty(B, np.int32); kept = np.empty(B, np.int32)
+    top1 = np.empty(B); top2 = np.empty(B)
     _load().orc_sample_filtered(_ptr(y), ld_y, B, V, _ptr(T), _ptr(seeds_a), _ptr(pos_a),
                                 _ptr(bias_a), ld_bias, _ptr(mask_a), ld_mask, base_seed, offset,
                                 int(bool(wide)), _ptr(tk), _ptr(tp), _ptr(mp), int(k_max),
                                 float(p_shift), float(minp_scale), _ptr(out), _ptr(status),
-                                _ptr(kept), threads or default_threads())
+                                _ptr(kept), _ptr(top1), _ptr(top2), threads or default_threads())
+    if want_top2:
+        return out, status, kept, top1, top2
     return out, status, kept

@@ -450,11 +450,13 @@ typedef struct {
     double p_shift;      /* added to top_p (to probe the decision boundary) */
     double minp_scale;   /* multiplies min_p (same) */
     int64_t* out; int32_t* status; int32_t* kept;
+    double* top1; double* top2;    /* optional: the two best perturbed scores of the kept set */
 } orc_filt_args;
 
 static void orc_filtered_row(const orc_filt_args* f, int64_t b) {
     int64_t V = f->V;
     double T = f->T ? f->T[b] : 1.0;
+    if (f->top1) { f->top1[b] = -INFINITY; f->top2[b] = -INFINITY; }
     if (isnan(T) || T < 0.0) { f->out[b] = -1; f->status[b] = 2; if (f->kept) f->kept[b] = 0; return; }
     const double* yrow = f->y + b * f->ld_y;
     orc_rows_args a = {NULL, 0, f->B, V, f->T, f->seeds, f->positions, f->bias, f->ld_bias, f->mask,
@@ -505,13 +507,19 @@ static void orc_filtered_row(const orc_filt_args* f, int64_t b) {
     }
     if (n < 1) n = 1;
     /* race over the kept prefix */
-    double best = -INFINITY;
+    double best = -INFINITY, second = -INFINITY;
     int64_t arg = -1;
     for (int64_t i = 0; i < n; ++i) {
         int64_t v = tv[i].v;
         double s = orc_score(&a, b, v, yrow[v]);
-        if (arg < 0 || s > best || (s == best && v < arg)) { best = s; arg = v; }
+        if (arg < 0 || s > best || (s == best && v < arg)) {
+            if (arg >= 0) second = best > second ? best : second;
+            best = s; arg = v;
+        } else if (s > second) {
+            second = s;
+        }
     }
+    if (f->top1) { f->top1[b] = best; f->top2[b] = second; }
     f->out[b] = arg;
     f->status[b] = 0;
     if (f->kept) f->kept[b] = (int32_t)n;
@@ -533,10 +541,10 @@ void orc_sample_filtered(const double* y, int64_t ld_y, int64_t B, int64_t V, co
                          uint64_t base_seed, uint64_t offset, int wide, const int32_t* top_k,
                          const double* top_p, const double* min_p, int32_t k_max, double p_shift,
                          double minp_scale, int64_t* out, int32_t* status, int32_t* kept,
-                         int nthreads) {
+                         double* top1, double* top2, int nthreads) {
     orc_filt_args f = {y, ld_y, B, V, T, seeds, positions, bias, ld_bias, mask, ld_mask,
                        base_seed, offset, wide, top_k, top_p, min_p, k_max, p_shift, minp_scale,
-                       out, status, kept};
+                       out, status, kept, top1, top2};
     if (nthreads < 1) nthreads = 1;
     if (nthreads > B) nthreads = (int)B;
     if (nthreads > 256) nthreads = 256;
