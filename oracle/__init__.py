@@ -69,6 +69,16 @@ def _load():
             lib.orc_sample_filtered.argtypes = [P, i64, i64, i64, P, P, P, P, i64, P, i64, u64, u64,
                                                 i32, P, P, P, i32, ctypes.c_double,
                                                 ctypes.c_double, P, P, P, P, P, i32]
+            lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+            lib.orc_e4m3_decode.restype = ctypes.c_double
+            lib.orc_e4m3_encode.argtypes = [ctypes.c_double]
+            lib.orc_e4m3_encode.restype = ctypes.c_uint8
+            lib.orc_quantize_rows_e4m3.argtypes = [P, i64, i64, i64, P, i64, P]
+            lib.orc_lmhead_logits_fp8.argtypes = [P, i64, P, P, i64, P, i64, i64, i64, P, i64, P, i32]
+            lib.orc_lmhead_sample_fp8.argtypes = [P, i64, P, i64, P, i64, i64, i64, P, i64, P, P, P,
+                                                  P, i64, P, i64, u64, u64, i32, i64, P, P, P, P,
+                                                  P, P, i32]
+            lib.orc_lmhead_sample_fp8.restype = ctypes.c_int
             lib.orc_uniform.argtypes = [ctypes.c_uint32, ctypes.c_uint32, i32]
             lib.orc_uniform.restype = ctypes.c_double
             _lib = lib
@@ -298,3 +308,72 @@ def sample_filtered(logits, *, B=None, temperature=None, seeds=None, positions=N
     if want_top2:
         return out, status, kept, top1, top2
     return out, status, kept
+
+
+# ---- FP8 (E4M3) inputs: W8A8 with per-row scales ----
+
+def e4m3_decode(codes) -> np.ndarray:
+    """E4M3 ("fn") codes -> fp64 values."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([lib.orc_e4m3_decode(int(x)) for x in c.ravel()]).reshape(c.shape)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Nearest finite E4M3 code (ties to even, saturating at +-448) of fp64 values."""
+    lib = _load()
+    a = np.asarray(x, dtype=np.float64)
+    return np.array([lib.orc_e4m3_encode(float(v)) for v in a.ravel()], np.uint8).reshape(a.shape)
+
+
+def quantize_rows_e4m3(H_bits):
+    """Per-row power-of-two quantisation of bf16 H [B, D]: (E4M3 codes uint8 [B, D], e int32 [B])
+    with e the smallest integer such that max |h| * 2^-e <= 448."""
+    H = _bits16(H_bits)
+    B, D = H.shape
+    q = np.empty((B, D), np.uint8)
+    e = np.empty(B, np.int32)
+    _load().orc_quantize_rows_e4m3(_ptr(H), D, B, D, _ptr(q), D, _ptr(e))
+    return q, e
+
+
+def lmhead_logits_fp8(H8, e_h, W8, w_scale, rows=None, threads=None) -> np.ndarray:
+    """y = 2^e_h[b] * w_scale[v] * sum_d E4M3(H8) E4M3(W8) in fp64 (rows: subset of H's rows)."""
+    H8 = _c(H8, np.uint8); W8 = _c(W8, np.uint8)
+    e_h = _c(e_h, np.int32); ws = _c(w_scale, np.float64)
+    B, D = H8.shape
+    V = W8.shape[0]
+    r = _c(rows, np.int64)
+    nb = B if r is None else r.shape[0]
+    y = np.empty((nb, V))
+    _load().orc_lmhead_logits_fp8(_ptr(H8), D, _ptr(e_h), _ptr(W8), D, _ptr(ws), B, D, V, _ptr(r),
+                                  0 if r is None else nb, _ptr(y), threads or default_threads())
+    return y
+
+
+def lmhead_sample_fp8(H_bits, W8, w_scale, *, rows=None, temperature=None, seeds=None,
+                      positions=None, bias=None, mask=None, base_seed=0, offset=0, wide=False,
+                      tile_v=128, threads=None) -> RowResult:
+    """The fused FP8 path's result: quantise H per row (power-of-two scale), fp64 logits from the
+    E4M3 operands and scales, then the per-row race; rows = a subset of the batch (or all)."""
+    H = _bits16(H_bits)
+    B, D = H.shape
+    W8 = _c(W8, np.uint8)
+    V = W8.shape[0]
+    ws = _c(w_scale, np.float64)
+    r = _c(rows, np.int64)
+    nb = B if r is None else r.shape[0]
+    T = _c(temperature, np.float64)
+    bias_a = _c(bias, np.float64)
+    ld_bias = 0 if bias_a is None or bias_a.ndim == 1 else bias_a.shape[1]
+    mask_a = _c(mask, np.uint32)
+    ld_mask = 0 if mask_a is None or mask_a.ndim == 1 else mask_a.shape[1]
+    seeds_a, pos_a = _c(seeds, np.int64), _c(positions, np.int64)
+    outs = _row_outputs(nb, V, tile_v, False)
+    rc = _load().orc_lmhead_sample_fp8(
+        _ptr(H), D, _ptr(W8), D, _ptr(ws), B, D, V, _ptr(r), 0 if r is None else nb, _ptr(T),
+        _ptr(seeds_a), _ptr(pos_a), _ptr(bias_a), ld_bias, _ptr(mask_a), ld_mask, base_seed,
+        offset, int(bool(wide)), tile_v, *[_ptr(o) for o in outs[:6]], threads or default_threads())
+    if rc != 0:
+        raise MemoryError("oracle could not allocate")
+    return RowResult(*outs)

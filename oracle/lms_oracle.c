@@ -556,3 +556,119 @@ void orc_sample_filtered(const double* y, int64_t ld_y, int64_t B, int64_t V, co
     }
     for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
 }
+
+/* ------------------------------------------------------------------------------------------ */
+/* FP8 (E4M3) inputs: W8A8 with per-row scales [FS "Limitations": low-precision FP8 inputs]     */
+/* ------------------------------------------------------------------------------------------ */
+/* E4M3 ("fn" variant): 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent field 0
+ * holds subnormals m/8 * 2^-6; no infinities; S.1111.111 is NaN; the largest finite value is
+ * S.1111.110 = 1.75 * 2^8 = 448. */
+double orc_e4m3_decode(uint8_t c) {
+    int s = (c >> 7) & 1, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, -6);
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* Round to the nearest finite E4M3 value (ties to the even code), saturating at +-448:
+ * written as a search over every finite code, so it can be checked by eye. */
+uint8_t orc_e4m3_encode(double x) {
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = (x < 0.0 || (x == 0.0 && signbit(x))) ? 0x80 : 0x00;
+    double a = fabs(x);
+    uint8_t best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {                       /* non-negative finite codes */
+        double d = fabs(orc_e4m3_decode((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) { best_d = d; best = (uint8_t)c; }
+    }
+    return (uint8_t)(sign | best);
+}
+
+/* Per-row power-of-two quantisation of bf16 activations: e_b is the smallest integer with
+ * max_d |h[b][d]| * 2^-e_b <= 448 (0 for an all-zero row); q = E4M3(h * 2^-e_b).  Scaling by a
+ * power of two is exact, so the rounding to E4M3 is the only step. */
+void orc_quantize_rows_e4m3(const uint16_t* H, int64_t ldh, int64_t B, int64_t D, uint8_t* q,
+                            int64_t ldq, int32_t* e_out) {
+    for (int64_t b = 0; b < B; ++b) {
+        double amax = 0.0;
+        for (int64_t d = 0; d < D; ++d) {
+            double h = fabs(orc_bf16(H[b * ldh + d]));
+            if (h > amax) amax = h;
+        }
+        int e = 0;
+        if (amax > 0.0) {
+            e = -160;
+            while (ldexp(amax, -e) > 448.0) ++e;
+        }
+        e_out[b] = e;
+        for (int64_t d = 0; d < D; ++d) q[b * ldq + d] = orc_e4m3_encode(ldexp(orc_bf16(H[b * ldh + d]), -e));
+    }
+}
+
+typedef struct {
+    const uint8_t* H8; int64_t ldh; const int32_t* e_h; const uint8_t* W8; int64_t ldw;
+    const double* w_scale; int64_t B, D, V; double* y; int64_t v0, v1; const int64_t* rows;
+} orc_gemm8_job;
+
+static void* orc_gemm8_worker(void* p) {
+    const orc_gemm8_job* j = (const orc_gemm8_job*)p;
+    double* wrow = (double*)malloc(sizeof(double) * (size_t)j->D);
+    for (int64_t v = j->v0; v < j->v1; ++v) {
+        for (int64_t d = 0; d < j->D; ++d) wrow[d] = orc_e4m3_decode(j->W8[v * j->ldw + d]);
+        for (int64_t i = 0; i < j->B; ++i) {
+            int64_t b = j->rows ? j->rows[i] : i;
+            double acc = 0.0;
+            for (int64_t d = 0; d < j->D; ++d) acc += orc_e4m3_decode(j->H8[b * j->ldh + d]) * wrow[d];
+            j->y[i * j->V + v] = acc * ldexp(1.0, j->e_h[b]) * j->w_scale[v];
+        }
+    }
+    free(wrow);
+    return NULL;
+}
+
+/* y[b][v] = 2^e_h[b] * w_scale[v] * sum_d E4M3(H8[b][d]) * E4M3(W8[v][d]), in fp64; rows as in
+ * orc_lmhead_sample_rows (NULL = all B). */
+void orc_lmhead_logits_fp8(const uint8_t* H8, int64_t ldh, const int32_t* e_h, const uint8_t* W8,
+                           int64_t ldw, const double* w_scale, int64_t B, int64_t D, int64_t V,
+                           const int64_t* rows, int64_t n_rows, double* y, int nthreads) {
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t th[256];
+    orc_gemm8_job jobs[256];
+    int64_t nb = rows ? n_rows : B;
+    for (int i = 0; i < nthreads; ++i) {
+        orc_gemm8_job j = {H8, ldh, e_h, W8, ldw, w_scale, nb, D, V, y, V * i / nthreads,
+                           V * (i + 1) / nthreads, rows};
+        jobs[i] = j;
+        pthread_create(&th[i], NULL, orc_gemm8_worker, &jobs[i]);
+    }
+    for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+}
+
+/* The fused FP8 path's result for rows (NULL = all): quantise H, fp64 logits from the FP8
+ * operands and scales, then the same per-row race (tile maxima for tile_v). */
+int orc_lmhead_sample_fp8(const uint16_t* H, int64_t ldh, const uint8_t* W8, int64_t ldw,
+                          const double* w_scale, int64_t B, int64_t D, int64_t V,
+                          const int64_t* rows, int64_t n_rows, const double* T,
+                          const int64_t* seeds, const int64_t* positions, const double* bias,
+                          int64_t ld_bias, const uint32_t* mask, int64_t ld_mask,
+                          uint64_t base_seed, uint64_t offset, int wide, int64_t tile_v,
+                          int64_t* out, int32_t* status, double* top1, double* top2,
+                          double* tile_max, int64_t* tile_idx, int nthreads) {
+    uint8_t* q = (uint8_t*)malloc((size_t)(B * D));
+    int32_t* e = (int32_t*)malloc(sizeof(int32_t) * (size_t)B);
+    int64_t nb = rows ? n_rows : B;
+    double* y = (double*)malloc(sizeof(double) * (size_t)(nb * V));
+    if (!q || !e || !y) { free(q); free(e); free(y); return 1; }
+    orc_quantize_rows_e4m3(H, ldh, B, D, q, D, e);
+    orc_lmhead_logits_fp8(q, D, e, W8, ldw, w_scale, B, D, V, rows, n_rows, y, nthreads);
+    orc_rows_args a = {y, V, B, V, T, seeds, positions, bias, ld_bias, mask, ld_mask,
+                       base_seed, offset, wide, tile_v, out, status, top1, top2,
+                       tile_max, tile_idx, NULL, rows, rows ? n_rows : 0};
+    orc_run_rows(&a, nthreads);
+    free(q); free(e); free(y);
+    return 0;
+}
