@@ -19,6 +19,8 @@ Workloads (synthetic, seeded; the shapes of the FlashSampling page's measurement
 - ``large-vocab`` (B in 128/256/512): D = 8192, V = 262144, wide noise.
 - ``logits``: ``lms_sample_from_logits`` over materialised N(0, 4) logits, V = 131072.
 - ``noise``: ``lms_philox_fill_noise`` of Gumbel noise, B x V float32.
+- ``qwen3-8b-fp8``: the Qwen3-8B shape through ``lms_lmhead_sample_fp8``. W is offline-quantised
+  to E4M3 with per-row scales, and H is quantised per row on the GPU each step (W8A8).
 - ``filtered``: ``lms_sample_from_logits_filtered`` with top-k 50 and top-p 0.9 at T = 0.7 over
   bf16 logits, V = 131072 (the Megatron-LM PR's filter settings).
 
@@ -56,8 +58,9 @@ if ROOT not in sys.path:
 METRIC = "µs per decode sample step & achieved HBM GB/s vs peak, fused LM-head+Gumbel"
 UNIT = "us/step"
 TC_SOURCES = ["lm_head_gumbel_lmhead_gb300/csrc/lmhead_tc.cu",
+              "lm_head_gumbel_lmhead_gb300/csrc/tcgen05_common.cuh",
               "lm_head_gumbel_lmhead_gb300/csrc/lms_device.cuh"]
-FUSED = ("qwen3-8b", "llama3-hetero", "large-vocab")
+FUSED = ("qwen3-8b", "llama3-hetero", "large-vocab", "qwen3-8b-fp8")
 
 
 def kernel_source_hash() -> str:
@@ -191,7 +194,7 @@ class ClockSampler:
 # ------------------------------------------------------------------------------------------
 def make_workload(name: str, B: int, D: int, V: int):
     from lm_head_gumbel_lmhead_gb300 import workloads
-    if name == "qwen3-8b":
+    if name in ("qwen3-8b", "qwen3-8b-fp8"):
         return workloads.qwen3_8b(B, D=D or 4096, V=V or 151936)
     if name == "llama3-hetero":
         return workloads.llama3_hetero(B, D=D or 4096, V=V or 128256)
@@ -329,23 +332,38 @@ def run_gpu(args):
         mask = None if w.mask is None else w.mask.to(dev)
         # positions advance with the step: one row per step, made before timing
         pos_all = (w.positions[None, :] + torch.arange(n_steps)[:, None]).contiguous().to(dev)
-        tv, nt, ws_bytes, path = lms.tile_info(lms.OP_LMHEAD, B, D, V)
+        fp8 = args.workload == "qwen3-8b-fp8"
+        tv, nt, ws_bytes, path = lms.tile_info(lms.OP_LMHEAD_FP8 if fp8 else lms.OP_LMHEAD, B, D, V)
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         out = torch.empty(B, dtype=torch.int64, device=dev)
         wide = w.noise_mode == 1
         kw = dict(temperature=T, seeds=seeds, bias=bias, mask=mask, base_seed=w.base_seed,
                   offset=w.offset, wide=wide, out=out, workspace=workspace)
         launches_per_step = (1 + (B - 1) // 256 if path == lms.PATH_TCGEN05 else 1) + 1
+        if fp8:
+            W8_h, wsc_h = workloads.quantize_weight_e4m3(w.W)
+            W8, wsc = W8_h.to(dev), wsc_h.to(dev)
+            W = None                               # the bf16 copy is not needed on the device
+            launches_per_step += 1                 # the activation quantisation
 
-        def step(i):
-            lms.lmhead_sample(H, W, positions=pos_all[i], **kw)
+            def step(i):
+                lms.lmhead_sample_fp8(H, W8, wsc, positions=pos_all[i], **kw)
+        else:
+            def step(i):
+                lms.lmhead_sample(H, W, positions=pos_all[i], **kw)
 
         alg = algorithmic_bytes(B, D, V, nt, bias is not None, mask is not None)
+        if fp8:
+            # W at one byte per weight plus its row scales; H read once, its E4M3 copy written
+            # and read once
+            alg = alg - V * D * 2 + V * D + V * 4 + 2 * B * D
         flops = 2 * B * V * D
-        config = {"workload": w.name, "B": B, "D": D, "V": V, "noise": "wide53" if wide else "fp32",
+        config = {"workload": w.name + (" fp8-e4m3 W8A8" if fp8 else ""), "B": B, "D": D, "V": V,
+                  "noise": "wide53" if wide else "fp32",
                   "path": {1: "gemv", 2: "tcgen05"}[path], "tile_v": tv,
-                  "l2": "inputs larger than L2 (W is %.2f GB), no flush" % (V * D * 2 / 1e9)}
-        kernel = "lmhead_tc_kernel + stage2_kernel (one step, CUDA events)"
+                  "l2": "inputs larger than L2 (W is %.2f GB), no flush" % (V * D * (1 if fp8 else 2) / 1e9)}
+        kernel = ("quantize_rows_e4m3_kernel + " if fp8 else "") + \
+            "lmhead_tc_kernel + stage2_kernel (one step, CUDA events)"
     elif args.workload == "logits":
         V = args.V or 131072
         D = 0
@@ -436,9 +454,13 @@ def run_gpu(args):
             for k, v in host.items():
                 devb[k].copy_(v, non_blocking=True)
             p_d.copy_(pos_h[i], non_blocking=True)
-            lms.lmhead_sample(devb["H"], W, temperature=devb["T"], seeds=devb["seeds"], positions=p_d,
-                              bias=devb.get("bias"), mask=devb.get("mask"), base_seed=w.base_seed,
-                              offset=w.offset, wide=wide, out=out, workspace=workspace)
+            ekw = dict(temperature=devb["T"], seeds=devb["seeds"], positions=p_d,
+                       bias=devb.get("bias"), mask=devb.get("mask"), base_seed=w.base_seed,
+                       offset=w.offset, wide=wide, out=out, workspace=workspace)
+            if fp8:
+                lms.lmhead_sample_fp8(devb["H"], W8, wsc, **ekw)
+            else:
+                lms.lmhead_sample(devb["H"], W, **ekw)
             out_h.copy_(out, non_blocking=True)
 
         e2e_ms, _, _, _ = _time_steps(e2e_step, args.warmup, args.steps, dev, stream)
@@ -449,13 +471,19 @@ def run_gpu(args):
     if rank != 0:
         return
     achieved_gbs = alg / (us * 1e-6) / 1e9
+    # a contraction takes the peak of its own input type: E4M3 runs at twice the bf16 rate
+    # (nominal 4.5 vs 2.25 PFLOP/s dense), applied to the measured bf16 figure
+    fp8_run = args.workload == "qwen3-8b-fp8"
+    tensor_peak = peaks["bf16_tflops"] * (2.0 if fp8_run else 1.0)
     t_hbm = alg / (peaks["hbm_gbs"] * 1e9)
-    t_tensor = flops / (peaks["bf16_tflops"] * 1e12) if flops else 0.0
+    t_tensor = flops / (tensor_peak * 1e12) if flops else 0.0
     if t_tensor > t_hbm:
         tf = flops / (us * 1e-6) / 1e12
-        roofline = {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
-                    "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
-                    "peak_source": peaks["source"] + " (MEASURED_PEAKS.json bf16_tflops, burst cuBLAS)",
+        roofline = {"bound": "tensor", "achieved": round(tf, 1), "peak": round(tensor_peak, 1),
+                    "unit": "TFLOP/s", "frac": round(tf / tensor_peak, 4),
+                    "peak_source": peaks["source"] + (" (MEASURED_PEAKS.json bf16_tflops x 2, the nominal "
+                                                      "fp8/bf16 ratio)" if fp8_run else
+                                                      " (MEASURED_PEAKS.json bf16_tflops, burst cuBLAS)"),
                     "algorithmic_flops": flops}
     else:
         roofline = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peaks["hbm_gbs"],
@@ -481,7 +509,7 @@ def run_gpu(args):
     if e2e is not None:
         line["e2e"] = e2e
     if not args.no_cpu_baseline:
-        if args.workload in FUSED:
+        if args.workload in FUSED and args.workload != "qwen3-8b-fp8":
             line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
         elif args.workload == "logits":
             threads = os.cpu_count() or 1

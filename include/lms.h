@@ -67,7 +67,7 @@ typedef enum {
     LMS_NOISE_OUT_EXPONENTIAL = 2,/* float  [B][V]: E = -log u as the sampling kernels compute it */
     LMS_NOISE_OUT_GUMBEL = 3      /* float  [B][V]: g = -log E as the sampling kernels compute it */
 } lms_noise_kind;
-typedef enum { LMS_OP_LMHEAD = 0, LMS_OP_LOGITS = 1 } lms_op;
+typedef enum { LMS_OP_LMHEAD = 0, LMS_OP_LOGITS = 1, LMS_OP_LMHEAD_FP8 = 2 } lms_op;
 typedef enum {
     LMS_PATH_AUTO = 0,            /* the library's choice (currently tcgen05 for every B)      */
     LMS_PATH_GEMV = 1,            /* CUDA-core dot products (B <= LMS_GEMV_MAX_B)                */
@@ -143,6 +143,24 @@ size_t lms_workspace_bytes(int32_t op, int64_t B, int64_t D, int64_t V, int32_t 
 lms_status lms_lmhead_sample(const void* H, int64_t ldh, const void* W, int64_t ldw, int64_t B,
                              int64_t D, int64_t V, const lms_sample_params* params, int64_t* out,
                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* The fused path with FP8 (E4M3) inputs, W8A8 (FlashSampling "Limitations": low-precision FP8
+ * inputs, which the kernel structure supports):
+ *   W8      E4M3 [V][ldw8] bytes ("fn" encoding: no infinities, max 448), w_scale fp32 [V]: the
+ *           weight is W[v][d] = E4M3(W8[v][d]) * w_scale[v] (quantised by the caller, offline).
+ *   H       bf16 [B][ldh], quantised by the call: row b is scaled by 2^-e_b, e_b the smallest
+ *           integer with max_d |H[b][d]| * 2^-e_b <= 448, and rounded to the nearest E4M3 value
+ *           (ties to even).  The power-of-two scale makes the scaling exact.
+ * Logits y[b][v] = 2^e_b * w_scale[v] * sum_d E4M3(H8[b][d]) E4M3(W8[v][d]) (tcgen05.mma
+ * kind::f8f6f4, fp32 accumulation); everything after that is lms_lmhead_sample's.  W streams at
+ * one byte per weight.  Workspace (lms_workspace_bytes(LMS_OP_LMHEAD_FP8, ...)): the candidates,
+ * then the quantised activations [B][round_up(D, 16)] bytes, then e_b int32 [B], each at a
+ * 256-byte aligned offset.  Requirements: D % 16 == 0, ldw8 >= D and % 16 == 0, ldh as for
+ * lms_lmhead_sample, H and W8 16-byte aligned; path AUTO or TCGEN05. */
+lms_status lms_lmhead_sample_fp8(const void* H, int64_t ldh, const void* W8, int64_t ldw8,
+                                 const float* w_scale, int64_t B, int64_t D, int64_t V,
+                                 const lms_sample_params* params, int64_t* out, void* workspace,
+                                 size_t workspace_bytes, void* stream);
 
 /* The same race over materialised logits [B][ld] (fp32 or bf16).  ld == 0 broadcasts one
  * row to all B draws (each draw keyed by its own row index / position).  Several CTAs share a

@@ -25,7 +25,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "liblms.so")
 LMS_OK, LMS_ERR_INVALID_ARG, LMS_ERR_UNSUPPORTED, LMS_ERR_WORKSPACE, LMS_ERR_CUDA = range(5)
 NOISE_FP32, NOISE_WIDE53 = 0, 1
 DTYPE_F32, DTYPE_BF16 = 0, 1
-OP_LMHEAD, OP_LOGITS = 0, 1
+OP_LMHEAD, OP_LOGITS, OP_LMHEAD_FP8 = 0, 1, 2
 PATH_AUTO, PATH_GEMV, PATH_TCGEN05, PATH_TCGEN05_PAIR = 0, 1, 2, 3
 NOISE_KINDS = {"words": 0, "uniform": 1, "exponential": 2, "gumbel": 3}
 ROW_OK, ROW_NO_CANDIDATE, ROW_BAD_TEMPERATURE, ROW_DEVICE_TIMEOUT = range(4)
@@ -98,6 +98,9 @@ def lib() -> ctypes.CDLL:
             L.lms_lmhead_sample_noalloc.argtypes = [P, i64, P, i64, i64, i64, i64,
                                                     ctypes.POINTER(SampleParams), P, P]
             L.lms_lmhead_sample_noalloc.restype = i32
+            L.lms_lmhead_sample_fp8.argtypes = [P, i64, P, i64, P, i64, i64, i64,
+                                                ctypes.POINTER(SampleParams), P, P, sz, P]
+            L.lms_lmhead_sample_fp8.restype = i32
             L.lms_sample_from_logits_filtered.argtypes = [P, i32, i64, i64, i64,
                                                           ctypes.POINTER(SampleParams),
                                                           ctypes.POINTER(FilterParams), P, P]
@@ -229,6 +232,52 @@ def lmhead_sample(H: torch.Tensor, W: torch.Tensor, *, temperature=None, seeds=N
                                    ctypes.byref(p), _ptr(out), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
+
+
+def lmhead_sample_fp8(H: torch.Tensor, W8: torch.Tensor, w_scale: torch.Tensor, *, temperature=None,
+                      seeds=None, positions=None, bias=None, mask=None, base_seed: int = 0,
+                      offset: int = 0, wide: bool = False, out=None, workspace=None,
+                      row_status=None, timeout_ms: int = 0, debug_flags: int = 0,
+                      stream=None) -> torch.Tensor:
+    """lmhead_sample with FP8 inputs: W8 E4M3 codes (uint8 or float8_e4m3fn [V, D]) with per-row
+    fp32 w_scale [V]; H bf16 [B, D] is quantised per row (power-of-two scale) by the call."""
+    if H.dtype != torch.bfloat16:
+        raise TypeError("H must be bfloat16")
+    if W8.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError("W8 must be uint8 or float8_e4m3fn")
+    if w_scale.dtype != torch.float32 or w_scale.dim() != 1 or w_scale.shape[0] != W8.shape[0]:
+        raise ValueError("w_scale must be float32 [V]")
+    if H.dim() != 2 or W8.dim() != 2 or H.shape[1] != W8.shape[1]:
+        raise ValueError("H must be [B, D] and W8 [V, D]")
+    if H.stride(1) != 1 or W8.stride(1) != 1:
+        raise ValueError("H and W8 must be row-major with unit inner stride")
+    B, D = H.shape
+    V = W8.shape[0]
+    dev = H.device
+    p = _params(B, dev, temperature, seeds, positions, bias, mask, base_seed, offset, wide, 0,
+                PATH_AUTO, row_status, timeout_ms, debug_flags)
+    if out is None:
+        out = torch.empty(B, dtype=torch.int64, device=dev)
+    if workspace is None:
+        workspace = torch.empty(workspace_bytes(OP_LMHEAD_FP8, B, D, V), dtype=torch.uint8, device=dev)
+    _check(lib().lms_lmhead_sample_fp8(_ptr(H), H.stride(0), _ptr(W8), W8.stride(0), _ptr(w_scale),
+                                       B, D, V, ctypes.byref(p), _ptr(out), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def split_workspace_fp8(ws: torch.Tensor, B: int, D: int, n_tiles: int):
+    """(score, index, quantised activations uint8 [B, round_up(D,16)], exponents int32 [B]) views
+    of an FP8-path workspace."""
+    score, index = split_workspace(ws, B, n_tiles)
+    n = B * n_tiles
+    off = 2 * ((4 * n + 255) // 256 * 256)
+    ldq = (D + 15) // 16 * 16
+    raw = ws.view(torch.uint8)
+    q = raw[off: off + B * ldq].view(B, ldq)
+    off2 = off + (B * ldq + 255) // 256 * 256
+    e = raw[off2: off2 + 4 * B].view(torch.int32)
+    return score, index, q, e
 
 
 def lmhead_sample_noalloc(H: torch.Tensor, W: torch.Tensor, *, temperature=None, seeds=None,

@@ -68,7 +68,7 @@ struct SmemLayout {
     }
 };
 
-template <int kEpiWarps, bool kWide>
+template <int kEpiWarps, bool kWide, bool kFp8>
 __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     lmhead_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
                      const TcParams prm) {
@@ -147,9 +147,11 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
                     if (!withhold) {
                         const uint32_t dst = base_addr + L.stages_off + stage * prm.stage_bytes;
                         mbar_arrive_expect_tx(full_bar(stage), prm.stage_bytes);
-                        tma_load_2d(dst, &tmW, kc * kBK, static_cast<int>(tile * kTileV),
+                        // one stage is 128 bytes of K: 64 bf16 or 128 E4M3 elements
+                        const int kx = kc * (kFp8 ? 2 * kBK : kBK);
+                        tma_load_2d(dst, &tmW, kx, static_cast<int>(tile * kTileV),
                                     full_bar(stage), pol_w);
-                        tma_load_2d(dst + kWStageBytes, &tmH, kc * kBK, static_cast<int>(a.row0),
+                        tma_load_2d(dst + kWStageBytes, &tmH, kx, static_cast<int>(a.row0),
                                     full_bar(stage), pol_h);
                         issued |= 1u << stage;
                         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            const uint32_t idesc = mma_idesc_bf16(n_pad, kTileV);
+            const uint32_t idesc = kFp8 ? mma_idesc_e4m3(n_pad, kTileV) : mma_idesc_bf16(n_pad, kTileV);
             int stage = 0;
             uint32_t phase = 0;
             int i = 0;
@@ -183,10 +185,12 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
                     const uint64_t adesc = kmajor_sw128_desc(sa);
                     const uint64_t bdesc = kmajor_sw128_desc(sa + kWStageBytes);
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k) {
-                        // advance 16 bf16 = 32 bytes along K inside the swizzle atom
-                        mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc,
-                                 (kc | k) != 0 ? 1u : 0u);
+                    for (int k = 0; k < 4; ++k) {
+                        // advance 32 bytes along K inside the swizzle atom (16 bf16 / 32 E4M3)
+                        if (kFp8)
+                            mma_e4m3(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kc | k) != 0 ? 1u : 0u);
+                        else
+                            mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kc | k) != 0 ? 1u : 0u);
                     }
                     mma_commit(empty_bar(stage));
                     if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -252,10 +256,10 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     }
 }
 
-template <int kEpiWarps, bool kWide>
+template <int kEpiWarps, bool kWide, bool kFp8>
 cudaError_t launch_variant(const CUtensorMap& tmW, const CUtensorMap& tmH, const TcParams& prm,
                            size_t smem, int grid, cudaStream_t stream) {
-    auto kern = lmhead_tc_kernel<kEpiWarps, kWide>;
+    auto kern = lmhead_tc_kernel<kEpiWarps, kWide, kFp8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -267,10 +271,11 @@ cudaError_t launch_variant(const CUtensorMap& tmW, const CUtensorMap& tmH, const
 
 cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int64_t D, int n_pad,
                              bool wide, uint32_t timeout_ms, uint32_t debug_flags,
-                             const SampleArgs& a, cudaStream_t stream) {
+                             const SampleArgs& a, cudaStream_t stream, bool fp8) {
     TcParams prm;
     prm.a = a;
-    prm.nk = static_cast<int>((D + kBK - 1) / kBK);
+    const int64_t k_per_stage = fp8 ? 2 * kBK : kBK;
+    prm.nk = static_cast<int>((D + k_per_stage - 1) / k_per_stage);
     prm.n_pad = n_pad;
     prm.stage_bytes = static_cast<uint32_t>(kWStageBytes + n_pad * kBK * 2);
     const uint32_t budget = 227u * 1024u - 1024u;   // opt-in maximum minus alignment slack
@@ -288,8 +293,11 @@ cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int
     const size_t smem = L.total + 1024;
     int sms = device_sm_count();
     int grid = static_cast<int>(a.n_tiles < sms ? a.n_tiles : sms);
-    return wide ? launch_variant<kEpilogueWarps, true>(tmW, tmH, prm, smem, grid, stream)
-                : launch_variant<kEpilogueWarps, false>(tmW, tmH, prm, smem, grid, stream);
+    if (fp8)
+        return wide ? launch_variant<kEpilogueWarps, true, true>(tmW, tmH, prm, smem, grid, stream)
+                    : launch_variant<kEpilogueWarps, false, true>(tmW, tmH, prm, smem, grid, stream);
+    return wide ? launch_variant<kEpilogueWarps, true, false>(tmW, tmH, prm, smem, grid, stream)
+                : launch_variant<kEpilogueWarps, false, false>(tmW, tmH, prm, smem, grid, stream);
 }
 
 }  // namespace lms

@@ -53,7 +53,7 @@ lms_status make_tiling(int32_t op, int64_t B, int64_t D, int64_t V, int32_t tile
     if (B <= 0 || V <= 0) return fail(LMS_ERR_INVALID_ARG, "B and V must be positive (B=%lld V=%lld)",
                                       (long long)B, (long long)V);
     if (V > kMaxV) return fail(LMS_ERR_INVALID_ARG, "V must be < 2^31 (V=%lld)", (long long)V);
-    if (op == LMS_OP_LMHEAD) {
+    if (op == LMS_OP_LMHEAD || op == LMS_OP_LMHEAD_FP8) {
         if (D <= 0) return fail(LMS_ERR_INVALID_ARG, "D must be positive (D=%lld)", (long long)D);
         if (B > 65536) return fail(LMS_ERR_INVALID_ARG, "B must be <= 65536 (B=%lld)", (long long)B);
         if (tile_req != 0 && tile_req != LMS_FUSED_TILE_V)
@@ -83,6 +83,12 @@ lms_status make_tiling(int32_t op, int64_t B, int64_t D, int64_t V, int32_t tile
         return fail(LMS_ERR_UNSUPPORTED, "B * n_tiles exceeds the launch grid limit");
     const size_t cand = static_cast<size_t>(B) * static_cast<size_t>(out->n_tiles) * 4;
     out->workspace = round_up(cand, 256) + round_up(cand, 256);
+    if (op == LMS_OP_LMHEAD_FP8) {
+        // + quantised activations [B][round_up(D, 16)] bytes + their exponents [B]
+        out->workspace += round_up(static_cast<size_t>(B) * round_up(static_cast<size_t>(D), 16), 256) +
+                          round_up(static_cast<size_t>(B) * 4, 256);
+        out->path = LMS_PATH_TCGEN05;
+    }
     return LMS_OK;
 }
 
@@ -122,6 +128,8 @@ lms::SampleArgs make_args(const lms_sample_params* p, int64_t B, int64_t V, cons
     const size_t cand = static_cast<size_t>(B) * static_cast<size_t>(t.n_tiles) * 4;
     a.cand_score = static_cast<float*>(workspace);
     a.cand_index = reinterpret_cast<int*>(static_cast<char*>(workspace) + round_up(cand, 256));
+    a.h_exp = nullptr;
+    a.w_scale = nullptr;
     return a;
 }
 
@@ -145,21 +153,28 @@ EncodeTiledFn encode_tiled_fn() {
     return fn;
 }
 
-// bf16 [rows][ld] row-major -> 2-D map {D, rows}, boxes of 64 x box_rows, 128-byte swizzle,
-// out-of-range elements read as zero.
-lms_status encode_bf16_map(CUtensorMap* tm, const void* ptr, int64_t rows, int64_t D, int64_t ld,
-                           int box_rows) {
+// [rows][ld] row-major -> 2-D map {D, rows}, boxes of 128 bytes x box_rows, 128-byte swizzle,
+// out-of-range elements read as zero.  bf16 (ld in elements of 2 bytes) or bytes (E4M3).
+lms_status encode_map(CUtensorMap* tm, const void* ptr, int64_t rows, int64_t D, int64_t ld,
+                      int box_rows, bool bytes) {
     EncodeTiledFn fn = encode_tiled_fn();
     if (fn == nullptr) return fail(LMS_ERR_CUDA, "cuTensorMapEncodeTiled not available from the driver");
+    const int esize = bytes ? 1 : 2;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esize};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
-                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    const CUresult r = fn(tm, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          2, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(LMS_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
     return LMS_OK;
+}
+
+lms_status encode_bf16_map(CUtensorMap* tm, const void* ptr, int64_t rows, int64_t D, int64_t ld,
+                           int box_rows) {
+    return encode_map(tm, ptr, rows, D, ld, box_rows, false);
 }
 
 }  // namespace
@@ -262,6 +277,60 @@ lms_status lms_lmhead_sample(const void* H, int64_t ldh, const void* W, int64_t 
     return LMS_OK;
 }
 
+lms_status lms_lmhead_sample_fp8(const void* H, int64_t ldh, const void* W8, int64_t ldw8,
+                                 const float* w_scale, int64_t B, int64_t D, int64_t V,
+                                 const lms_sample_params* params, int64_t* out, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+    g_last_error[0] = '\0';
+    if (H == nullptr || W8 == nullptr || w_scale == nullptr || out == nullptr)
+        return fail(LMS_ERR_INVALID_ARG, "H, W8, w_scale and out are required");
+    Tiling t;
+    lms_status st = make_tiling(LMS_OP_LMHEAD_FP8, B, D, V, params ? params->tile_v : 0, &t);
+    if (st != LMS_OK) return st;
+    if ((st = check_params(params, V)) != LMS_OK) return st;
+    if (D % 16 != 0) return fail(LMS_ERR_UNSUPPORTED, "D must be a multiple of 16 (D=%lld)", (long long)D);
+    if (D > 65536) return fail(LMS_ERR_UNSUPPORTED, "D must be <= 65536");
+    if (ldh < D || ldh % 8 != 0 || ldw8 < D || ldw8 % 16 != 0)
+        return fail(LMS_ERR_UNSUPPORTED, "ldh must be >= D and a multiple of 8; ldw8 >= D and a multiple of 16");
+    if (reinterpret_cast<uintptr_t>(H) % 16 != 0 || reinterpret_cast<uintptr_t>(W8) % 16 != 0)
+        return fail(LMS_ERR_UNSUPPORTED, "H and W8 must be 16-byte aligned");
+    if (params->path != LMS_PATH_AUTO && params->path != LMS_PATH_TCGEN05)
+        return fail(LMS_ERR_UNSUPPORTED, "the FP8 path runs on the tcgen05 kernel only");
+    if (workspace == nullptr || workspace_bytes < t.workspace)
+        return fail(LMS_ERR_WORKSPACE, "workspace of %zu bytes needed", t.workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    lms::SampleArgs a = make_args(params, B, V, t, workspace);
+    const size_t cand = static_cast<size_t>(B) * static_cast<size_t>(t.n_tiles) * 4;
+    const int64_t ldq = static_cast<int64_t>(round_up(static_cast<size_t>(D), 16));
+    uint8_t* q = static_cast<uint8_t*>(workspace) + 2 * round_up(cand, 256);
+    int32_t* h_exp = reinterpret_cast<int32_t*>(q + round_up(static_cast<size_t>(B) * ldq, 256));
+    a.h_exp = h_exp;
+    a.w_scale = w_scale;
+    cudaError_t e = lms::launch_quantize_rows_e4m3(static_cast<const uint16_t*>(H), ldh, B, D, q, ldq, h_exp, s);
+    if (e != cudaSuccess) return cuda_fail(e, "activation quantisation launch");
+    CUtensorMap tmW;
+    if ((st = encode_map(&tmW, W8, V, D, ldw8, 128, true)) != LMS_OK) return st;
+    const bool wide = params->noise_mode == LMS_NOISE_WIDE53;
+    const uint32_t timeout_ms = params->timeout_ms ? params->timeout_ms : 2000u;
+    for (int64_t r0 = 0; r0 < B; r0 += kTcMaxBatchPerLaunch) {
+        const int64_t nb = (B - r0 < kTcMaxBatchPerLaunch) ? B - r0 : kTcMaxBatchPerLaunch;
+        const int n_pad = static_cast<int>(nb < 16 ? 16 : (nb + 15) / 16 * 16);
+        CUtensorMap tmH;
+        if ((st = encode_map(&tmH, q, B, D, ldq, n_pad, true)) != LMS_OK) return st;
+        lms::SampleArgs ac = a;
+        ac.B = nb;
+        ac.row0 = r0;
+        ac.cand_score = a.cand_score + r0 * t.n_tiles;
+        ac.cand_index = a.cand_index + r0 * t.n_tiles;
+        e = lms::launch_lmhead_tc(tmW, tmH, D, n_pad, wide, timeout_ms, params->debug_flags, ac, s, true);
+        if (e != cudaSuccess) return cuda_fail(e, "tcgen05 FP8 Stage-1 launch");
+    }
+    e = lms::launch_stage2(a.cand_score, a.cand_index, t.n_tiles, B, params->temperature, out,
+                           params->row_status, s);
+    if (e != cudaSuccess) return cuda_fail(e, "Stage-2 launch");
+    return LMS_OK;
+}
+
 lms_status lms_sample_from_logits(const void* logits, int32_t dtype, int64_t ld, int64_t B,
                                   int64_t V, const lms_sample_params* params, int64_t* out,
                                   void* workspace, size_t workspace_bytes, void* stream) {
@@ -323,6 +392,8 @@ lms_status lms_sample_from_logits_filtered(const void* logits, int32_t dtype, in
     f.a.n_tiles = 0;
     f.a.cand_score = nullptr;
     f.a.cand_index = nullptr;
+    f.a.h_exp = nullptr;
+    f.a.w_scale = nullptr;
     f.top_k = filters->top_k;
     f.top_p = filters->top_p;
     f.min_p = filters->min_p;

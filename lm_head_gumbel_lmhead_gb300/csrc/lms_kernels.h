@@ -24,6 +24,9 @@ struct SampleArgs {
     int64_t n_tiles;  // candidate columns per row in the workspace
     float* cand_score;  // [B][n_tiles] (already offset to row0)
     int* cand_index;    // [B][n_tiles]
+    // FP8 (W8A8) fused path only, else null: logits = acc * 2^h_exp[row] * w_scale[v]
+    const int32_t* h_exp;
+    const float* w_scale;
 };
 
 // The filtered race (one CTA per row; writes tokens and statuses directly).
@@ -39,6 +42,9 @@ struct FilterArgs {
 
 cudaError_t launch_filtered_race(const void* logits, bool bf16, int64_t ld, bool wide,
                                  const FilterArgs& f, cudaStream_t stream);
+
+cudaError_t launch_quantize_rows_e4m3(const uint16_t* H, int64_t ldh, int64_t B, int64_t D,
+                                      uint8_t* q, int64_t ldq, int32_t* e_out, cudaStream_t stream);
 
 cudaError_t launch_noise_fill(void* out, int kind, bool wide, int64_t B, int64_t V,
                               const int64_t* seeds, const int64_t* positions, uint64_t base_seed,
@@ -56,9 +62,10 @@ cudaError_t launch_lmhead_gemv(const uint16_t* H, int64_t ldh, const uint16_t* W
 
 // The tcgen05 path.  tmW / tmH are TMA descriptors (bf16, 128-byte swizzle, boxes of 64 x 128
 // for W and 64 x n_pad for H).  B <= 256 per launch.
+// fp8: E4M3 operands (kind::f8f6f4), boxes of 128 x 128 / 128 x n_pad bytes; a.h_exp / a.w_scale set.
 cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int64_t D, int n_pad,
                              bool wide, uint32_t timeout_ms, uint32_t debug_flags,
-                             const SampleArgs& a, cudaStream_t stream);
+                             const SampleArgs& a, cudaStream_t stream, bool fp8 = false);
 
 // The CTA-pair tcgen05 path (cta_group::2, M = 256): tmH boxes are 64 x (n_pad / 2).
 cudaError_t launch_lmhead_tc_pair(const CUtensorMap& tmW, const CUtensorMap& tmH, int64_t D,

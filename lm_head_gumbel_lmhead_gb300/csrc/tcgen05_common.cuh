@@ -118,6 +118,17 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, E4M3 inputs (K = 32 per instruction), fp32 accumulate.
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when all tcgen05 operations issued so far by this thread have completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
@@ -186,6 +197,12 @@ __device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t saddr) {
     return d;
 }
 
+// Instruction descriptor, kind::f8f6f4: fp32 accumulator, E4M3 A and B (format code 0), both
+// K-major, N and M.
+__host__ __device__ constexpr uint32_t mma_idesc_e4m3(int n, int m) {
+    return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major, N and M.
 __host__ __device__ constexpr uint32_t mma_idesc_bf16(int n, int m) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
@@ -239,6 +256,12 @@ __device__ __forceinline__ void epilogue_tile_columns(const SampleArgs& a, const
                     gumbel_run<kWide, 8>(p.key, static_cast<uint32_t>(v0), g);
                 }
                 const int64_t row = a.row0 + b;
+                if (a.w_scale) {                 // FP8 inputs: logits = acc * 2^e_h * w_scale
+                    const int eh = a.h_exp[row];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (v0 + e < a.V) y[e] *= ldexpf(__ldg(a.w_scale + v0 + e), eh);
+                }
                 const float* brow = a.bias ? a.bias + row * a.ld_bias : nullptr;
                 // the eight entries share one mask word (v0 is a multiple of 8)
                 const uint32_t mword =

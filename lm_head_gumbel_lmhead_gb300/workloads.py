@@ -136,3 +136,20 @@ def logits_normal(B: int, V: int, std: float = 2.0, seed: int = 0,
                   dtype: torch.dtype = torch.float32) -> torch.Tensor:
     """Materialised logits ~ N(0, std^2) in fp32 or bf16."""
     return (torch.randn(B, V, generator=_gen(seed + 41)) * std).to(dtype)
+
+
+def quantize_weight_e4m3(W: torch.Tensor, chunk_rows: int = 8192):
+    """Offline per-row FP8 (E4M3) weight quantisation, as a model would ship its LM head:
+    w_scale[v] = max_d |W[v][d]| / 448 (fp32, 1 for an all-zero row), W8 = E4M3(W / w_scale)
+    (torch's float8_e4m3fn cast), returned as (uint8 codes [V, D], fp32 scales [V])."""
+    V, D = W.shape
+    W8 = torch.empty(V, D, dtype=torch.uint8)
+    scale = torch.empty(V, dtype=torch.float32)
+    for r0 in range(0, V, chunk_rows):
+        r1 = min(V, r0 + chunk_rows)
+        w = W[r0:r1].float()
+        s = w.abs().amax(dim=1) / 448.0
+        s = torch.where(s > 0, s, torch.ones_like(s))
+        scale[r0:r1] = s
+        W8[r0:r1] = (w / s[:, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+    return W8, scale
