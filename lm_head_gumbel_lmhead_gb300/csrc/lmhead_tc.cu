@@ -129,6 +129,8 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
+            // FP8 inputs: H8 is written by the quantisation kernel this launch may overlap
+            if (kFp8) pdl_wait_primary();
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_h = l2_policy_evict_last();
             uint32_t issued = 0, issued_parity = 0;   // per-stage: load in flight, its phase
@@ -206,6 +208,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     } else {
         // ---------------- epilogue ----------------
         const int epi_tid = threadIdx.x - 64;
+        if (kFp8) pdl_wait_primary();   // the activation exponents come from the quantisation kernel
         const int epi_threads = 32 * kEpiWarps;
         const int quad = warp & 3;                       // TMEM lanes 32*quad .. 32*quad+31
         const int col_group = (warp - 2) >> 2;           // which column chunks this warp takes
@@ -263,8 +266,23 @@ cudaError_t launch_variant(const CUtensorMap& tmW, const CUtensorMap& tmH, const
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    kern<<<grid, 32 * (2 + kEpiWarps), smem, stream>>>(tmW, tmH, prm);
-    return cudaGetLastError();
+    if (!kFp8) {
+        kern<<<grid, 32 * (2 + kEpiWarps), smem, stream>>>(tmW, tmH, prm);
+        return cudaGetLastError();
+    }
+    // FP8: a programmatic dependent of the activation quantisation, so the prologue (barriers,
+    // TMEM, descriptor prefetch) overlaps it; the roles that read its output wait for it.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(32 * (2 + kEpiWarps));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmW, tmH, prm);
 }
 
 }  // namespace

@@ -7,10 +7,12 @@
 // normalised except the top-p prefix mass.
 //
 // One CTA of 1024 threads per row:
-//   1. radix select (4 passes of 8 bits over order-preserving 32-bit keys of t) finds the key of
-//      the k-th largest entry, k = min(top_k, k_max) (k_max when only top-p is on);
-//   2. one pass gathers exactly k candidates: every key above it and, in index order, the first
-//      entries equal to it (ties keep the smallest indices);
+//   1. radix select (4 passes of 8 bits over order-preserving 32-bit keys of t, histograms built
+//      with warp-aggregated shared-memory atomics) finds the key K of the k-th largest entry,
+//      k = min(top_k, k_max) (k_max when only top-p is on); if fewer entries equal to K are kept
+//      than exist, a second radix select over their indices finds the largest kept index, so ties
+//      keep the smallest indices;
+//   2. one pass gathers exactly k candidates (key > K, or key == K and index <= that bound);
 //   3. a bitonic sort in shared memory orders them by (t descending, v ascending);
 //   4. fp32 prefix sums of exp(t_i - t_0) give the top-p cut, a threshold t_0 + log(min_p) the
 //      min-p cut;
@@ -132,6 +134,65 @@ __device__ __forceinline__ void block_argmax(float& s, int& i, float* shs, int* 
     i = shi[0];
 }
 
+// hist[bin] += 1 for every thread with `in`, one shared-memory atomic per distinct bin per warp.
+// Every lane of the warp must call it (full-mask ballot).
+__device__ __forceinline__ void hist_add(int* hist, uint32_t bin, bool in) {
+    const unsigned active = __ballot_sync(0xffffffffu, in);
+    if (in) {
+        const unsigned peers = __match_any_sync(active, bin);
+        if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+    }
+}
+
+// Warp 0 (called by its 32 lanes): the bin where the count from the top (bin 255 down) reaches
+// `need`; writes the bin and the rank left inside it.  Lane l owns bins 255-8l .. 248-8l.
+__device__ __forceinline__ void find_bin_desc(const int* hist, int need, int* bin_out, int* rem_out) {
+    const int l = threadIdx.x & 31;
+    int local = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) local += hist[255 - 8 * l - j];
+    int incl = local;
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (l >= off) incl += y;
+    }
+    const int excl = incl - local;
+    if (excl < need && need <= incl) {
+        int cum = excl, j = 0;
+        for (; j < 7; ++j) {
+            const int h = hist[255 - 8 * l - j];
+            if (cum + h >= need) break;
+            cum += h;
+        }
+        *bin_out = 255 - 8 * l - j;
+        *rem_out = need - cum;
+    }
+}
+
+// The same from the bottom (bin 0 up), for the ascending index select.
+__device__ __forceinline__ void find_bin_asc(const int* hist, int need, int* bin_out, int* rem_out) {
+    const int l = threadIdx.x & 31;
+    int local = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) local += hist[8 * l + j];
+    int incl = local;
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (l >= off) incl += y;
+    }
+    const int excl = incl - local;
+    if (excl < need && need <= incl) {
+        int cum = excl, j = 0;
+        for (; j < 7; ++j) {
+            const int h = hist[8 * l + j];
+            if (cum + h >= need) break;
+            cum += h;
+        }
+        *bin_out = 8 * l + j;
+        *rem_out = need - cum;
+    }
+}
+
 template <typename T, bool kWide>
 __global__ void __launch_bounds__(kThreads, 1) filtered_race_kernel(const T* __restrict__ logits,
                                                                     int64_t ld, FilterArgs f) {
@@ -165,18 +226,13 @@ __global__ void __launch_bounds__(kThreads, 1) filtered_race_kernel(const T* __r
     const bool minp_on = mp > 0.0f && mp <= 1.0f;
     const bool greedy = r.p.flags & kRowGreedy;
 
-    // t_max over the row (also tells whether any entry is above -inf)
-    float tmax = -CUDART_INF_F;
-    for (int64_t v = tid; v < V; v += kThreads) tmax = fmaxf(tmax, t_of<T>(r, v));
-    tmax = block_max(tmax, shf);
-    if (!(tmax > -CUDART_INF_F)) {
-        if (tid == 0) { f.out[b] = -1; if (f.row_status) f.row_status[b] = 1; }
-        return;
-    }
-
     float best_s = -CUDART_INF_F;
     int best_i = kNoIndex;
     if (greedy || !(topk_on || topp_on)) {
+        // t_max over the row (for the min-p threshold)
+        float tmax = -CUDART_INF_F;
+        for (int64_t v = tid; v < V; v += kThreads) tmax = fmaxf(tmax, t_of<T>(r, v));
+        tmax = block_max(tmax, shf);
         // greedy rows, min-p only, or no filter: one threshold race over the row.  Greedy rows
         // need no filter (every filter keeps the top token).
         const float thr = (minp_on && !greedy) ? tmax + logf(mp) : -CUDART_INF_F;
@@ -205,20 +261,15 @@ __global__ void __launch_bounds__(kThreads, 1) filtered_race_kernel(const T* __r
         for (int shift = 24; shift >= 0; shift -= 8) {
             if (tid < 256) hist[tid] = 0;
             __syncthreads();
-            for (int64_t v = tid; v < V; v += kThreads) {
-                const uint32_t key = order_key(t_of<T>(r, v));
-                if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+            // whole 1024-wide chunks, so that every lane of every warp reaches hist_add
+            for (int64_t base = 0; base < V; base += kThreads) {
+                const int64_t v = base + tid;
+                const bool valid = v < V;
+                const uint32_t key = valid ? order_key(t_of<T>(r, v)) : 0u;
+                hist_add(hist, (key >> shift) & 255u, valid && (key & pmask) == prefix);
             }
             __syncthreads();
-            if (tid == 0) {
-                int cum = 0, d = 255;
-                for (; d > 0; --d) {
-                    if (cum + hist[d] >= remaining) break;
-                    cum += hist[d];
-                }
-                sh_int[0] = d;
-                sh_int[1] = remaining - cum;
-            }
+            if (tid < 32) find_bin_desc(hist, remaining, &sh_int[0], &sh_int[1]);
             __syncthreads();
             prefix |= static_cast<uint32_t>(sh_int[0]) << shift;
             pmask |= 255u << shift;
@@ -227,28 +278,50 @@ __global__ void __launch_bounds__(kThreads, 1) filtered_race_kernel(const T* __r
         }
         const uint32_t kstar = prefix;   // the k-th largest key
         const int need_eq = remaining;   // entries equal to it that are kept (smallest indices)
-        // ---- 2. gather exactly min(k, V) candidates ----
-        if (tid == 0) { sh_int[2] = 0; sh_int[3] = 0; }
+        // ties at K: the need_eq-th smallest index among entries with key == K, by a radix select
+        // over the index bits (ascending); skipped when every such entry is kept
+        int eq_count = 0;
+        for (int64_t v = tid; v < V; v += kThreads) eq_count += order_key(t_of<T>(r, v)) == kstar;
+        eq_count = block_sum<int>(eq_count, shi);
+        uint32_t vmax = 0xffffffffu;
+        if (need_eq < eq_count) {
+            int bits = 1;
+            while ((int64_t{1} << bits) < V) ++bits;
+            uint32_t vprefix = 0, vmask = 0;
+            int rem = need_eq;
+            for (int shift = ((bits + 7) / 8 - 1) * 8; shift >= 0; shift -= 8) {
+                if (tid < 256) hist[tid] = 0;
+                __syncthreads();
+                for (int64_t base = 0; base < V; base += kThreads) {
+                    const int64_t v = base + tid;
+                    const bool in = v < V && order_key(t_of<T>(r, v)) == kstar &&
+                                    (static_cast<uint32_t>(v) & vmask) == vprefix;
+                    hist_add(hist, (static_cast<uint32_t>(v) >> shift) & 255u, in);
+                }
+                __syncthreads();
+                if (tid < 32) find_bin_asc(hist, rem, &sh_int[0], &sh_int[1]);
+                __syncthreads();
+                vprefix |= static_cast<uint32_t>(sh_int[0]) << shift;
+                vmask |= 255u << shift;
+                rem = sh_int[1];
+                __syncthreads();
+            }
+            vmax = vprefix;
+        }
+        // ---- 2. gather exactly min(k, V) candidates (unordered; sorted next) ----
+        if (tid == 0) sh_int[2] = 0;
         cand[tid] = 0ull;                // below every real candidate (kMaxK == kThreads)
         __syncthreads();
-        for (int64_t base = 0; base < V; base += kThreads) {
-            const int64_t v = base + tid;
-            const uint32_t key = v < V ? order_key(t_of<T>(r, v)) : 0u;
-            const int eq = (v < V && key == kstar) ? 1 : 0;
-            const int taken_before = sh_int[3];
-            int eq_rank = 0;
-            if (__syncthreads_or(eq)) eq_rank = block_scan_incl<int>(eq, hist) - eq;
-            const bool take = (v < V && key > kstar) || (eq && taken_before + eq_rank < need_eq);
-            if (take) {
+        for (int64_t v = tid; v < V; v += kThreads) {
+            const uint32_t key = order_key(t_of<T>(r, v));
+            if (key > kstar || (key == kstar && static_cast<uint32_t>(v) <= vmax)) {
                 const int pos = atomicAdd(&sh_int[2], 1);
                 if (pos < kMaxK)
                     cand[pos] = (static_cast<unsigned long long>(key) << 32) |
                                 static_cast<uint32_t>(~static_cast<uint32_t>(v));
             }
-            const int eq_total = __syncthreads_count(eq);
-            if (tid == 0) sh_int[3] = taken_before + eq_total;
-            __syncthreads();
         }
+        __syncthreads();
         const int n_cand = sh_int[2] < kMaxK ? sh_int[2] : kMaxK;
         // ---- 3. bitonic sort, descending ----
         for (int size = 2; size <= kMaxK; size <<= 1) {

@@ -16,6 +16,7 @@ constexpr int kThreads = 256;
 __global__ void __launch_bounds__(kThreads) quantize_rows_e4m3_kernel(
     const __nv_bfloat16* __restrict__ H, int64_t ldh, int64_t D, uint8_t* __restrict__ q,
     int64_t ldq, int32_t* __restrict__ e_out) {
+    pdl_launch_dependents();          // the fused kernel may start its prologue now
     const int64_t b = blockIdx.x;
     const __nv_bfloat16* h = H + b * ldh;
     float amax = 0.0f;
