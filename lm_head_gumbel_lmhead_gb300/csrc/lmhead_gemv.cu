@@ -146,13 +146,11 @@ cudaError_t launch_b(const uint16_t* H, int64_t ldh, const uint16_t* W, int64_t 
     const unsigned grid = static_cast<unsigned>(a.n_tiles);
     cudaError_t e;
     if (wide) {
-        e = cudaFuncSetAttribute(lmhead_gemv_kernel<kB, true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        e = ensure_dynamic_smem(reinterpret_cast<const void*>(lmhead_gemv_kernel<kB, true>), smem);
         if (e != cudaSuccess) return e;
         lmhead_gemv_kernel<kB, true><<<grid, kThreads, smem, stream>>>(H, ldh, W, ldw, static_cast<int>(D), a);
     } else {
-        e = cudaFuncSetAttribute(lmhead_gemv_kernel<kB, false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        e = ensure_dynamic_smem(reinterpret_cast<const void*>(lmhead_gemv_kernel<kB, false>), smem);
         if (e != cudaSuccess) return e;
         lmhead_gemv_kernel<kB, false><<<grid, kThreads, smem, stream>>>(H, ldh, W, ldw, static_cast<int>(D), a);
     }

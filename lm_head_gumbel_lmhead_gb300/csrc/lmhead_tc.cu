@@ -263,8 +263,7 @@ template <int kEpiWarps, bool kWide, bool kFp8>
 cudaError_t launch_variant(const CUtensorMap& tmW, const CUtensorMap& tmH, const TcParams& prm,
                            size_t smem, int grid, cudaStream_t stream) {
     auto kern = lmhead_tc_kernel<kEpiWarps, kWide, kFp8>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     if (!kFp8) {
         kern<<<grid, 32 * (2 + kEpiWarps), smem, stream>>>(tmW, tmH, prm);

@@ -375,8 +375,7 @@ template <bool kWide>
 cudaError_t launch_pair_variant(const CUtensorMap& tmW, const CUtensorMap& tmH, const PairParams& prm,
                                 size_t smem, int64_t n_super, cudaStream_t stream) {
     auto kern = lmhead_tc_pair_kernel<kWide>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];

@@ -1,13 +1,15 @@
 // C-ABI entry points (include/lms.h): argument checks, tiling, TMA descriptors, launches.
 // Host-detectable errors return before anything is launched; nothing here allocates device
-// memory or keeps state between calls.
+// memory; the only state kept between calls is per-device launch settings (kernel attributes).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "lms.h"
 #include "lms_kernels.h"
@@ -181,6 +183,20 @@ lms_status encode_bf16_map(CUtensorMap* tm, const void* ptr, int64_t rows, int64
 
 namespace lms {
 void set_last_error(const char* msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+
+cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void*>, size_t> limits;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    size_t& have = limits[std::make_pair(dev, kernel)];
+    if (have >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e == cudaSuccess && bytes > have) have = bytes;
+    return e;
+}
 
 int device_sm_count() {
     int dev = 0, sms = 0;

@@ -74,6 +74,10 @@ cudaError_t launch_lmhead_tc_pair(const CUtensorMap& tmW, const CUtensorMap& tmH
 
 int device_sm_count();
 
+// Raises `kernel`'s dynamic shared-memory limit on the current device to at least `bytes`; the
+// runtime is called only when the limit cached for (device, kernel) is lower.
+cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
+
 // Sets the thread-local message that lms_last_error() returns.
 void set_last_error(const char* msg);
 

@@ -171,3 +171,90 @@ def test_batch_position_invariance_with_filters_full_vocab(filters):
     if "top_k" in filters:
         args["top_k"] = np.full(4, filters["top_k"], np.int32)
     check_filtered(full[:4].cpu().numpy(), np.zeros(4, np.int32), y, **args)
+
+
+@pytest.mark.parametrize("dtype,wide", [(torch.float32, False), (torch.bfloat16, True)])
+def test_parity_multi_cta_rows_with_ties_across_slices(dtype, wide):
+    """Rows long enough to span several CTAs of a cluster, with logits on a coarse grid so that
+    the k-th value is shared by entries in different slices (the index cut at K)."""
+    rng = np.random.default_rng(17)
+    B, V = 6, 50_000
+    y = np.round(rng.standard_normal((B, V)) * 8.0) / 4.0          # many exact ties
+    logits = torch.from_numpy(y.astype(np.float32)).to(dtype)
+    yd = logits.double().numpy()
+    T = np.array([1.0, 0.5, 0.8, 1.25, 0.7, 2.0], np.float32)
+    top_k = np.array([37, 500, 1000, 0, 3, 1024], np.int32)
+    top_p = np.array([1.0, 0.9, 1.0, 0.95, 0.5, 0.3], np.float32)
+    min_p = np.array([0.0, 0.0, 0.1, 0.0, 0.0, 0.02], np.float32)
+    seeds = np.arange(B, dtype=np.int64) + 77
+    pos = np.arange(B, dtype=np.int64) * 5
+    allowed = rng.random((B, V)) < 0.9
+    allowed[:3] = True
+    mask = workloads.pack_allow_bits(torch.from_numpy(allowed)).numpy()
+    kw = dict(temperature=T, top_k=top_k, top_p=top_p, min_p=min_p, seeds=seeds, positions=pos,
+              mask=mask, base_seed=5, offset=9, wide=wide)
+    for rep in range(3):                                              # several positions
+        kw["positions"] = pos + 1000 * rep
+        g_out, g_st = _gpu(logits.to(DEV), **kw)
+        kw_o = dict(kw, temperature=T.astype(np.float64), top_p=top_p.astype(np.float64),
+                    min_p=min_p.astype(np.float64))
+        check_filtered(g_out, g_st, yd, **kw_o)
+
+
+@pytest.mark.parametrize("filters", [dict(top_k=50), dict(top_k=50, top_p=0.9), dict(top_p=0.5)])
+def test_tail_row_keeps_smallest_indices_at_the_cut(filters):
+    """The Megatron-LM PR's tail row [0, -D, ..., -D] (V = 131072): every entry but the first ties
+    at the k-th value, so the kept set is {0} and the smallest tied indices."""
+    V, B = 131072, 32
+    row = workloads.tail_row(V, 0.999)
+    seeds = np.arange(B, dtype=np.int64)
+    kw = {k: np.full(B, v, np.int32 if k == "top_k" else np.float32) for k, v in filters.items()}
+    g_out, g_st = _gpu(row.to(DEV), B=B, seeds=seeds, positions=seeds, **kw)
+    check_filtered(g_out, g_st, row.double().numpy(), B=B, seeds=seeds, positions=seeds,
+                   **{k: (v.astype(np.float64) if v.dtype == np.float32 else v) for k, v in kw.items()})
+    k = filters.get("top_k", 1024)
+    assert (g_st == 0).all() and (g_out < k).all()
+
+
+def test_parity_rows_beyond_the_shared_memory_slice():
+    """V = 800000: a slice no longer fits in shared memory, so keys are recomputed from global
+    memory on every pass."""
+    rng = np.random.default_rng(23)
+    B, V = 3, 800_000
+    logits = workloads.logits_normal(B, V, std=2.0, seed=12, dtype=torch.float32)
+    y = logits.double().numpy()
+    T = np.array([0.9, 1.0, 0.6], np.float32)
+    top_k = np.array([100, 0, 1024], np.int32)
+    top_p = np.array([0.95, 0.8, 1.0], np.float32)
+    seeds = np.array([1, -1, 3], np.int64)
+    pos = np.array([4, 5, 6], np.int64)
+    kw = dict(temperature=T, top_k=top_k, top_p=top_p, seeds=seeds, positions=pos, base_seed=2)
+    g_out, g_st = _gpu(logits.to(DEV), **kw)
+    check_filtered(g_out, g_st, y, **dict(kw, temperature=T.astype(np.float64),
+                                          top_p=top_p.astype(np.float64)))
+
+
+@pytest.mark.parametrize("wide", [False, True])
+def test_parity_outliers_and_bf16_ties(wide):
+    """Rows that leave the near window (an outlier maximum, so fewer than k entries lie within two
+    octaves of it) and bf16 rows whose ties make the boundary bin hold many equal keys."""
+    B, V = 6, 40_000
+    logits = workloads.logits_normal(B, V, std=2.0, seed=31, dtype=torch.float32)
+    logits[0, 777] = 60.0                        # one outlier, top-k 50: the full-width select
+    logits[1, [5, 30000, 39999]] = torch.tensor([45.0, 44.0, 46.0])
+    logits = logits.to(torch.bfloat16)           # bf16: about a thousand distinct values per row
+    y = logits.double().numpy()
+    T = np.array([1.0, 0.8, 0.7, 1.3, 0.9, 0.6], np.float32)
+    top_k = np.array([50, 0, 1024, 700, 1000, 200], np.int32)
+    top_p = np.array([1.0, 0.9, 0.95, 0.8, 1.0, 0.99], np.float32)
+    min_p = np.array([0.0, 0.0, 0.0, 0.05, 0.01, 0.0], np.float32)
+    seeds = np.arange(B, dtype=np.int64) + 900
+    for rep in range(3):
+        pos = np.arange(B, dtype=np.int64) + 50 * rep
+        kw = dict(temperature=T, top_k=top_k, top_p=top_p, min_p=min_p, seeds=seeds, positions=pos,
+                  wide=wide)
+        g_out, g_st = _gpu(logits.to(DEV), **kw)
+        check_filtered(g_out, g_st, y, **dict(kw, temperature=T.astype(np.float64),
+                                              top_p=top_p.astype(np.float64),
+                                              min_p=min_p.astype(np.float64)))
+        assert g_out[0] == 777
