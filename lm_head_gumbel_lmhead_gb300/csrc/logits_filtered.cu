@@ -50,8 +50,6 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-// k_max <= 1024 entries survive the top-k cut; the top-p scan gives each thread two of them.
-static_assert(2 * kThreads >= 1024, "top-p scan covers 1024 entries");
 // The leader's candidate list: the kk <= 1024 entries of the top-k cut, or a superset of at most
 // kCap entries made of the entries above the bin holding the kk-th one plus that whole bin, when
 // the bin holds at most kTie entries (the leader then ranks the bin's entries among themselves).
