@@ -11,7 +11,8 @@ readings taken where the pages are silent are listed in ``lms_oracle.c``'s heade
 Every function here has a pin in ``tests/test_oracle_*.py`` (Philox against Triton's own
 Philox run in its CPU interpreter, the noise ranges the Megatron-LM PR prints, the tail-rate
 closed form, chi-square against softmax, brute force over tile widths, fp64 GEMM against
-numpy's matmul, greedy against numpy's argmax).
+numpy's matmul, greedy against numpy's argmax, the filters' hand-worked kept sets, the E4M3
+codec against torch's cast, the Plackett-Luce law of Gumbel-top-k).
 """
 from __future__ import annotations
 
@@ -64,7 +65,7 @@ def _load():
                                                  P, i64, u64, u64, i32, i64, P, P, P]
             lib.orc_lmhead_sample_rows.argtypes = [P, i64, P, i64, i64, i64, i64, P, i64, P, P,
                                                    P, P, i64, P, i64, u64, u64, i32, i64, P, P,
-                                                   P, P, P, P, i32]
+                                                   P, P, P, P, P, i32]
             lib.orc_lmhead_sample_rows.restype = ctypes.c_int
             lib.orc_sample_filtered.argtypes = [P, i64, i64, i64, P, P, P, P, i64, P, i64, u64, u64,
                                                 i32, P, P, P, i32, ctypes.c_double,
@@ -230,9 +231,10 @@ def lmhead_sample(H_bits, W_bits, *, temperature=None, seeds=None, positions=Non
 
 def lmhead_sample_rows(H_bits, W_bits, rows, *, temperature=None, seeds=None, positions=None,
                        bias=None, mask=None, base_seed=0, offset=0, wide=False, tile_v=128,
-                       threads=None) -> RowResult:
+                       want_scores=False, threads=None) -> RowResult:
     """The fused path's result for chosen batch rows of a B-row problem (each row keeps its own
-    parameters and its batch index), for sampled checks at full size."""
+    parameters and its batch index), for sampled checks at full size; with want_scores, also
+    every perturbed score of those rows."""
     H, W = _bits16(H_bits), _bits16(W_bits)
     B, D = H.shape
     V = W.shape[0]
@@ -244,11 +246,11 @@ def lmhead_sample_rows(H_bits, W_bits, rows, *, temperature=None, seeds=None, po
     mask_a = _c(mask, np.uint32)
     ld_mask = 0 if mask_a is None or mask_a.ndim == 1 else mask_a.shape[1]
     seeds_a, pos_a = _c(seeds, np.int64), _c(positions, np.int64)
-    outs = _row_outputs(n, V, tile_v, False)
+    outs = _row_outputs(n, V, tile_v, want_scores)
     rc = _load().orc_lmhead_sample_rows(
         _ptr(H), D, _ptr(W), D, B, D, V, _ptr(rows), n, _ptr(T), _ptr(seeds_a), _ptr(pos_a),
         _ptr(bias_a), ld_bias, _ptr(mask_a), ld_mask, base_seed, offset, int(bool(wide)), tile_v,
-        *[_ptr(o) for o in outs[:6]], threads or default_threads())
+        *[_ptr(o) for o in outs], threads or default_threads())
     if rc != 0:
         raise MemoryError("oracle could not allocate the fp64 logits")
     return RowResult(*outs)
@@ -308,6 +310,61 @@ def sample_filtered(logits, *, B=None, temperature=None, seeds=None, positions=N
     if want_top2:
         return out, status, kept, top1, top2
     return out, status, kept
+
+
+# ---- Gumbel-top-k: k draws without replacement ----
+
+def topk_from_scores(scores, k: int):
+    """Gumbel-top-k (FlashSampling "Limitations" and "Future directions": sampling without
+    replacement through Gumbel-top-k): per row, the k largest perturbed scores, in order (larger
+    score first, then the smaller index); -inf is never taken.  Returns (indices [B, k] int64,
+    with -1 where fewer than k scores are finite; scores [B, k], -inf there)."""
+    s = np.asarray(scores, dtype=np.float64)
+    B = s.shape[0]
+    idx = np.full((B, k), -1, np.int64)
+    val = np.full((B, k), -np.inf)
+    for b in range(B):
+        fin = np.nonzero(s[b] > -np.inf)[0]
+        order = fin[np.lexsort((fin, -s[b][fin]))]     # score descending, then index ascending
+        m = min(k, order.shape[0])
+        idx[b, :m] = order[:m]
+        val[b, :m] = s[b][order[:m]]
+    return idx, val
+
+
+def tile_topk_from_scores(scores, k: int, tile_v: int):
+    """The same selection within each vocabulary tile of tile_v entries: ([B, nt, k], [B, nt, k])."""
+    s = np.asarray(scores, dtype=np.float64)
+    B, V = s.shape
+    nt = (V + tile_v - 1) // tile_v
+    idx = np.full((B, nt, k), -1, np.int64)
+    val = np.full((B, nt, k), -np.inf)
+    for t in range(nt):
+        i, x = topk_from_scores(s[:, t * tile_v:(t + 1) * tile_v], k)
+        idx[:, t] = np.where(i >= 0, i + t * tile_v, -1)
+        val[:, t] = x
+    return idx, val
+
+
+def gumbel_topk(logits, k: int, **race_kw):
+    """Gumbel-top-k over materialised logits: the race's perturbed scores (``sample_from_logits``,
+    same transform and noise), then ``topk_from_scores``.  Returns (indices [B, k], scores [B, k],
+    status [B]) with the race's statuses (1: no finite score, 2: invalid temperature)."""
+    r = sample_from_logits(logits, want_scores=True, **race_kw)
+    idx, val = topk_from_scores(r.scores, k)
+    return idx, val, r.status
+
+
+def lmhead_gumbel_topk(H_bits, W_bits, k: int, rows=None, **race_kw):
+    """Gumbel-top-k of the fused path (fp64 logits H W^T, then ``gumbel_topk``'s selection), for
+    all rows or for chosen batch rows of a larger batch (each keeps its parameters and index)."""
+    H = _bits16(H_bits)
+    if rows is None:
+        rows = np.arange(H.shape[0])
+    race_kw.setdefault("tile_v", 128)
+    r = lmhead_sample_rows(H_bits, W_bits, rows, want_scores=True, **race_kw)
+    idx, val = topk_from_scores(r.scores, k)
+    return idx, val, r.status, r.scores
 
 
 # ---- FP8 (E4M3) inputs: W8A8 with per-row scales ----

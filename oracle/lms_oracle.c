@@ -397,20 +397,22 @@ void orc_lmhead_scores_at(const uint16_t* H, int64_t ldh, const uint16_t* W, int
 
 /* The fused path's result for a subset of the batch: rows[i] (i < n_rows) are batch rows of the
  * full B-row problem (their own temperature, seed, position, bias and mask rows, and row index
- * for unseeded keys); outputs are [n_rows] / [n_rows][n_tiles]. */
+ * for unseeded keys); outputs are [n_rows] / [n_rows][n_tiles], and the perturbed scores
+ * [n_rows][V] when `scores` is not NULL. */
 int orc_lmhead_sample_rows(const uint16_t* H, int64_t ldh, const uint16_t* W, int64_t ldw,
                            int64_t B, int64_t D, int64_t V, const int64_t* rows, int64_t n_rows,
                            const double* T, const int64_t* seeds, const int64_t* positions,
                            const double* bias, int64_t ld_bias, const uint32_t* mask,
                            int64_t ld_mask, uint64_t base_seed, uint64_t offset, int wide,
                            int64_t tile_v, int64_t* out, int32_t* status, double* top1,
-                           double* top2, double* tile_max, int64_t* tile_idx, int nthreads) {
+                           double* top2, double* tile_max, int64_t* tile_idx, double* scores,
+                           int nthreads) {
     double* y = (double*)malloc(sizeof(double) * (size_t)(n_rows * V));
     if (!y) return 1;
     orc_gemm(H, ldh, W, ldw, n_rows, D, V, y, rows, nthreads);
     orc_rows_args a = {y, V, B, V, T, seeds, positions, bias, ld_bias, mask, ld_mask,
                        base_seed, offset, wide, tile_v, out, status, top1, top2,
-                       tile_max, tile_idx, NULL, rows, n_rows};
+                       tile_max, tile_idx, scores, rows, n_rows};
     orc_run_rows(&a, nthreads);
     free(y);
     return 0;
