@@ -23,6 +23,8 @@ Workloads (synthetic, seeded; the shapes of the FlashSampling page's measurement
   to E4M3 with per-row scales, and H is quantised per row on the GPU each step (W8A8).
 - ``filtered``: ``lms_sample_from_logits_filtered`` with top-k 50 and top-p 0.9 at T = 0.7 over
   bf16 logits, V = 131072 (the Megatron-LM PR's filter settings).
+- ``qwen3-8b-topk``: the Qwen3-8B shape through ``lms_lmhead_sample_topk`` (Gumbel-top-k: k
+  draws without replacement per row, k = ``--topk``, default 8).
 
 Every input is larger than L2 (the fused workloads stream W of 1.05–4.3 GB), so no flush is needed.
 
@@ -60,7 +62,7 @@ UNIT = "us/step"
 TC_SOURCES = ["lm_head_gumbel_lmhead_gb300/csrc/lmhead_tc.cu",
               "lm_head_gumbel_lmhead_gb300/csrc/tcgen05_common.cuh",
               "lm_head_gumbel_lmhead_gb300/csrc/lms_device.cuh"]
-FUSED = ("qwen3-8b", "llama3-hetero", "large-vocab", "qwen3-8b-fp8")
+FUSED = ("qwen3-8b", "llama3-hetero", "large-vocab", "qwen3-8b-fp8", "qwen3-8b-topk")
 
 
 def kernel_source_hash() -> str:
@@ -194,7 +196,7 @@ class ClockSampler:
 # ------------------------------------------------------------------------------------------
 def make_workload(name: str, B: int, D: int, V: int):
     from lm_head_gumbel_lmhead_gb300 import workloads
-    if name in ("qwen3-8b", "qwen3-8b-fp8"):
+    if name in ("qwen3-8b", "qwen3-8b-fp8", "qwen3-8b-topk"):
         return workloads.qwen3_8b(B, D=D or 4096, V=V or 151936)
     if name == "llama3-hetero":
         return workloads.llama3_hetero(B, D=D or 4096, V=V or 128256)
@@ -333,9 +335,13 @@ def run_gpu(args):
         # positions advance with the step: one row per step, made before timing
         pos_all = (w.positions[None, :] + torch.arange(n_steps)[:, None]).contiguous().to(dev)
         fp8 = args.workload == "qwen3-8b-fp8"
+        topk = args.topk if args.workload == "qwen3-8b-topk" else 0
         tv, nt, ws_bytes, path = lms.tile_info(lms.OP_LMHEAD_FP8 if fp8 else lms.OP_LMHEAD, B, D, V)
+        if topk:
+            ws_bytes = lms.lib().lms_workspace_bytes_topk(B, V, topk)
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-        out = torch.empty(B, dtype=torch.int64, device=dev)
+        out = torch.empty((B, topk) if topk else (B,), dtype=torch.int64, device=dev)
+        scores_k = torch.empty(B, topk, dtype=torch.float32, device=dev) if topk else None
         wide = w.noise_mode == 1
         kw = dict(temperature=T, seeds=seeds, bias=bias, mask=mask, base_seed=w.base_seed,
                   offset=w.offset, wide=wide, out=out, workspace=workspace)
@@ -348,6 +354,9 @@ def run_gpu(args):
 
             def step(i):
                 lms.lmhead_sample_fp8(H, W8, wsc, positions=pos_all[i], **kw)
+        elif topk:
+            def step(i):
+                lms.lmhead_sample_topk(H, W, topk, positions=pos_all[i], scores=scores_k, **kw)
         else:
             def step(i):
                 lms.lmhead_sample(H, W, positions=pos_all[i], **kw)
@@ -357,13 +366,19 @@ def run_gpu(args):
             # W at one byte per weight plus its row scales; H read once, its E4M3 copy written
             # and read once
             alg = alg - V * D * 2 + V * D + V * 4 + 2 * B * D
+        if topk:
+            # the tiles' ordered k-lists written and read instead of one candidate each, and k
+            # indices and scores per row out
+            alg = alg - 2 * B * nt * 8 - B * 8 + 2 * B * nt * topk * 8 + B * topk * 12
         flops = 2 * B * V * D
-        config = {"workload": w.name + (" fp8-e4m3 W8A8" if fp8 else ""), "B": B, "D": D, "V": V,
+        config = {"workload": w.name + (" fp8-e4m3 W8A8" if fp8 else "") +
+                  (f" Gumbel-top-{topk}" if topk else ""), "B": B, "D": D, "V": V,
                   "noise": "wide53" if wide else "fp32",
                   "path": {1: "gemv", 2: "tcgen05"}[path], "tile_v": tv,
                   "l2": "inputs larger than L2 (W is %.2f GB), no flush" % (V * D * (1 if fp8 else 2) / 1e9)}
         kernel = ("quantize_rows_e4m3_kernel + " if fp8 else "") + \
-            "lmhead_tc_kernel + stage2_kernel (one step, CUDA events)"
+            ("lmhead_tc_kernel (top-k epilogue) + stage2_topk_kernel" if topk else
+             "lmhead_tc_kernel + stage2_kernel") + " (one step, CUDA events)"
     elif args.workload == "logits":
         V = args.V or 131072
         D = 0
@@ -448,7 +463,7 @@ def run_gpu(args):
         pos_h = pos_all.cpu().pin_memory()
         devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
         p_d = torch.empty(B, dtype=torch.int64, device=dev)
-        out_h = torch.empty(B, dtype=torch.int64).pin_memory()
+        out_h = torch.empty(tuple(out.shape), dtype=torch.int64).pin_memory()
 
         def e2e_step(i):
             for k, v in host.items():
@@ -459,6 +474,8 @@ def run_gpu(args):
                        offset=w.offset, wide=wide, out=out, workspace=workspace)
             if fp8:
                 lms.lmhead_sample_fp8(devb["H"], W8, wsc, **ekw)
+            elif topk:
+                lms.lmhead_sample_topk(devb["H"], W, topk, scores=scores_k, **ekw)
             else:
                 lms.lmhead_sample(devb["H"], W, **ekw)
             out_h.copy_(out, non_blocking=True)
@@ -466,7 +483,7 @@ def run_gpu(args):
         e2e_ms, _, _, _ = _time_steps(e2e_step, args.warmup, args.steps, dev, stream)
         e2e = {"value": round(max_over_ranks(e2e_ms, dev) * 1e3, 2), "unit": UNIT,
                "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()) + B * 8,
-               "d2h_bytes_per_step": B * 8}
+               "d2h_bytes_per_step": out.numel() * 8}
 
     if rank != 0:
         return
@@ -509,7 +526,7 @@ def run_gpu(args):
     if e2e is not None:
         line["e2e"] = e2e
     if not args.no_cpu_baseline:
-        if args.workload in FUSED and args.workload != "qwen3-8b-fp8":
+        if args.workload in ("qwen3-8b", "llama3-hetero", "large-vocab"):
             line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
         elif args.workload == "logits":
             threads = os.cpu_count() or 1
@@ -530,6 +547,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="qwen3-8b",
                     choices=list(FUSED) + ["logits", "noise", "filtered"])
     ap.add_argument("--batch", type=int, default=0)
+    ap.add_argument("--topk", type=int, default=8, help="k of the qwen3-8b-topk workload")
     ap.add_argument("--D", type=int, default=0)
     ap.add_argument("--V", type=int, default=0)
     ap.add_argument("--logits-dtype", choices=["fp32", "bf16"], default="bf16")

@@ -162,6 +162,26 @@ lms_status lms_lmhead_sample_fp8(const void* H, int64_t ldh, const void* W8, int
                                  const lms_sample_params* params, int64_t* out, void* workspace,
                                  size_t workspace_bytes, void* stream);
 
+/* Gumbel-top-k of the fused path: k draws without replacement per row (FlashSampling
+ * "Limitations" and "Future directions": sampling without replacement by Gumbel-top-k, useful for
+ * beam search).  The perturbed scores s = (y + bias) / T + g are lms_lmhead_sample's, with the
+ * same noise; the call returns each row's k largest, larger score first, then the smaller index.
+ * out[b][0] is the token lms_lmhead_sample draws.  Greedy rows (T == 0) get the k largest
+ * y + bias.  Masked entries are never drawn.
+ *   k        1 <= k <= LMS_TOPK_MAX
+ *   out      int64 [B][k] (device): vocabulary indices; -1 past a row's finite scores
+ *   scores   fp32 [B][k] (device) or NULL: the perturbed scores (-inf where out is -1)
+ *   workspace  lms_workspace_bytes_topk(B, V, k) bytes: the tiles' ordered key lists
+ *              uint64 [B][ceil(V / 128)][k]
+ * Row statuses as for lms_lmhead_sample (1: no finite score, 2: invalid T, 3: a bounded wait ran
+ * out).  Requirements as for lms_lmhead_sample; path AUTO or TCGEN05 (bf16 H and W). */
+#define LMS_TOPK_MAX 16
+size_t lms_workspace_bytes_topk(int64_t B, int64_t V, int32_t k);
+lms_status lms_lmhead_sample_topk(const void* H, int64_t ldh, const void* W, int64_t ldw, int64_t B,
+                                  int64_t D, int64_t V, int32_t k, const lms_sample_params* params,
+                                  int64_t* out, float* scores, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
 /* The same race over materialised logits [B][ld] (fp32 or bf16).  ld == 0 broadcasts one
  * row to all B draws (each draw keyed by its own row index / position).  Several CTAs share a
  * row (one per tile of tile_v entries); the noise is generated in registers.

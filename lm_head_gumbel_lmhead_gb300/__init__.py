@@ -105,6 +105,11 @@ def lib() -> ctypes.CDLL:
                                                           ctypes.POINTER(SampleParams),
                                                           ctypes.POINTER(FilterParams), P, P]
             L.lms_sample_from_logits_filtered.restype = i32
+            L.lms_workspace_bytes_topk.argtypes = [i64, i64, i32]
+            L.lms_workspace_bytes_topk.restype = sz
+            L.lms_lmhead_sample_topk.argtypes = [P, i64, P, i64, i64, i64, i64, i32,
+                                                 ctypes.POINTER(SampleParams), P, P, P, sz, P]
+            L.lms_lmhead_sample_topk.restype = i32
             L.lms_philox_fill_noise.argtypes = [P, i32, i32, i64, i64, P, P, u64, u64, P]
             L.lms_philox_fill_noise.restype = i32
             _lib = L
@@ -232,6 +237,44 @@ def lmhead_sample(H: torch.Tensor, W: torch.Tensor, *, temperature=None, seeds=N
                                    ctypes.byref(p), _ptr(out), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
+
+
+TOPK_MAX = 16
+
+
+def lmhead_sample_topk(H: torch.Tensor, W: torch.Tensor, k: int, *, temperature=None, seeds=None,
+                       positions=None, bias=None, mask=None, base_seed: int = 0, offset: int = 0,
+                       wide: bool = False, out=None, scores=None, want_scores: bool = True,
+                       workspace=None, row_status=None, timeout_ms: int = 0, debug_flags: int = 0,
+                       stream=None):
+    """Gumbel-top-k of the fused path: per row of H [B, D], the k largest perturbed scores of
+    lmhead_sample's race (k draws without replacement), larger first, then the smaller index.
+    Returns (indices int64 [B, k], -1 past a row's finite scores; scores fp32 [B, k] or None)."""
+    if H.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise TypeError("H and W must be bfloat16")
+    if not H.is_cuda or W.device != H.device:
+        raise ValueError("H and W must be on the same CUDA device")
+    if H.dim() != 2 or W.dim() != 2 or H.shape[1] != W.shape[1]:
+        raise ValueError("H must be [B, D] and W [V, D]")
+    if H.stride(1) != 1 or W.stride(1) != 1:
+        raise ValueError("H and W must be row-major with unit inner stride")
+    B, D = H.shape
+    V = W.shape[0]
+    dev = H.device
+    p = _params(B, dev, temperature, seeds, positions, bias, mask, base_seed, offset, wide, 0,
+                PATH_AUTO, row_status, timeout_ms, debug_flags)
+    if out is None:
+        out = torch.empty(B, k, dtype=torch.int64, device=dev)
+    if scores is None and want_scores:
+        scores = torch.empty(B, k, dtype=torch.float32, device=dev)
+    if workspace is None:
+        need = lib().lms_workspace_bytes_topk(B, V, k)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _check(lib().lms_lmhead_sample_topk(_ptr(H), H.stride(0), _ptr(W), W.stride(0), B, D, V, k,
+                                        ctypes.byref(p), _ptr(out),
+                                        _ptr(scores) if scores is not None else None, _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out, scores
 
 
 def lmhead_sample_fp8(H: torch.Tensor, W8: torch.Tensor, w_scale: torch.Tensor, *, temperature=None,

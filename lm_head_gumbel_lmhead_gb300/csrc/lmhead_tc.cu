@@ -68,7 +68,7 @@ struct SmemLayout {
     }
 };
 
-template <int kEpiWarps, bool kWide, bool kFp8>
+template <int kEpiWarps, bool kWide, bool kFp8, bool kTopK>
 __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     lmhead_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
                      const TcParams prm) {
@@ -224,28 +224,41 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
                 // Poison this tile's candidates (and, through the loop, every later one).
                 if (epi_tid == 0) *err = 1;
                 for (int b = epi_tid; b < B; b += epi_threads) {
-                    a.cand_score[b * nt + tile] = -CUDART_INF_F;
-                    a.cand_index[b * nt + tile] = kPoisonIndex;
+                    if constexpr (kTopK) {
+                        for (int r = 0; r < a.topk; ++r) a.cand_keys[(b * nt + tile) * a.topk + r] = kPoisonKey;
+                    } else {
+                        a.cand_score[b * nt + tile] = -CUDART_INF_F;
+                        a.cand_index[b * nt + tile] = kPoisonIndex;
+                    }
                 }
                 continue;
             }
             tc_fence_after_sync();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) +
                                    static_cast<uint32_t>(ab * n_pad);
-            epilogue_tile_columns<kEpiWarps, kWide>(a, rows, red, tr, t_row, tile, quad, col_group, lane, B);
+            if constexpr (kTopK) {
+                const uint8_t* tr_group = base + L.tr_off + 4 * col_group * kTrWarpBytes;
+                epilogue_tile_topk<kEpiWarps, kWide>(a, rows, tr, tr_group, t_row, tile, quad, col_group,
+                                                     ((warp - 2) & 3) == 0, lane, B);
+            } else {
+                epilogue_tile_columns<kEpiWarps, kWide>(a, rows, red, tr, t_row, tile, quad, col_group,
+                                                        lane, B);
+            }
             // The accumulator buffer is free for the MMA of tile i+2.
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(ab));
-            epi_barrier(epi_threads);
-            for (int b = epi_tid; b < B; b += epi_threads) {
-                const unsigned long long key = red[b];
-                red[b] = 0ull;                       // ready for the next tile
-                const float s = unpack_score(key);
-                a.cand_score[b * nt + tile] = s;
-                a.cand_index[b * nt + tile] = candidate_index(s, unpack_index(key));
+            if constexpr (!kTopK) {
+                epi_barrier(epi_threads);
+                for (int b = epi_tid; b < B; b += epi_threads) {
+                    const unsigned long long key = red[b];
+                    red[b] = 0ull;                       // ready for the next tile
+                    const float s = unpack_score(key);
+                    a.cand_score[b * nt + tile] = s;
+                    a.cand_index[b * nt + tile] = candidate_index(s, unpack_index(key));
+                }
+                epi_barrier(epi_threads);
             }
-            epi_barrier(epi_threads);
         }
     }
 
@@ -259,10 +272,10 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     }
 }
 
-template <int kEpiWarps, bool kWide, bool kFp8>
+template <int kEpiWarps, bool kWide, bool kFp8, bool kTopK = false>
 cudaError_t launch_variant(const CUtensorMap& tmW, const CUtensorMap& tmH, const TcParams& prm,
                            size_t smem, int grid, cudaStream_t stream) {
-    auto kern = lmhead_tc_kernel<kEpiWarps, kWide, kFp8>;
+    auto kern = lmhead_tc_kernel<kEpiWarps, kWide, kFp8, kTopK>;
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     if (!kFp8) {
@@ -310,6 +323,11 @@ cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int
     const size_t smem = L.total + 1024;
     int sms = device_sm_count();
     int grid = static_cast<int>(a.n_tiles < sms ? a.n_tiles : sms);
+    if (a.topk > 0) {
+        if (fp8 || a.topk > kMaxTopK || a.cand_keys == nullptr) return cudaErrorInvalidValue;
+        return wide ? launch_variant<kEpilogueWarps, true, false, true>(tmW, tmH, prm, smem, grid, stream)
+                    : launch_variant<kEpilogueWarps, false, false, true>(tmW, tmH, prm, smem, grid, stream);
+    }
     if (fp8)
         return wide ? launch_variant<kEpilogueWarps, true, true>(tmW, tmH, prm, smem, grid, stream)
                     : launch_variant<kEpilogueWarps, false, true>(tmW, tmH, prm, smem, grid, stream);

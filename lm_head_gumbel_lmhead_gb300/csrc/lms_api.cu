@@ -293,6 +293,64 @@ lms_status lms_lmhead_sample(const void* H, int64_t ldh, const void* W, int64_t 
     return LMS_OK;
 }
 
+size_t lms_workspace_bytes_topk(int64_t B, int64_t V, int32_t k) {
+    if (B <= 0 || V <= 0 || V > kMaxV || k < 1 || k > LMS_TOPK_MAX) return 0;
+    const int64_t nt = (V + LMS_FUSED_TILE_V - 1) / LMS_FUSED_TILE_V;
+    return round_up(static_cast<size_t>(B) * static_cast<size_t>(nt) * static_cast<size_t>(k) * 8, 256);
+}
+
+lms_status lms_lmhead_sample_topk(const void* H, int64_t ldh, const void* W, int64_t ldw, int64_t B,
+                                  int64_t D, int64_t V, int32_t k, const lms_sample_params* params,
+                                  int64_t* out, float* scores, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    g_last_error[0] = '\0';
+    if (H == nullptr || W == nullptr || out == nullptr)
+        return fail(LMS_ERR_INVALID_ARG, "H, W and out are required");
+    if (k < 1 || k > LMS_TOPK_MAX) return fail(LMS_ERR_INVALID_ARG, "k must be in [1, %d] (k=%d)", LMS_TOPK_MAX, k);
+    Tiling t;
+    lms_status st = make_tiling(LMS_OP_LMHEAD, B, D, V, params ? params->tile_v : 0, &t);
+    if (st != LMS_OK) return st;
+    if ((st = check_params(params, V)) != LMS_OK) return st;
+    if (D % 8 != 0) return fail(LMS_ERR_UNSUPPORTED, "D must be a multiple of 8 (D=%lld)", (long long)D);
+    if (D > 65536) return fail(LMS_ERR_UNSUPPORTED, "D must be <= 65536");
+    if (ldh < D || ldw < D || ldh % 8 != 0 || ldw % 8 != 0)
+        return fail(LMS_ERR_UNSUPPORTED, "ldh/ldw must be >= D and multiples of 8 elements");
+    if (reinterpret_cast<uintptr_t>(H) % 16 != 0 || reinterpret_cast<uintptr_t>(W) % 16 != 0)
+        return fail(LMS_ERR_UNSUPPORTED, "H and W must be 16-byte aligned");
+    if (params->path != LMS_PATH_AUTO && params->path != LMS_PATH_TCGEN05)
+        return fail(LMS_ERR_UNSUPPORTED, "Gumbel-top-k runs on the tcgen05 kernel only");
+    const size_t need = lms_workspace_bytes_topk(B, V, k);
+    if (workspace == nullptr || workspace_bytes < need)
+        return fail(LMS_ERR_WORKSPACE, "workspace of %zu bytes needed", need);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool wide = params->noise_mode == LMS_NOISE_WIDE53;
+    lms::SampleArgs a = make_args(params, B, V, t, workspace);
+    a.cand_score = nullptr;
+    a.cand_index = nullptr;
+    a.cand_keys = static_cast<unsigned long long*>(workspace);
+    a.topk = k;
+    CUtensorMap tmW;
+    if ((st = encode_bf16_map(&tmW, W, V, D, ldw, 128)) != LMS_OK) return st;
+    const uint32_t timeout_ms = params->timeout_ms ? params->timeout_ms : 2000u;
+    for (int64_t r0 = 0; r0 < B; r0 += kTcMaxBatchPerLaunch) {
+        const int64_t nb = (B - r0 < kTcMaxBatchPerLaunch) ? B - r0 : kTcMaxBatchPerLaunch;
+        const int n_pad = static_cast<int>(nb < 16 ? 16 : (nb + 15) / 16 * 16);
+        CUtensorMap tmH;
+        if ((st = encode_bf16_map(&tmH, H, B, D, ldh, n_pad)) != LMS_OK) return st;
+        lms::SampleArgs ac = a;
+        ac.B = nb;
+        ac.row0 = r0;
+        ac.cand_keys = a.cand_keys + r0 * t.n_tiles * k;
+        const cudaError_t e = lms::launch_lmhead_tc(tmW, tmH, D, n_pad, wide, timeout_ms,
+                                                    params->debug_flags, ac, s);
+        if (e != cudaSuccess) return cuda_fail(e, "tcgen05 top-k Stage-1 launch");
+    }
+    const cudaError_t e = lms::launch_stage2_topk(a.cand_keys, t.n_tiles, k, B, params->temperature,
+                                                  out, scores, params->row_status, s);
+    if (e != cudaSuccess) return cuda_fail(e, "top-k Stage-2 launch");
+    return LMS_OK;
+}
+
 lms_status lms_lmhead_sample_fp8(const void* H, int64_t ldh, const void* W8, int64_t ldw8,
                                  const float* w_scale, int64_t B, int64_t D, int64_t V,
                                  const lms_sample_params* params, int64_t* out, void* workspace,

@@ -27,9 +27,12 @@ struct SampleArgs {
     // FP8 (W8A8) fused path only, else null: logits = acc * 2^h_exp[row] * w_scale[v]
     const int32_t* h_exp;
     const float* w_scale;
+    // Gumbel-top-k (topk > 0) only: [B][n_tiles][topk] ordered (score, index) keys per tile
+    unsigned long long* cand_keys = nullptr;
+    int topk = 0;
 };
 
-// The filtered race (one CTA per row; writes tokens and statuses directly).
+// The filtered race (a cluster per row; writes tokens and statuses directly).
 struct FilterArgs {
     SampleArgs a;
     const int32_t* top_k;
@@ -57,6 +60,12 @@ cudaError_t launch_stage2(const float* cand_score, const int* cand_index, int64_
                           int64_t B, const float* temperature, int64_t* out, int32_t* row_status,
                           cudaStream_t stream);
 
+// Stage 2 of Gumbel-top-k: per row, the k best of the tiles' ordered key lists
+// (cand_keys [B][n_tiles][k]); out [B][k] indices (-1 past the finite ones), scores [B][k] or null.
+cudaError_t launch_stage2_topk(const unsigned long long* cand_keys, int64_t n_tiles, int k, int64_t B,
+                               const float* temperature, int64_t* out, float* scores,
+                               int32_t* row_status, cudaStream_t stream);
+
 cudaError_t launch_lmhead_gemv(const uint16_t* H, int64_t ldh, const uint16_t* W, int64_t ldw,
                                int64_t D, bool wide, const SampleArgs& a, cudaStream_t stream);
 
@@ -66,6 +75,7 @@ cudaError_t launch_lmhead_gemv(const uint16_t* H, int64_t ldh, const uint16_t* W
 cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int64_t D, int n_pad,
                              bool wide, uint32_t timeout_ms, uint32_t debug_flags,
                              const SampleArgs& a, cudaStream_t stream, bool fp8 = false);
+// (a.topk > 0 selects the Gumbel-top-k epilogue: bf16 only.)
 
 // The CTA-pair tcgen05 path (cta_group::2, M = 256): tmH boxes are 64 x (n_pad / 2).
 cudaError_t launch_lmhead_tc_pair(const CUtensorMap& tmW, const CUtensorMap& tmH, int64_t D,

@@ -3,6 +3,7 @@
 // smaller index, which is the earlier tile.  Also writes the per-row status.
 #include "lms_device.cuh"
 #include "lms_kernels.h"
+#include "tcgen05_common.cuh"
 
 namespace lms {
 namespace {
@@ -59,7 +60,100 @@ __global__ void __launch_bounds__(kStage2Threads) stage2_kernel(
     }
 }
 
+// Stage 2 of Gumbel-top-k: row b's candidates are n_tiles ordered lists of k keys (larger score,
+// then smaller index first; key 0 and the keys of -inf scores are below every finite one).  Each
+// thread folds the lists of tiles tid, tid + 512, ... into its own ordered k best: a tile's k keys
+// are loaded together, then inserted in order until one is not above the thread's current k-th.
+// The 512 lists are then merged pairwise in 9 rounds.  The merged list's first k keys are the
+// row's k best: every one of them is among the k best of its own tile.  Launched in stream order,
+// not as a programmatic dependent: its resident, waiting CTAs slowed the top-k Stage 1 (measured).
+constexpr int kTopKThreads = 512;
+
+__global__ void __launch_bounds__(kTopKThreads) stage2_topk_kernel(
+    const unsigned long long* __restrict__ cand_keys, int64_t n_tiles, int k,
+    const float* __restrict__ temperature, int64_t* __restrict__ out, float* __restrict__ scores,
+    int32_t* __restrict__ row_status) {
+    // lst[r * kTopKThreads + t]: rank r of thread t's list (thread-minor, so that the threads of
+    // a warp touch distinct banks)
+    extern __shared__ unsigned long long lst[];
+    const int tid = threadIdx.x;
+    const int64_t b = blockIdx.x;
+    const unsigned long long* keys = cand_keys + b * n_tiles * k;
+    unsigned long long* mine = lst + tid;
+    auto at = [&](unsigned long long* l, int r) -> unsigned long long& { return l[r * kTopKThreads]; };
+    for (int r = 0; r < k; ++r) at(mine, r) = 0ull;
+    for (int64_t t = tid; t < n_tiles; t += kTopKThreads) {
+        const unsigned long long* tl = keys + t * k;
+        unsigned long long v[tc::kMaxTopK];
+#pragma unroll
+        for (int r = 0; r < tc::kMaxTopK; ++r) v[r] = r < k ? __ldg(tl + r) : 0ull;
+#pragma unroll
+        for (int r = 0; r < tc::kMaxTopK; ++r) {
+            if (r >= k || v[r] <= at(mine, k - 1)) break;     // the tile's list is ordered
+            int j = k - 1;
+            while (j > 0 && at(mine, j - 1) < v[r]) { at(mine, j) = at(mine, j - 1); --j; }
+            at(mine, j) = v[r];
+        }
+    }
+    __syncthreads();
+    for (int stride = 1; stride < kTopKThreads; stride <<= 1) {
+        const bool merging = (tid & (2 * stride - 1)) == 0;
+        unsigned long long m[tc::kMaxTopK];
+        if (merging) {
+            unsigned long long* x = lst + tid;
+            unsigned long long* y = lst + tid + stride;
+            int i = 0, j = 0;
+#pragma unroll
+            for (int r = 0; r < tc::kMaxTopK; ++r) {
+                if (r < k) {
+                    const unsigned long long xv = i < k ? at(x, i) : 0ull, yv = j < k ? at(y, j) : 0ull;
+                    if (xv >= yv) { m[r] = xv; ++i; } else { m[r] = yv; ++j; }
+                }
+            }
+        }
+        __syncthreads();
+        if (merging) {
+#pragma unroll
+            for (int r = 0; r < tc::kMaxTopK; ++r)
+                if (r < k) at(mine, r) = m[r];
+        }
+        __syncthreads();
+    }
+    if (tid == 0) {
+        const float T = temperature ? temperature[b] : 1.0f;
+        const bool poisoned = at(lst, 0) == tc::kPoisonKey;
+        const bool invalid = !(T >= 0.0f);
+        int found = 0;
+        for (int r = 0; r < k; ++r) {
+            const unsigned long long key = at(lst, r);
+            float s = -CUDART_INF_F;
+            int64_t idx = -1;
+            if (!poisoned && !invalid && key != 0ull) {
+                s = tc::unpack_score(key);
+                idx = candidate_index(s, tc::unpack_index(key));
+                if (idx < 0) s = -CUDART_INF_F;
+            }
+            found += idx >= 0;
+            out[b * k + r] = idx;
+            if (scores) scores[b * k + r] = s;
+        }
+        if (row_status) row_status[b] = poisoned ? 3 : invalid ? 2 : (found > 0 ? 0 : 1);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_stage2_topk(const unsigned long long* cand_keys, int64_t n_tiles, int k, int64_t B,
+                               const float* temperature, int64_t* out, float* scores,
+                               int32_t* row_status, cudaStream_t stream) {
+    if (k < 1 || k > tc::kMaxTopK) return cudaErrorInvalidValue;
+    const size_t smem = static_cast<size_t>(kTopKThreads) * k * sizeof(unsigned long long);
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(stage2_topk_kernel), smem);
+    if (e != cudaSuccess) return e;
+    stage2_topk_kernel<<<static_cast<unsigned>(B), kTopKThreads, smem, stream>>>(
+        cand_keys, n_tiles, k, temperature, out, scores, row_status);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_stage2(const float* cand_score, const int* cand_index, int64_t n_tiles,
                           int64_t B, const float* temperature, int64_t* out, int32_t* row_status,
