@@ -55,8 +55,10 @@ struct TcParams {
 // Shared-memory layout (offsets from a 1024-byte aligned base)
 // ------------------------------------------------------------------------------------------
 struct SmemLayout {
-    uint32_t stages_off, bars_off, misc_off, rows_off, red_off, tr_off, total;
-    __host__ __device__ SmemLayout(int stages, uint32_t stage_bytes, int n_pad, int epi_warps) {
+    uint32_t stages_off, bars_off, misc_off, rows_off, red_off, tr_off, run_off, total;
+    // topk > 0: per TMEM quadrant and batch column, the top-k threshold key (Gumbel-top-k only)
+    __host__ __device__ SmemLayout(int stages, uint32_t stage_bytes, int n_pad, int epi_warps,
+                                   int topk = 0) {
         stages_off = 0;
         bars_off = stages * stage_bytes;
         // full[S], empty[S], acc_full[2], acc_empty[2], drain
@@ -64,7 +66,8 @@ struct SmemLayout {
         rows_off = (misc_off + 16 + 15) & ~15u;   // misc: tmem slot, error flag
         red_off = rows_off + n_pad * static_cast<uint32_t>(sizeof(RowParams));
         tr_off = red_off + n_pad * 8;
-        total = tr_off + epi_warps * kTrWarpBytes;
+        run_off = tr_off + epi_warps * kTrWarpBytes;
+        total = run_off + (topk > 0 ? static_cast<uint32_t>(4 * n_pad) * 8u : 0u);
     }
 };
 
@@ -76,7 +79,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
     uint8_t* base = smem_raw + (base_addr - raw_addr);
-    const SmemLayout L(prm.stages, prm.stage_bytes, prm.n_pad, kEpiWarps);
+    const SmemLayout L(prm.stages, prm.stage_bytes, prm.n_pad, kEpiWarps, kTopK ? prm.a.topk : 0);
 
     const SampleArgs& a = prm.a;
     const int S = prm.stages;
@@ -119,6 +122,10 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
         rows[b] = make_row_params(a.temperature, a.seeds, a.positions, a.base_seed, a.offset,
                                   a.row0 + b);
         red[b] = 0ull;
+    }
+    if constexpr (kTopK) {
+        unsigned long long* run = reinterpret_cast<unsigned long long*>(base + L.run_off);
+        for (int i = threadIdx.x; i < 4 * n_pad; i += blockDim.x) run[i] = 0ull;
     }
     if (warp == 1) tmem_alloc(base_addr + L.misc_off, prm.tmem_cols);
     tc_fence_before_sync();
@@ -225,7 +232,8 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
                 if (epi_tid == 0) *err = 1;
                 for (int b = epi_tid; b < B; b += epi_threads) {
                     if constexpr (kTopK) {
-                        for (int r = 0; r < a.topk; ++r) a.cand_keys[(b * nt + tile) * a.topk + r] = kPoisonKey;
+                        for (int r = 0; r < 4 * a.topk; ++r)
+                            a.cand_keys[(b * nt + tile) * 4 * a.topk + r] = kPoisonKey;
                     } else {
                         a.cand_score[b * nt + tile] = -CUDART_INF_F;
                         a.cand_index[b * nt + tile] = kPoisonIndex;
@@ -237,9 +245,9 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) +
                                    static_cast<uint32_t>(ab * n_pad);
             if constexpr (kTopK) {
-                const uint8_t* tr_group = base + L.tr_off + 4 * col_group * kTrWarpBytes;
-                epilogue_tile_topk<kEpiWarps, kWide>(a, rows, tr, tr_group, t_row, tile, quad, col_group,
-                                                     ((warp - 2) & 3) == 0, lane, B);
+                unsigned long long* thr = reinterpret_cast<unsigned long long*>(base + L.run_off);
+                epilogue_tile_topk<kEpiWarps, kWide>(a, rows, tr, thr, n_pad, t_row, tile, quad,
+                                                     col_group, lane, B);
             } else {
                 epilogue_tile_columns<kEpiWarps, kWide>(a, rows, red, tr, t_row, tile, quad, col_group,
                                                         lane, B);
@@ -309,7 +317,7 @@ cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int
     prm.n_pad = n_pad;
     prm.stage_bytes = static_cast<uint32_t>(kWStageBytes + n_pad * kBK * 2);
     const uint32_t budget = 227u * 1024u - 1024u;   // opt-in maximum minus alignment slack
-    const SmemLayout fixed(0, prm.stage_bytes, n_pad, kEpilogueWarps);
+    const SmemLayout fixed(0, prm.stage_bytes, n_pad, kEpilogueWarps, a.topk);
     int stages = static_cast<int>((budget - fixed.total - (2 * kMaxStages + 5) * 8) / prm.stage_bytes);
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return cudaErrorInvalidValue;
@@ -319,7 +327,7 @@ cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int
     prm.tmem_cols = cols;
     prm.timeout_ns = static_cast<uint64_t>(timeout_ms) * 1000000ull;
     prm.debug_flags = debug_flags;
-    const SmemLayout L(stages, prm.stage_bytes, n_pad, kEpilogueWarps);
+    const SmemLayout L(stages, prm.stage_bytes, n_pad, kEpilogueWarps, a.topk);
     const size_t smem = L.total + 1024;
     int sms = device_sm_count();
     int grid = static_cast<int>(a.n_tiles < sms ? a.n_tiles : sms);

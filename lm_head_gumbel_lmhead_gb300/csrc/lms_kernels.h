@@ -27,7 +27,8 @@ struct SampleArgs {
     // FP8 (W8A8) fused path only, else null: logits = acc * 2^h_exp[row] * w_scale[v]
     const int32_t* h_exp;
     const float* w_scale;
-    // Gumbel-top-k (topk > 0) only: [B][n_tiles][topk] ordered (score, index) keys per tile
+    // Gumbel-top-k (topk > 0) only: [B][n_tiles][4][topk] ordered (score, index) keys per tile
+    // and TMEM quadrant
     unsigned long long* cand_keys = nullptr;
     int topk = 0;
 };
@@ -60,9 +61,9 @@ cudaError_t launch_stage2(const float* cand_score, const int* cand_index, int64_
                           int64_t B, const float* temperature, int64_t* out, int32_t* row_status,
                           cudaStream_t stream);
 
-// Stage 2 of Gumbel-top-k: per row, the k best of the tiles' ordered key lists
-// (cand_keys [B][n_tiles][k]); out [B][k] indices (-1 past the finite ones), scores [B][k] or null.
-cudaError_t launch_stage2_topk(const unsigned long long* cand_keys, int64_t n_tiles, int k, int64_t B,
+// Stage 2 of Gumbel-top-k: per row, the k best of n_lists ordered key lists of k keys
+// (cand_keys [B][n_lists][k]); out [B][k] indices (-1 past the finite ones), scores [B][k] or null.
+cudaError_t launch_stage2_topk(const unsigned long long* cand_keys, int64_t n_lists, int k, int64_t B,
                                const float* temperature, int64_t* out, float* scores,
                                int32_t* row_status, cudaStream_t stream);
 

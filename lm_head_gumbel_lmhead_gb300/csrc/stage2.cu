@@ -60,17 +60,18 @@ __global__ void __launch_bounds__(kStage2Threads) stage2_kernel(
     }
 }
 
-// Stage 2 of Gumbel-top-k: row b's candidates are n_tiles ordered lists of k keys (larger score,
+// Stage 2 of Gumbel-top-k: row b's candidates are n_lists ordered lists of k keys (larger score,
 // then smaller index first; key 0 and the keys of -inf scores are below every finite one).  Each
-// thread folds the lists of tiles tid, tid + 512, ... into its own ordered k best: a tile's k keys
-// are loaded together, then inserted in order until one is not above the thread's current k-th.
+// thread folds lists tid, tid + 512, ... into its own ordered k best, inserting a list's keys in
+// order until one is not above the thread's current k-th (a list shorter than k ends with key 0).
 // The 512 lists are then merged pairwise in 9 rounds.  The merged list's first k keys are the
-// row's k best: every one of them is among the k best of its own tile.  Launched in stream order,
+// row's k best, since the lists hold every one of them (Stage 1's selection guarantees it).  Launched in stream order,
 // not as a programmatic dependent: its resident, waiting CTAs slowed the top-k Stage 1 (measured).
 constexpr int kTopKThreads = 512;
 
+template <int kM>
 __global__ void __launch_bounds__(kTopKThreads) stage2_topk_kernel(
-    const unsigned long long* __restrict__ cand_keys, int64_t n_tiles, int k,
+    const unsigned long long* __restrict__ cand_keys, int64_t n_lists, int k,
     const float* __restrict__ temperature, int64_t* __restrict__ out, float* __restrict__ scores,
     int32_t* __restrict__ row_status) {
     // lst[r * kTopKThreads + t]: rank r of thread t's list (thread-minor, so that the threads of
@@ -78,33 +79,73 @@ __global__ void __launch_bounds__(kTopKThreads) stage2_topk_kernel(
     extern __shared__ unsigned long long lst[];
     const int tid = threadIdx.x;
     const int64_t b = blockIdx.x;
-    const unsigned long long* keys = cand_keys + b * n_tiles * k;
+    const unsigned long long* keys = cand_keys + b * n_lists * k;
     unsigned long long* mine = lst + tid;
     auto at = [&](unsigned long long* l, int r) -> unsigned long long& { return l[r * kTopKThreads]; };
-    for (int r = 0; r < k; ++r) at(mine, r) = 0ull;
-    for (int64_t t = tid; t < n_tiles; t += kTopKThreads) {
-        const unsigned long long* tl = keys + t * k;
-        unsigned long long v[tc::kMaxTopK];
+    // This thread's best kM >= k keys, ordered, in registers (the first k are used); insertion
+    // is a branch-free pass over the kM slots, so no slot is indexed at run time.
+    unsigned long long best[kM];
 #pragma unroll
-        for (int r = 0; r < tc::kMaxTopK; ++r) v[r] = r < k ? __ldg(tl + r) : 0ull;
+    for (int i = 0; i < kM; ++i) best[i] = 0ull;
+    // First keys of 4 lists at a time are loaded together; a list is read further only when its
+    // first key beats this thread's current k-th (most lists of a warmed-up Stage 1 are empty).
+    unsigned long long kth = 0ull;
+    constexpr int kBatch = 4;
+    for (int64_t base = tid; base < n_lists; base += static_cast<int64_t>(kBatch) * kTopKThreads) {
+        unsigned long long first[kBatch];
 #pragma unroll
-        for (int r = 0; r < tc::kMaxTopK; ++r) {
-            if (r >= k || v[r] <= at(mine, k - 1)) break;     // the tile's list is ordered
-            int j = k - 1;
-            while (j > 0 && at(mine, j - 1) < v[r]) { at(mine, j) = at(mine, j - 1); --j; }
-            at(mine, j) = v[r];
+        for (int j = 0; j < kBatch; ++j) {
+            const int64_t t = base + static_cast<int64_t>(j) * kTopKThreads;
+            first[j] = t < n_lists ? __ldg(keys + t * k) : 0ull;
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            if (first[j] <= kth) continue;
+            // the list's k slots are loaded together (one latency); a shorter list ends with a key
+            // 0, and the stale slots after it (left by an earlier call) are zeroed before use
+            const unsigned long long* tl = keys + (base + static_cast<int64_t>(j) * kTopKThreads) * k;
+            // keys in groups of 4 loaded together; the list is ordered and ends with a key 0, so
+            // the first key not above kth ends it
+            for (int r0 = 0; r0 < k; r0 += 4) {
+                unsigned long long q[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int r = r0 + u;
+                    q[u] = r == 0 ? first[j] : (r < k ? __ldg(tl + r) : 0ull);
+                }
+                bool stop = false;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    stop = stop || !(q[u] > kth);
+                    const unsigned long long x = stop ? 0ull : q[u];     // 0 changes nothing
+#pragma unroll
+                    for (int i = kM - 1; i > 0; --i)                     // past the kM-th: dropped
+                        best[i] = x > best[i - 1] ? best[i - 1] : (x > best[i] ? x : best[i]);
+                    best[0] = x > best[0] ? x : best[0];
+                }
+                if (stop) break;
+            }
+            // the k-th key, as the least of the first k (the list is ordered); written as a min so
+            // that it is not folded into a run-time index of best[]
+            unsigned long long t = ~0ull;
+#pragma unroll
+            for (int i = 0; i < kM; ++i) t = (i < k && best[i] < t) ? best[i] : t;
+            kth = t;
         }
     }
+#pragma unroll
+    for (int r = 0; r < kM; ++r)
+        if (r < k) lst[r * kTopKThreads + tid] = best[r];
     __syncthreads();
     for (int stride = 1; stride < kTopKThreads; stride <<= 1) {
         const bool merging = (tid & (2 * stride - 1)) == 0;
-        unsigned long long m[tc::kMaxTopK];
+        unsigned long long m[kM];
         if (merging) {
             unsigned long long* x = lst + tid;
             unsigned long long* y = lst + tid + stride;
             int i = 0, j = 0;
 #pragma unroll
-            for (int r = 0; r < tc::kMaxTopK; ++r) {
+            for (int r = 0; r < kM; ++r) {
                 if (r < k) {
                     const unsigned long long xv = i < k ? at(x, i) : 0ull, yv = j < k ? at(y, j) : 0ull;
                     if (xv >= yv) { m[r] = xv; ++i; } else { m[r] = yv; ++j; }
@@ -114,7 +155,7 @@ __global__ void __launch_bounds__(kTopKThreads) stage2_topk_kernel(
         __syncthreads();
         if (merging) {
 #pragma unroll
-            for (int r = 0; r < tc::kMaxTopK; ++r)
+            for (int r = 0; r < kM; ++r)
                 if (r < k) at(mine, r) = m[r];
         }
         __syncthreads();
@@ -143,15 +184,23 @@ __global__ void __launch_bounds__(kTopKThreads) stage2_topk_kernel(
 
 }  // namespace
 
-cudaError_t launch_stage2_topk(const unsigned long long* cand_keys, int64_t n_tiles, int k, int64_t B,
+cudaError_t launch_stage2_topk(const unsigned long long* cand_keys, int64_t n_lists, int k, int64_t B,
                                const float* temperature, int64_t* out, float* scores,
                                int32_t* row_status, cudaStream_t stream) {
     if (k < 1 || k > tc::kMaxTopK) return cudaErrorInvalidValue;
     const size_t smem = static_cast<size_t>(kTopKThreads) * k * sizeof(unsigned long long);
-    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(stage2_topk_kernel), smem);
-    if (e != cudaSuccess) return e;
-    stage2_topk_kernel<<<static_cast<unsigned>(B), kTopKThreads, smem, stream>>>(
-        cand_keys, n_tiles, k, temperature, out, scores, row_status);
+    for (const void* f : {reinterpret_cast<const void*>(stage2_topk_kernel<1>),
+                          reinterpret_cast<const void*>(stage2_topk_kernel<2>),
+                          reinterpret_cast<const void*>(stage2_topk_kernel<4>),
+                          reinterpret_cast<const void*>(stage2_topk_kernel<8>),
+                          reinterpret_cast<const void*>(stage2_topk_kernel<16>)}) {
+        const cudaError_t e = ensure_dynamic_smem(f, smem);
+        if (e != cudaSuccess) return e;
+    }
+    auto kern = k <= 1 ? stage2_topk_kernel<1> : k <= 2 ? stage2_topk_kernel<2>
+              : k <= 4 ? stage2_topk_kernel<4> : k <= 8 ? stage2_topk_kernel<8> : stage2_topk_kernel<16>;
+    kern<<<static_cast<unsigned>(B), kTopKThreads, smem, stream>>>(cand_keys, n_lists, k, temperature,
+                                                                    out, scores, row_status);
     return cudaGetLastError();
 }
 

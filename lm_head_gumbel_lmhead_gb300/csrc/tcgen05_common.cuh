@@ -295,34 +295,27 @@ constexpr int kMaxTopK = 16;
 // Written in place of a tile's keys when a bounded wait ran out; above every real key (a real
 // key's high half is at most the order key of +inf, 0xff800000).
 constexpr unsigned long long kPoisonKey = ~0ull;
-static_assert(8 * kMaxTopK * 8 <= static_cast<int>(kTrWarpBytes), "a warp's lists fit its transpose tile");
 
-// bar.sync over the 4 epilogue warps that share a column group (ids 2..5; 0 is __syncthreads
-// and 1 the whole epilogue's barrier).
-__device__ __forceinline__ void group_barrier(int col_group) {
-    asm volatile("bar.sync %0, 128;" ::"r"(2 + col_group) : "memory");
-}
-
-// One tile's Gumbel-top-k epilogue.  Scores as in epilogue_tile_columns; then, per column, the 4
-// threads holding its 32 rows (this warp's TMEM quadrant) extract their k best entries by k
-// rounds of shuffle-argmax with removal, and write them, in order, to the warp's transpose tile
-// (free once the chunk is read).  After a barrier of the column group's 4 warps (one per
-// quadrant), the group's first warp merges the 4 ordered lists of each column into the tile's k
-// best keys, written to a.cand_keys[(b * n_tiles + tile) * k + r].  `tr_group` is the transpose
-// tile of the group's first warp; the 4 warps' tiles are consecutive.
+// One tile's Gumbel-top-k epilogue.  Scores as in epilogue_tile_columns, then as ordered 64-bit
+// keys (0 for -inf).  Per column, the 4 threads holding its 32 rows (this warp's TMEM quadrant)
+// extract their best keys by rounds of shuffle-max with removal, at most k, and the warp writes
+// that ordered list to a.cand_keys[((b * n_tiles + tile) * 4 + quad) * k + r], ended by a key 0
+// when shorter than k (the slots after it are not written).
+// thr[quad * n_pad + b] holds the k-th key of this warp's last full list for column b: k keys of
+// the row lie above it, so entries not above it cannot be among the row's k best and are dropped
+// before the rounds, which stop once no column of the warp has a key left.  Every key among the
+// row's k best therefore reaches some list; Stage 2 merges them.  No step crosses warps.
 template <int kEpiWarps, bool kWide>
 __device__ __forceinline__ void epilogue_tile_topk(const SampleArgs& a, const RowParams* rows,
-                                                   float* tr, const uint8_t* tr_group,
+                                                   float* tr, unsigned long long* thr, int n_pad,
                                                    uint32_t t_row, int64_t tile, int quad,
-                                                   int col_group, bool group_lead, int lane,
-                                                   int B) {
+                                                   int col_group, int lane, int B) {
     constexpr int kColGroups = kEpiWarps / 4;
     const int k = a.topk;
     const int n_chunks = (B + 7) / 8;
     const int my_col = lane & 7;
     const int my_r0 = (lane >> 3) * 8;
     const int64_t v0 = tile * kTileV + 32 * quad + my_r0;   // a multiple of 8
-    unsigned long long* lst = reinterpret_cast<unsigned long long*>(tr);
     for (int cc = col_group; cc < n_chunks; cc += kColGroups) {
         uint32_t acc[8];
         tmem_load_8(t_row + 8u * cc, acc);
@@ -336,9 +329,11 @@ __device__ __forceinline__ void epilogue_tile_topk(const SampleArgs& a, const Ro
         y[0] = y0.x; y[1] = y0.y; y[2] = y0.z; y[3] = y0.w;
         y[4] = y1.x; y[5] = y1.y; y[6] = y1.z; y[7] = y1.w;
         const int b = cc * 8 + my_col;
-        float sc[8];
+        unsigned long long* th = thr + quad * n_pad + (b < B ? b : 0);
+        const unsigned long long theta = b < B ? *th : 0ull;
+        unsigned long long ky[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) sc[e] = -CUDART_INF_F;
+        for (int e = 0; e < 8; ++e) ky[e] = 0ull;
         if (b < B && v0 < a.V) {
             const RowParams p = rows[b];
             if (!(p.flags & kRowInvalid)) {
@@ -358,57 +353,40 @@ __device__ __forceinline__ void epilogue_tile_topk(const SampleArgs& a, const Ro
                     const int64_t v = v0 + e;
                     if (v < a.V) {
                         const float bias = brow ? __ldg(brow + v) : 0.0f;
-                        sc[e] = perturb(p, y[e], bias, (mword >> e) & 1u, g[e]);
+                        const float sc = perturb(p, y[e], bias, (mword >> e) & 1u, g[e]);
+                        const unsigned long long key = pack_candidate(sc, static_cast<int>(v));
+                        ky[e] = (sc > -CUDART_INF_F && key > theta) ? key : 0ull;
                     }
                 }
             }
         }
-        // k rounds: the best entry not yet taken among the column's 32 rows; its owner drops it
-        uint32_t taken = 0u;
-        for (int r = 0; r < k; ++r) {
-            float bs = -CUDART_INF_F;
-            int bi = kNoIndex, be = -1;
+        unsigned long long* out =
+            a.cand_keys + ((static_cast<int64_t>(b < B ? b : 0) * a.n_tiles + tile) * 4 + quad) * k;
+        // rounds: the column's best remaining key; its owner drops it
+        int r = 0;
+        unsigned long long last = 0ull;
+        for (; r < k; ++r) {
+            unsigned long long bk = 0ull;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                // strict '>': -inf is never taken, and ties keep the smaller index (larger e later)
-                if (!((taken >> e) & 1u) && sc[e] > bs) { bs = sc[e]; bi = static_cast<int>(v0) + e; be = e; }
-            }
-            float ws = bs;
-            int wi = bi;
+            for (int e = 0; e < 8; ++e) bk = ky[e] > bk ? ky[e] : bk;
+            unsigned long long wk = bk;
 #pragma unroll
             for (int off = 8; off <= 16; off <<= 1) {
-                const float so = __shfl_xor_sync(0xffffffffu, ws, off);
-                const int io = __shfl_xor_sync(0xffffffffu, wi, off);
-                if (better(so, io, ws, wi)) { ws = so; wi = io; }
+                const unsigned long long o = __shfl_xor_sync(0xffffffffu, wk, off);
+                wk = o > wk ? o : wk;
             }
-            if (be >= 0 && wi == bi) taken |= 1u << be;
-            if (lane < 8) lst[my_col * kMaxTopK + r] = pack_candidate(ws, wi);
-        }
-        __syncwarp();
-        group_barrier(col_group);
-        if (group_lead && lane < 8 && cc * 8 + lane < B) {
-            // 4-way merge of the ordered lists of column `lane` (key 0: list exhausted)
-            const unsigned long long* l0 =
-                reinterpret_cast<const unsigned long long*>(tr_group) + lane * kMaxTopK;
-            const int stride = static_cast<int>(kTrWarpBytes / 8);
-            const unsigned long long* l1 = l0 + stride;
-            const unsigned long long* l2 = l0 + 2 * stride;
-            const unsigned long long* l3 = l0 + 3 * stride;
-            int p0 = 0, p1 = 0, p2 = 0, p3 = 0;
-            unsigned long long* out = a.cand_keys + (static_cast<int64_t>(cc * 8 + lane) * a.n_tiles + tile) * k;
-            for (int r = 0; r < k; ++r) {
-                const unsigned long long h0 = p0 < k ? l0[p0] : 0ull, h1 = p1 < k ? l1[p1] : 0ull;
-                const unsigned long long h2 = p2 < k ? l2[p2] : 0ull, h3 = p3 < k ? l3[p3] : 0ull;
-                const unsigned long long m01 = h0 > h1 ? h0 : h1, m23 = h2 > h3 ? h2 : h3;
-                const unsigned long long m = m01 > m23 ? m01 : m23;
-                out[r] = m;
-                if (m == h0) ++p0;
-                else if (m == h1) ++p1;
-                else if (m == h2) ++p2;
-                else ++p3;
+            if (!__any_sync(0xffffffffu, wk != 0ull)) break;   // no column of the warp has one left
+            if (wk != 0ull && wk == bk) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ky[e] = ky[e] == bk ? 0ull : ky[e];
             }
+            if (lane < 8 && b < B) out[r] = wk;
+            last = wk;
         }
-        group_barrier(col_group);
+        if (lane < 8 && b < B) {
+            if (r < k) out[r] = 0ull;                    // a shorter list ends with key 0
+            if (r == k && last != 0ull) *th = last;     // a full list: its k-th key
+        }
     }
 }
 
