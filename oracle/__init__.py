@@ -80,6 +80,9 @@ def _load():
                                                   P, i64, P, i64, u64, u64, i32, i64, P, P, P, P,
                                                   P, P, i32]
             lib.orc_lmhead_sample_fp8.restype = ctypes.c_int
+            lib.orc_noise_row.argtypes = [i32, i64, i64, u64, u64, i64, i64, i32, P]
+            lib.orc_accept_uniform.argtypes = [i32, i64, i64, u64, u64, i64, i32]
+            lib.orc_accept_uniform.restype = ctypes.c_double
             lib.orc_uniform.argtypes = [ctypes.c_uint32, ctypes.c_uint32, i32]
             lib.orc_uniform.restype = ctypes.c_double
             _lib = lib
@@ -365,6 +368,120 @@ def lmhead_gumbel_topk(H_bits, W_bits, k: int, rows=None, **race_kw):
     r = lmhead_sample_rows(H_bits, W_bits, rows, want_scores=True, **race_kw)
     idx, val = topk_from_scores(r.scores, k)
     return idx, val, r.status, r.scores
+
+
+# ---- Speculative-decoding verification ----
+
+def noise_row(seeded, seed, pos, base_seed, offset, row, V, wide):
+    """Gumbel noise [V] of one row with an explicit row index and absolute position."""
+    g = np.empty(V)
+    _load().orc_noise_row(int(bool(seeded)), int(seed), int(pos), int(base_seed), int(offset),
+                          int(row), int(V), int(bool(wide)), _ptr(g))
+    return g
+
+
+def accept_uniform(seeded, seed, pos, base_seed, offset, row, wide) -> float:
+    """The acceptance uniform of one verification step (Philox call index 0xffffffff)."""
+    return _load().orc_accept_uniform(int(bool(seeded)), int(seed), int(pos), int(base_seed),
+                                      int(offset), int(row), int(bool(wide)))
+
+
+def _softmax(z):
+    m = np.max(z)
+    if not np.isfinite(m):
+        return np.zeros_like(z)
+    e = np.exp(z - m)
+    return e / e.sum()
+
+
+def verify_from_logits(target, draft, draft_tokens, *, temperature=None, seeds=None,
+                       positions=None, base_seed=0, offset=0, wide=False, want_detail=False):
+    """Speculative-decoding verification (spec-decode-ops "verify": the canonical rejection
+    sampling of Leviathan et al. and Chen et al.).  target [B, k+1, V] and draft [B, k, V]
+    logits, draft_tokens [B, k]; p = softmax(logits / T) per position, T per row.
+
+    Draft token x_i is accepted when u_i * p_d(x_i) < p_t(x_i) (probability min(1, p_t / p_d)),
+    in order; the first rejection j is replaced by a draw from the residual max(p_t - p_d, 0) at
+    position j (Gumbel race over log r + g; p_t itself if no entry of r is positive); with every
+    draft accepted a bonus token is drawn from p_t at position k (the plain race).  T == 0 rows:
+    accept while x_i is the target's argmax (smallest index on ties), then emit the argmax.
+
+    Noise: row b's draw at step position i uses the race's Philox noise at absolute position
+    positions[b] + i (seeded rows) or row index b (k + 1) + i with (base_seed, offset)
+    (unseeded rows); u_i is ``accept_uniform`` with the same keying.
+
+    Returns (accept_len [B] int64, out [B, k+1] int64 with -1 after the emitted tokens,
+    status [B] int32: 0 ok, 1 no finite target entry at the drawn position, 2 invalid T).
+    With want_detail, also the margins u_i p_d(x_i) - p_t(x_i) [B, k] (nan where not reached)
+    and the top-two scores of the final draw [B, 2]."""
+    t = np.asarray(target, np.float64)
+    d = np.asarray(draft, np.float64)
+    x = np.asarray(draft_tokens, np.int64)
+    B, K1, V = t.shape
+    k = K1 - 1
+    T = np.ones(B) if temperature is None else np.asarray(temperature, np.float64)
+    acc = np.zeros(B, np.int64)
+    out = np.full((B, K1), -1, np.int64)
+    status = np.zeros(B, np.int32)
+    margin = np.full((B, k), np.nan)
+    top2 = np.full((B, 2), -np.inf)
+    for b in range(B):
+        Tb = T[b]
+        if not (Tb >= 0.0):
+            status[b] = 2
+            continue
+        seeded = seeds is not None and seeds[b] >= 0
+        seed = int(seeds[b]) if seeded else 0
+        pos0 = int(positions[b]) if seeded else 0
+
+        def keying(i):
+            return dict(seeded=seeded, seed=seed, pos=pos0 + i if seeded else 0, base_seed=base_seed,
+                        offset=offset, row=b * K1 + i, wide=wide)
+
+        j = k
+        if Tb == 0.0:
+            for i in range(k):
+                a = int(np.argmax(t[b, i]))
+                if x[b, i] == a and np.isfinite(t[b, i, a]):
+                    out[b, i] = x[b, i]
+                else:
+                    j = i
+                    break
+            s = t[b, j].copy()
+        else:
+            for i in range(k):
+                pt = _softmax(t[b, i] / Tb)
+                pd = _softmax(d[b, i] / Tb)
+                u = accept_uniform(**keying(i))
+                xi = x[b, i]
+                margin[b, i] = u * pd[xi] - pt[xi]
+                if u * pd[xi] < pt[xi]:
+                    out[b, i] = xi
+                else:
+                    j = i
+                    break
+            g = noise_row(V=V, **keying(j))
+            if j < k:
+                r = np.maximum(_softmax(t[b, j] / Tb) - _softmax(d[b, j] / Tb), 0.0)
+                if (r > 0).any():
+                    with np.errstate(divide="ignore"):
+                        s = np.where(r > 0, np.log(r), -np.inf) + g
+                else:
+                    s = t[b, j] / Tb + g
+            else:
+                s = t[b, k] / Tb + g
+        s = np.where(np.isnan(s), -np.inf, s)
+        if not np.isfinite(s).any() and not (s == np.inf).any():
+            status[b] = 1
+            continue
+        a = int(np.argmax(s))                      # the first maximum: smallest index on ties
+        srt = np.sort(s)[::-1]
+        top2[b] = srt[:2] if V > 1 else (srt[0], -np.inf)
+        out[b, j] = a
+        acc[b] = j
+    if want_detail:
+        return acc, out, status, margin, top2
+    return acc, out, status
 
 
 # ---- FP8 (E4M3) inputs: W8A8 with per-row scales ----

@@ -172,6 +172,29 @@ void orc_noise_fill(int64_t B, int64_t V, const int64_t* seeds, const int64_t* p
     }
 }
 
+/* Gumbel noise g[v] (v < V) of one row given its row index and absolute position explicitly
+ * (speculative verification draws at positions pos + i of one batch row). */
+void orc_noise_row(int seeded, int64_t seed, int64_t pos, uint64_t base_seed, uint64_t offset,
+                   int64_t row, int64_t V, int wide, double* g) {
+    for (int64_t v = 0; v < V; ++v) {
+        uint32_t w[4], lo, hi;
+        orc_entry_words(seeded, seed, pos, base_seed, offset, row, (uint32_t)v, wide, w, &lo, &hi);
+        g[v] = orc_gumbel(orc_uniform(lo, hi, wide));
+    }
+}
+
+/* The acceptance uniform of speculative verification [SDO "verify", "Randomness"]: the Philox
+ * call with counter word 0 = 0xffffffff (a call index no vocabulary entry uses, V < 2^31), keyed
+ * like the race's noise; its first word (fp32 noise) or first two words (wide noise) give the
+ * midpoint uniform. */
+double orc_accept_uniform(int seeded, int64_t seed, int64_t pos, uint64_t base_seed,
+                          uint64_t offset, int64_t row, int wide) {
+    uint32_t ctr[4], key[2], w[4];
+    orc_key_counter(seeded, seed, pos, base_seed, offset, row, 0xffffffffu, ctr, key);
+    orc_philox4x32(ctr, key, 10, w);
+    return orc_uniform(w[0], w[1], wide);
+}
+
 /* ------------------------------------------------------------------------------------------ */
 /* Per-row race: transform, perturb, argmax, per-tile maxima [FS steps 2-6, Stage 2; SK]        */
 /* ------------------------------------------------------------------------------------------ */
