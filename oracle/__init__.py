@@ -404,7 +404,9 @@ def verify_from_logits(target, draft, draft_tokens, *, temperature=None, seeds=N
     in order; the first rejection j is replaced by a draw from the residual max(p_t - p_d, 0) at
     position j (Gumbel race over log r + g; p_t itself if no entry of r is positive); with every
     draft accepted a bonus token is drawn from p_t at position k (the plain race).  T == 0 rows:
-    accept while x_i is the target's argmax (smallest index on ties), then emit the argmax.
+    accept while x_i is the target's argmax (smallest index on ties), then emit the argmax.  A
+    draft token outside [0, V) is rejected.  NaN logits count as -inf (never drawn), as in the
+    race; a row with nothing finite at the drawn position emits no token at all.
 
     Noise: row b's draw at step position i uses the race's Philox noise at absolute position
     positions[b] + i (seeded rows) or row index b (k + 1) + i with (base_seed, offset)
@@ -412,10 +414,13 @@ def verify_from_logits(target, draft, draft_tokens, *, temperature=None, seeds=N
 
     Returns (accept_len [B] int64, out [B, k+1] int64 with -1 after the emitted tokens,
     status [B] int32: 0 ok, 1 no finite target entry at the drawn position, 2 invalid T).
-    With want_detail, also the margins u_i p_d(x_i) - p_t(x_i) [B, k] (nan where not reached)
-    and the top-two scores of the final draw [B, 2]."""
+    With want_detail, also the margins u_i p_d(x_i) - p_t(x_i) [B, k] (nan where not reached),
+    the top-two scores of the final draw [B, 2] and its scores [B, V] (-inf on rows that made
+    no draw)."""
     t = np.asarray(target, np.float64)
     d = np.asarray(draft, np.float64)
+    t = np.where(np.isnan(t), -np.inf, t)
+    d = np.where(np.isnan(d), -np.inf, d)
     x = np.asarray(draft_tokens, np.int64)
     B, K1, V = t.shape
     k = K1 - 1
@@ -425,6 +430,7 @@ def verify_from_logits(target, draft, draft_tokens, *, temperature=None, seeds=N
     status = np.zeros(B, np.int32)
     margin = np.full((B, k), np.nan)
     top2 = np.full((B, 2), -np.inf)
+    scores = np.full((B, V), -np.inf) if want_detail else None
     for b in range(B):
         Tb = T[b]
         if not (Tb >= 0.0):
@@ -454,6 +460,9 @@ def verify_from_logits(target, draft, draft_tokens, *, temperature=None, seeds=N
                 pd = _softmax(d[b, i] / Tb)
                 u = accept_uniform(**keying(i))
                 xi = x[b, i]
+                if not 0 <= xi < V:                     # not a vocabulary entry: rejected
+                    j = i
+                    break
                 margin[b, i] = u * pd[xi] - pt[xi]
                 if u * pd[xi] < pt[xi]:
                     out[b, i] = xi
@@ -473,14 +482,17 @@ def verify_from_logits(target, draft, draft_tokens, *, temperature=None, seeds=N
         s = np.where(np.isnan(s), -np.inf, s)
         if not np.isfinite(s).any() and not (s == np.inf).any():
             status[b] = 1
+            out[b] = -1
             continue
         a = int(np.argmax(s))                      # the first maximum: smallest index on ties
         srt = np.sort(s)[::-1]
         top2[b] = srt[:2] if V > 1 else (srt[0], -np.inf)
+        if want_detail:
+            scores[b] = s
         out[b, j] = a
         acc[b] = j
     if want_detail:
-        return acc, out, status, margin, top2
+        return acc, out, status, margin, top2, scores
     return acc, out, status
 
 

@@ -119,6 +119,13 @@ def test_greedy_invalid_and_masked_rows():
     assert acc[1] == 1 and out[1, 1] == np.argmax(tl[1, 1]) and (out[1, 2:] == -1).all()
     assert st[2] == 2 and st[4] == 2 and (out[2] == -1).all()
     assert st[3] == 1 and (out[3] == -1).all()
+    # nothing finite at the drawn position after an accepted prefix: no token at all
+    tl2 = tl[:2].copy()
+    tl2[:, 1] = -np.inf
+    tl2[1, 1, 7] = np.nan
+    acc2, out2, st2 = oracle.verify_from_logits(tl2, tl2[:, :k], x[:2, :], temperature=[0.0, 1.0],
+                                                seeds=[1, 2], positions=[0, 0])
+    assert (st2 == 1).all() and (acc2 == 0).all() and (out2 == -1).all()
 
 
 def test_seeded_rows_are_batch_position_invariant():
