@@ -25,8 +25,13 @@ Workloads (synthetic, seeded; the shapes of the FlashSampling page's measurement
   bf16 logits, V = 131072 (the Megatron-LM PR's filter settings).
 - ``qwen3-8b-topk``: the Qwen3-8B shape through ``lms_lmhead_sample_topk`` (Gumbel-top-k: k
   draws without replacement per row, k = ``--topk``, default 8).
+- ``verify``: ``lms_verify_from_logits`` (speculative-decoding verification) over bf16 target
+  [B, k+1, V] and draft [B, k, V] logits, V = 128256 (the spec-decode-ops page's latency
+  vocabulary), k = ``--spec-k`` (default 4), T = 0.8, draft tokens drawn from the draft.
 
-Every input is larger than L2 (the fused workloads stream W of 1.05–4.3 GB), so no flush is needed.
+The fused workloads stream W of 1.05–4.3 GB, larger than L2, so they need no flush. The
+materialised-logits workloads write a 256 MB buffer between timed steps whenever their inputs are
+under 512 MB (``--l2-flush auto``), and time each step's own events.
 
 The script prints one JSON line:
 
@@ -206,7 +211,7 @@ def make_workload(name: str, B: int, D: int, V: int):
 
 
 def default_batch(name: str) -> int:
-    return {"large-vocab": 256, "logits": 64, "noise": 64, "filtered": 64}.get(name, 64)
+    return {"large-vocab": 256, "logits": 64, "noise": 64, "filtered": 64, "verify": 64}.get(name, 64)
 
 
 # ------------------------------------------------------------------------------------------
@@ -240,6 +245,19 @@ def oracle_logits_time(logits, v_slice: int, threads: int):
     t0 = time.perf_counter()
     oracle.sample_from_logits(y, temperature=np.full(B, 0.7), seeds=np.arange(B) + 1000,
                               positions=np.zeros(B, np.int64), threads=threads)
+    return time.perf_counter() - t0
+
+
+def oracle_verify_time(tgt, dft, tokens, rows: int):
+    """Seconds for the oracle's verification of the first `rows` batch rows (full vocabulary)."""
+    import numpy as np
+    import oracle
+    t = tgt[:rows].double().numpy()
+    d = dft[:rows].double().numpy()
+    x = tokens[:rows].numpy()
+    t0 = time.perf_counter()
+    oracle.verify_from_logits(t, d, x, temperature=np.full(rows, 0.8), seeds=np.arange(rows) + 1000,
+                              positions=np.zeros(rows, np.int64))
     return time.perf_counter() - t0
 
 
@@ -288,11 +306,28 @@ def run_reference(args):
 # ------------------------------------------------------------------------------------------
 # the GPU arm
 # ------------------------------------------------------------------------------------------
-def _time_steps(step, n_warm, n_steps, dev, stream, first_index=0):
+def _time_steps(step, n_warm, n_steps, dev, stream, first_index=0, flush=None):
     import torch
     for i in range(n_warm):
         step(first_index + i)
     torch.cuda.synchronize(dev)
+    if flush is not None:
+        # L2 flushed before every timed step, outside its own pair of events
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps)]
+        barrier()
+        torch.cuda.synchronize(dev)
+        t0 = time.time()
+        for k in range(n_steps):
+            flush()
+            e0[k].record(stream)
+            step(first_index + n_warm + k)
+            e1[k].record(stream)
+        torch.cuda.synchronize(dev)
+        t1 = time.time()
+        barrier()
+        per_ms = [e0[k].elapsed_time(e1[k]) for k in range(n_steps)]
+        return statistics.mean(per_ms), per_ms, t0, t1
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_steps + 1)]
     barrier()
     torch.cuda.synchronize(dev)
@@ -424,6 +459,39 @@ def run_gpu(args):
                   "B": B, "V": V, "noise": "fp32",
                   "l2": "inputs %s L2 (%.0f MB)" % ("larger than" if alg > 130e6 else "within", alg / 1e6)}
         kernel = "filtered_race_kernel (one launch per step)"
+    elif args.workload == "verify":
+        V = args.V or 128256
+        D = 0
+        k = args.spec_k
+        dt = torch.bfloat16 if args.logits_dtype == "bf16" else torch.float32
+        tgt_h, dft_h = workloads.spec_logits(B, k, V, seed=7, dtype=dt)
+        tgt, dft = tgt_h.to(dev), dft_h.to(dev)
+        T = torch.full((B,), 0.8, device=dev)
+        seeds = 1000 + torch.arange(B, dtype=torch.int64, device=dev)
+        # positions advance by k + 1 per step; draft tokens drawn from the draft at T (setup)
+        pos_all = (torch.arange(n_steps, dtype=torch.int64)[:, None] * (k + 1)).expand(n_steps, B) \
+            .contiguous().to(dev)
+        gen = torch.Generator(device=dev).manual_seed(5)
+        pd = torch.softmax(dft.float() / 0.8, dim=-1).reshape(B * k, V)
+        tokens = torch.multinomial(pd, 1, generator=gen).reshape(B, k).contiguous()
+        del pd
+        ws_bytes = lms.lib().lms_workspace_bytes_verify(B, k, V)
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        acc = torch.empty(B, dtype=torch.int64, device=dev)
+        out = torch.empty(B, k + 1, dtype=torch.int64, device=dev)
+        launches_per_step = 4
+
+        def step(i):
+            lms.verify_from_logits(tgt, dft, tokens, temperature=T, seeds=seeds, positions=pos_all[i],
+                                   accept_len=acc, out=out, workspace=workspace)
+
+        esz = tgt.element_size()
+        # every logit read once; draft tokens and row parameters in; accept_len and k + 1 tokens out
+        alg = (2 * k + 1) * B * V * esz + B * k * 8 + B * 20 + B * (k + 2) * 8
+        flops = 0
+        config = {"workload": f"verify_from_logits B={B} k={k} V={V} {args.logits_dtype} logits, "
+                              f"draft corr 0.8, T 0.8", "B": B, "k": k, "V": V, "noise": "fp32"}
+        kernel = "verify_partials + verify_decide + verify_race + verify_finalize (one step, CUDA events)"
     elif args.workload == "noise":
         V = args.V or 151936
         D = 0
@@ -443,9 +511,18 @@ def run_gpu(args):
     else:
         raise SystemExit(f"unknown workload {args.workload}")
 
+    flush = None
+    if args.workload not in FUSED and (args.l2_flush == "on" or (args.l2_flush == "auto" and alg < 512e6)):
+        flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+        def flush():
+            flush_buf.fill_(1)
+        config["l2"] = "inputs %.0f MB; a 256 MB buffer written between timed steps" % (alg / 1e6)
+    elif "l2" not in config:
+        config["l2"] = "inputs %.0f MB, larger than L2, no flush" % (alg / 1e6)
     if rank == 0:
         sampler = ClockSampler(local)
-    avg_ms, per_ms, t0, t1 = _time_steps(step, args.warmup, args.steps, dev, stream)
+    avg_ms, per_ms, t0, t1 = _time_steps(step, args.warmup, args.steps, dev, stream, flush=flush)
     clocks = sampler.stop(t0, t1) if sampler else None
     ms_per_step = max_over_ranks(avg_ms, dev)
     us = ms_per_step * 1e3
@@ -535,6 +612,15 @@ def run_gpu(args):
             line["cpu_baseline"] = {"value": t / vs * V * 1e6, "unit": UNIT, "cores": threads,
                                     "kind": "oracle",
                                     "sample": f"B={B} rows x first {vs} of {V} logits, scaled linearly"}
+        elif args.workload == "verify":
+            rows = 1
+            t = oracle_verify_time(tgt_h, dft_h, tokens.cpu(), rows)
+            rows = int(max(1, min(B, args.cpu_seconds / max(t, 1e-3))))
+            t = oracle_verify_time(tgt_h, dft_h, tokens.cpu(), rows)
+            line["cpu_baseline"] = {"value": t / rows * B * 1e6, "unit": UNIT, "cores": 1,
+                                    "kind": "oracle",
+                                    "sample": f"{rows} of {B} batch rows (k={k}, full V={V}), "
+                                              f"{t:.1f} s wall, numpy fp64 on one thread, scaled linearly"}
     line.update(extra)
     print(json.dumps(line), flush=True)
 
@@ -545,9 +631,11 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=25)
     ap.add_argument("--workload", default="qwen3-8b",
-                    choices=list(FUSED) + ["logits", "noise", "filtered"])
+                    choices=list(FUSED) + ["logits", "noise", "filtered", "verify"])
     ap.add_argument("--batch", type=int, default=0)
     ap.add_argument("--topk", type=int, default=8, help="k of the qwen3-8b-topk workload")
+    ap.add_argument("--spec-k", type=int, default=4, help="draft length k of the verify workload")
+    ap.add_argument("--l2-flush", choices=["auto", "on", "off"], default="auto")
     ap.add_argument("--D", type=int, default=0)
     ap.add_argument("--V", type=int, default=0)
     ap.add_argument("--logits-dtype", choices=["fp32", "bf16"], default="bf16")

@@ -182,6 +182,31 @@ lms_status lms_lmhead_sample_topk(const void* H, int64_t ldh, const void* W, int
                                   int64_t* out, float* scores, void* workspace,
                                   size_t workspace_bytes, void* stream);
 
+/* Speculative-decoding verification (spec-decode-ops "verify": the canonical rejection sampling
+ * of speculative decoding) over materialised logits.  For batch row b with draft tokens
+ * x_0..x_{k-1} and p = softmax(logits / T) per position (T per row, for target and draft alike):
+ * x_i is accepted when u_i * p_d(x_i) < p_t(x_i), i.e. with probability min(1, p_t / p_d), in
+ * order; the first rejection j is replaced by a draw from the residual max(p_t - p_d, 0)
+ * renormalised (the target's own draw if no entry of it is positive); with every draft
+ * accepted, a bonus token is drawn from the target at position k.  The emitted tokens follow the
+ * target's distribution exactly.  T == 0 rows accept while x_i is the target's argmax (smallest
+ * index on ties) and then emit the argmax.  A draft token outside [0, V) is rejected.
+ *   target   [B][k + 1] rows, draft [B][k] rows, each row ld >= V elements apart (fp32 or bf16)
+ *   draft_tokens int64 [B][k]
+ *   accept_len   int64 [B]: the accepted draft tokens j
+ *   out          int64 [B][k + 1]: x_0..x_{j-1}, then the drawn token, then -1
+ * Noise: the race's Philox noise for row b at absolute position positions[b] + i (seeded rows)
+ * or row index b (k + 1) + i under (base_seed, offset) (unseeded rows); u_i is the same key's
+ * call with counter word 0 = 0xffffffff (fp32 noise: its first word, wide noise: its first two).
+ * params: temperature, seeds, positions, base_seed, offset, noise_mode, row_status (1: nothing
+ * finite at the drawn position, 2: invalid T); bias, mask, tile_v, path and debug_flags must be
+ * 0 / NULL.  1 <= k <= 32, V < 2^31.  Workspace: lms_workspace_bytes_verify(B, k, V). */
+size_t lms_workspace_bytes_verify(int64_t B, int32_t k, int64_t V);
+lms_status lms_verify_from_logits(const void* target, const void* draft, int32_t dtype, int64_t ld,
+                                  int64_t B, int32_t k, int64_t V, const int64_t* draft_tokens,
+                                  const lms_sample_params* params, int64_t* accept_len, int64_t* out,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
 /* The same race over materialised logits [B][ld] (fp32 or bf16).  ld == 0 broadcasts one
  * row to all B draws (each draw keyed by its own row index / position).  Several CTAs share a
  * row (one per tile of tile_v entries); the noise is generated in registers.

@@ -110,6 +110,11 @@ def lib() -> ctypes.CDLL:
             L.lms_lmhead_sample_topk.argtypes = [P, i64, P, i64, i64, i64, i64, i32,
                                                  ctypes.POINTER(SampleParams), P, P, P, sz, P]
             L.lms_lmhead_sample_topk.restype = i32
+            L.lms_workspace_bytes_verify.argtypes = [i64, i32, i64]
+            L.lms_workspace_bytes_verify.restype = sz
+            L.lms_verify_from_logits.argtypes = [P, P, i32, i64, i64, i32, i64, P,
+                                                 ctypes.POINTER(SampleParams), P, P, P, sz, P]
+            L.lms_verify_from_logits.restype = i32
             L.lms_philox_fill_noise.argtypes = [P, i32, i32, i64, i64, P, P, u64, u64, P]
             L.lms_philox_fill_noise.restype = i32
             _lib = L
@@ -418,6 +423,55 @@ def sample_from_logits_filtered(logits: torch.Tensor, *, B: Optional[int] = None
     _check(lib().lms_sample_from_logits_filtered(_ptr(logits), dt, ld, B, V, ctypes.byref(p),
                                                  ctypes.byref(fp), _ptr(out), _stream(stream)))
     return out
+
+
+VERIFY_MAX_K = 32
+
+
+def verify_from_logits(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.Tensor, *,
+                       temperature=None, seeds=None, positions=None, base_seed: int = 0,
+                       offset: int = 0, wide: bool = False, accept_len=None, out=None,
+                       workspace=None, row_status=None, stream=None):
+    """Speculative-decoding verification: target logits [B, k+1, V], draft logits [B, k, V]
+    (fp32 or bf16, same dtype, unit inner stride, rows ld apart within each tensor's [B, k(+1)]
+    block as laid out contiguously), draft_tokens int64 [B, k].  Draft token x_i is accepted with
+    probability min(1, p_t / p_d) in order; the first rejection is replaced by a draw from
+    max(p_t - p_d, 0), and a fully accepted row draws a bonus token from the target at position k.
+    Returns (accept_len int64 [B], out int64 [B, k+1] with -1 after the emitted tokens)."""
+    if target.dtype not in (torch.float32, torch.bfloat16) or draft.dtype != target.dtype:
+        raise TypeError("target and draft must both be float32 or both bfloat16")
+    if not target.is_cuda or draft.device != target.device:
+        raise ValueError("target and draft must be on the same CUDA device")
+    if target.dim() != 3 or draft.dim() != 3:
+        raise ValueError("target must be [B, k+1, V] and draft [B, k, V]")
+    B, K1, V = target.shape
+    k = K1 - 1
+    if tuple(draft.shape) != (B, k, V) or k < 1:
+        raise ValueError("draft must be [B, k, V] with k >= 1 and target [B, k+1, V]")
+    ld = target.stride(1)
+    for t, n, rows in ((target, "target", K1), (draft, "draft", k)):
+        if t.stride(2) != 1 or t.stride(1) != ld or t.stride(0) != rows * ld:
+            raise ValueError(f"{n} rows must be ld elements apart with unit inner stride")
+    dev = target.device
+    draft_tokens = _dev(draft_tokens, torch.int64, "draft_tokens", dev)
+    if tuple(draft_tokens.shape) != (B, k) or not draft_tokens.is_contiguous():
+        raise ValueError("draft_tokens must be a contiguous int64 [B, k]")
+    p = _params(B, dev, temperature, seeds, positions, None, None, base_seed, offset, wide, 0,
+                PATH_AUTO, row_status, 0, 0)
+    if accept_len is None:
+        accept_len = torch.empty(B, dtype=torch.int64, device=dev)
+    if out is None:
+        out = torch.empty(B, K1, dtype=torch.int64, device=dev)
+    if workspace is None:
+        need = lib().lms_workspace_bytes_verify(B, k, V)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    dt = DTYPE_F32 if target.dtype == torch.float32 else DTYPE_BF16
+    _check(lib().lms_verify_from_logits(_ptr(target), _ptr(draft), dt, ld, B, k, V,
+                                        _ptr(draft_tokens), ctypes.byref(p), _ptr(accept_len),
+                                        _ptr(out), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(),
+                                        _stream(stream)))
+    return accept_len, out
 
 
 def philox_fill_noise(B: int, V: int, *, kind: str = "gumbel", wide: bool = False, seeds=None,

@@ -352,6 +352,87 @@ lms_status lms_lmhead_sample_topk(const void* H, int64_t ldh, const void* W, int
     return LMS_OK;
 }
 
+namespace {
+// Workspace of lms_verify_from_logits, region by region (each 256-byte aligned).
+struct VerifyLayout {
+    int64_t nc, ncr;
+    size_t part, dec, cand, total;
+    VerifyLayout(int64_t B, int64_t k, int64_t V) {
+        lms::verify_chunks(V, &nc, &ncr);
+        const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(2 * k + 1) * static_cast<size_t>(nc);
+        part = round_up(rows * 4, 256);                                 // each of pmax, psum, parg
+        dec = round_up(static_cast<size_t>(B) * 4, 256);                // each of dec_*
+        cand = round_up(static_cast<size_t>(B) * static_cast<size_t>(ncr) * 2 * 4, 256);  // c_s, c_i
+        total = 3 * part + 4 * dec + 2 * cand;
+    }
+};
+constexpr int kVerifyMaxK = 32;
+}  // namespace
+
+size_t lms_workspace_bytes_verify(int64_t B, int32_t k, int64_t V) {
+    if (B <= 0 || V <= 0 || V > kMaxV || k < 1 || k > kVerifyMaxK) return 0;
+    return VerifyLayout(B, k, V).total;
+}
+
+lms_status lms_verify_from_logits(const void* target, const void* draft, int32_t dtype, int64_t ld,
+                                  int64_t B, int32_t k, int64_t V, const int64_t* draft_tokens,
+                                  const lms_sample_params* params, int64_t* accept_len, int64_t* out,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+    g_last_error[0] = '\0';
+    if (target == nullptr || draft == nullptr || draft_tokens == nullptr || accept_len == nullptr ||
+        out == nullptr)
+        return fail(LMS_ERR_INVALID_ARG, "target, draft, draft_tokens, accept_len and out are required");
+    if (dtype != LMS_DTYPE_F32 && dtype != LMS_DTYPE_BF16)
+        return fail(LMS_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+    if (B <= 0 || V <= 0 || V > kMaxV) return fail(LMS_ERR_INVALID_ARG, "need B > 0 and 0 < V < 2^31");
+    if (k < 1 || k > kVerifyMaxK) return fail(LMS_ERR_INVALID_ARG, "k must be in [1, %d] (k=%d)", kVerifyMaxK, k);
+    if (ld < V) return fail(LMS_ERR_INVALID_ARG, "ld must be >= V");
+    lms_status st = check_params(params, V);
+    if (st != LMS_OK) return st;
+    if (params->bias != nullptr || params->allow_mask != nullptr || params->tile_v != 0 ||
+        params->path != LMS_PATH_AUTO || params->debug_flags != 0)
+        return fail(LMS_ERR_INVALID_ARG, "bias, mask, tile_v, path and debug_flags do not apply to verify");
+    const VerifyLayout L(B, k, V);
+    if (B * (2 * k + 1) * L.nc > (int64_t{1} << 31) - 1 || B * L.ncr > (int64_t{1} << 31) - 1)
+        return fail(LMS_ERR_UNSUPPORTED, "B * (2k + 1) * ceil(V / 8192) exceeds the launch grid limit");
+    if (workspace == nullptr || workspace_bytes < L.total)
+        return fail(LMS_ERR_WORKSPACE, "workspace of %zu bytes needed", L.total);
+    char* w = static_cast<char*>(workspace);
+    lms::VerifyArgs a;
+    a.target = target;
+    a.draft = draft;
+    a.ld = ld;
+    a.B = B;
+    a.k = k;
+    a.V = V;
+    a.tokens = draft_tokens;
+    a.temperature = params->temperature;
+    a.seeds = params->seeds;
+    a.positions = params->positions;
+    a.base_seed = params->base_seed;
+    a.offset = params->offset;
+    a.nc = L.nc;
+    a.ncr = L.ncr;
+    a.pmax = reinterpret_cast<float*>(w);
+    a.psum = reinterpret_cast<float*>(w + L.part);
+    a.parg = reinterpret_cast<int*>(w + 2 * L.part);
+    char* d = w + 3 * L.part;
+    a.dec_j = reinterpret_cast<int*>(d);
+    a.dec_mode = reinterpret_cast<int*>(d + L.dec);
+    a.dec_lt = reinterpret_cast<float*>(d + 2 * L.dec);
+    a.dec_ld = reinterpret_cast<float*>(d + 3 * L.dec);
+    char* c = d + 4 * L.dec;
+    a.c_s = reinterpret_cast<float*>(c);
+    a.c_i = reinterpret_cast<int*>(c + L.cand);
+    a.accept_len = accept_len;
+    a.out = out;
+    a.row_status = params->row_status;
+    const cudaError_t e = lms::launch_verify(a, dtype == LMS_DTYPE_BF16, params->noise_mode == LMS_NOISE_WIDE53,
+                                             static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "verify launch");
+    return LMS_OK;
+}
+
 lms_status lms_lmhead_sample_fp8(const void* H, int64_t ldh, const void* W8, int64_t ldw8,
                                  const float* w_scale, int64_t B, int64_t D, int64_t V,
                                  const lms_sample_params* params, int64_t* out, void* workspace,

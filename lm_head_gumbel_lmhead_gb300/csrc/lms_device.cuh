@@ -4,6 +4,7 @@
 // functions, so the noise-fill kernel tests exactly what the samplers use.
 #pragma once
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
@@ -166,6 +167,35 @@ __device__ __forceinline__ void gumbel_run(const RowKey& k, uint32_t v0, float (
             g[4 * c + 2] = gumbel_from_exponential(exponential_fp32(w.w2));
             g[4 * c + 3] = gumbel_from_exponential(exponential_fp32(w.w3));
         }
+    }
+}
+
+// Entries p[0 .. 7] as floats (0 past n): one or two 16-byte loads when the unit is whole and
+// p is 16-byte aligned, else element loads.
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, int n, bool vec, float (&out)[8]) {
+    if (vec && n >= 8) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(p));
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            out[2 * i] = __uint_as_float(u[i] << 16);
+            out[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) out[e] = e < n ? __bfloat162float(p[e]) : 0.0f;
+    }
+}
+
+__device__ __forceinline__ void load8(const float* p, int n, bool vec, float (&out)[8]) {
+    if (vec && n >= 8) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+        const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+        out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+        out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) out[e] = e < n ? __ldg(p + e) : 0.0f;
     }
 }
 

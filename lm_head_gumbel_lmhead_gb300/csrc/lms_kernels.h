@@ -33,6 +33,40 @@ struct SampleArgs {
     int topk = 0;
 };
 
+// Speculative-decoding verification over materialised logits (see verify.cu).
+struct VerifyArgs {
+    const void* target;        // [B][k + 1] rows of ld elements (fp32 or bf16)
+    const void* draft;         // [B][k] rows of ld elements
+    int64_t ld;
+    int64_t B;
+    int k;
+    int64_t V;
+    const int64_t* tokens;     // [B][k] draft tokens
+    const float* temperature;
+    const int64_t* seeds;
+    const int64_t* positions;
+    uint64_t base_seed, offset;
+    int64_t nc;                // partials chunks per row
+    int64_t ncr;               // race chunks per row
+    // workspace
+    float* pmax;               // [B (2k + 1)][nc] online-softmax partials
+    float* psum;
+    int* parg;
+    int* dec_j;                // [B] first rejection (k: none)
+    int* dec_mode;             // [B] 0 finished, 1 race at j pending
+    float* dec_lt;             // [B] target log-normaliser at j
+    float* dec_ld;             // [B] draft log-normaliser at j (j < k)
+    float* c_s;                // [B][ncr][2] race candidates: residual, target
+    int* c_i;
+    // outputs
+    int64_t* accept_len;       // [B]
+    int64_t* out;              // [B][k + 1]
+    int32_t* row_status;       // [B] or null
+};
+
+void verify_chunks(int64_t V, int64_t* partial_chunks, int64_t* race_chunks);
+cudaError_t launch_verify(const VerifyArgs& a, bool bf16, bool wide, cudaStream_t stream);
+
 // The filtered race (a cluster per row; writes tokens and statuses directly).
 struct FilterArgs {
     SampleArgs a;

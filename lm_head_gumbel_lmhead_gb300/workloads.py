@@ -138,6 +138,18 @@ def logits_normal(B: int, V: int, std: float = 2.0, seed: int = 0,
     return (torch.randn(B, V, generator=_gen(seed + 41)) * std).to(dtype)
 
 
+def spec_logits(B: int, k: int, V: int, seed: int = 0, dtype: torch.dtype = torch.bfloat16,
+                std: float = 2.0, draft_corr: float = 0.8):
+    """Target logits [B, k+1, V] ~ N(0, std^2) and draft logits [B, k, V] correlated with the
+    target's first k positions (draft = c * target + sqrt(1 - c^2) * independent N(0, std^2)),
+    a draft that agrees with the target often but not always."""
+    g = _gen(seed + 57)
+    tgt = torch.randn(B, k + 1, V, generator=g) * std
+    noise = torch.randn(B, k, V, generator=g) * std
+    dft = draft_corr * tgt[:, :k] + (1.0 - draft_corr ** 2) ** 0.5 * noise
+    return tgt.to(dtype), dft.to(dtype)
+
+
 def quantize_weight_e4m3(W: torch.Tensor, chunk_rows: int = 8192):
     """Offline per-row FP8 (E4M3) weight quantisation, as a model would ship its LM head:
     w_scale[v] = max_d |W[v][d]| / 448 (fp32, 1 for an all-zero row), W8 = E4M3(W / w_scale)

@@ -115,3 +115,31 @@ def test_logits_and_noise_host_validation(L):
     assert L.lms_philox_fill_noise(FAKE, 9, 0, 4, 100, None, None, 0, 0, None) == lms.LMS_ERR_INVALID_ARG
     assert L.lms_philox_fill_noise(FAKE, 0, 0, 0, 100, None, None, 0, 0, None) == lms.LMS_ERR_INVALID_ARG
     assert L.lms_philox_fill_noise(ctypes.c_void_p(0x100008), 0, 0, 4, 100, None, None, 0, 0, None) == lms.LMS_ERR_UNSUPPORTED
+
+
+def test_verify_host_validation(L):
+    def call(p=None, dtype=0, ld=1000, B=4, k=3, V=1000, ws_bytes=1 << 24, tokens=FAKE):
+        p = _params() if p is None else p
+        return L.lms_verify_from_logits(FAKE, FAKE, dtype, ld, B, k, V, tokens, ctypes.byref(p),
+                                        FAKE, FAKE, FAKE, ws_bytes, None)
+    assert call(dtype=5) == lms.LMS_ERR_INVALID_ARG
+    assert call(k=0) == lms.LMS_ERR_INVALID_ARG
+    assert call(k=lms.VERIFY_MAX_K + 1) == lms.LMS_ERR_INVALID_ARG
+    assert call(ld=999) == lms.LMS_ERR_INVALID_ARG
+    assert call(B=0) == lms.LMS_ERR_INVALID_ARG
+    assert call(tokens=None) == lms.LMS_ERR_INVALID_ARG
+    assert call(p=_params(bias=0x1000, ld_bias=1000)) == lms.LMS_ERR_INVALID_ARG
+    assert call(p=_params(allow_mask=0x1000, ld_mask=32)) == lms.LMS_ERR_INVALID_ARG
+    assert call(p=_params(path=lms.PATH_GEMV)) == lms.LMS_ERR_INVALID_ARG
+    assert call(p=_params(seeds=0x1000)) == lms.LMS_ERR_INVALID_ARG     # seeds without positions
+    need = L.lms_workspace_bytes_verify(4, 3, 1000)
+    assert need > 0 and call(ws_bytes=need - 1) == lms.LMS_ERR_WORKSPACE
+    assert L.lms_workspace_bytes_verify(4, 0, 1000) == 0
+    assert L.lms_workspace_bytes_verify(4, 3, 2**31) == 0
+    # partials of 2k+1 rows per batch row (three arrays), decisions, two candidates per chunk
+    # (partials over chunks of 8192 entries, race candidates over chunks of 4096)
+    assert need == 3 * 256 + 4 * 256 + 2 * 256
+    big = L.lms_workspace_bytes_verify(64, 4, 151936)
+    nc, ncr = -(-151936 // 8192), -(-151936 // 4096)
+    r256 = lambda x: -(-x // 256) * 256
+    assert big == 3 * r256(64 * 9 * nc * 4) + 4 * r256(64 * 4) + 2 * r256(64 * ncr * 8)
