@@ -354,16 +354,20 @@ lms_status lms_lmhead_sample_topk(const void* H, int64_t ldh, const void* W, int
 
 namespace {
 // Workspace of lms_verify_from_logits, region by region (each 256-byte aligned).
+// Sized for fp32 logits, whose chunks are the shorter, so one size serves both types.
 struct VerifyLayout {
     int64_t nc, ncr;
-    size_t part, dec, cand, total;
-    VerifyLayout(int64_t B, int64_t k, int64_t V) {
-        lms::verify_chunks(V, &nc, &ncr);
-        const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(2 * k + 1) * static_cast<size_t>(nc);
-        part = round_up(rows * 4, 256);                                 // each of pmax, psum, parg
-        dec = round_up(static_cast<size_t>(B) * 4, 256);                // each of dec_*
-        cand = round_up(static_cast<size_t>(B) * static_cast<size_t>(ncr) * 2 * 4, 256);  // c_s, c_i
-        total = 3 * part + 4 * dec + 2 * cand;
+    size_t part, dec, cand, cnt, total;
+    VerifyLayout(int64_t B, int64_t k, int64_t V, bool bf16) {
+        int64_t nc32, ncr32;
+        lms::verify_chunks(V, false, &nc32, &ncr32);
+        lms::verify_chunks(V, bf16, &nc, &ncr);
+        const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(2 * k + 1) * static_cast<size_t>(nc32);
+        part = round_up(rows * 8 * 4, 256);          // each of pmax, psum, parg: one per warp (8)
+        dec = round_up(static_cast<size_t>(B) * sizeof(lms::VerifyDecision), 256);
+        cand = round_up(static_cast<size_t>(B) * static_cast<size_t>(ncr32) * 2 * 4, 256);  // c_s, c_i
+        cnt = round_up(static_cast<size_t>(B) * 4, 256);                // cnt_r
+        total = 3 * part + dec + 2 * cand + cnt;
     }
 };
 constexpr int kVerifyMaxK = 32;
@@ -371,7 +375,7 @@ constexpr int kVerifyMaxK = 32;
 
 size_t lms_workspace_bytes_verify(int64_t B, int32_t k, int64_t V) {
     if (B <= 0 || V <= 0 || V > kMaxV || k < 1 || k > kVerifyMaxK) return 0;
-    return VerifyLayout(B, k, V).total;
+    return VerifyLayout(B, k, V, false).total;
 }
 
 lms_status lms_verify_from_logits(const void* target, const void* draft, int32_t dtype, int64_t ld,
@@ -392,9 +396,7 @@ lms_status lms_verify_from_logits(const void* target, const void* draft, int32_t
     if (params->bias != nullptr || params->allow_mask != nullptr || params->tile_v != 0 ||
         params->path != LMS_PATH_AUTO || params->debug_flags != 0)
         return fail(LMS_ERR_INVALID_ARG, "bias, mask, tile_v, path and debug_flags do not apply to verify");
-    const VerifyLayout L(B, k, V);
-    if (B * (2 * k + 1) * L.nc > (int64_t{1} << 31) - 1 || B * L.ncr > (int64_t{1} << 31) - 1)
-        return fail(LMS_ERR_UNSUPPORTED, "B * (2k + 1) * ceil(V / 8192) exceeds the launch grid limit");
+    const VerifyLayout L(B, k, V, dtype == LMS_DTYPE_BF16);
     if (workspace == nullptr || workspace_bytes < L.total)
         return fail(LMS_ERR_WORKSPACE, "workspace of %zu bytes needed", L.total);
     char* w = static_cast<char*>(workspace);
@@ -416,14 +418,11 @@ lms_status lms_verify_from_logits(const void* target, const void* draft, int32_t
     a.pmax = reinterpret_cast<float*>(w);
     a.psum = reinterpret_cast<float*>(w + L.part);
     a.parg = reinterpret_cast<int*>(w + 2 * L.part);
-    char* d = w + 3 * L.part;
-    a.dec_j = reinterpret_cast<int*>(d);
-    a.dec_mode = reinterpret_cast<int*>(d + L.dec);
-    a.dec_lt = reinterpret_cast<float*>(d + 2 * L.dec);
-    a.dec_ld = reinterpret_cast<float*>(d + 3 * L.dec);
-    char* c = d + 4 * L.dec;
+    a.dec = reinterpret_cast<lms::VerifyDecision*>(w + 3 * L.part);
+    char* c = w + 3 * L.part + L.dec;
     a.c_s = reinterpret_cast<float*>(c);
     a.c_i = reinterpret_cast<int*>(c + L.cand);
+    a.cnt_r = reinterpret_cast<int*>(c + 2 * L.cand);
     a.accept_len = accept_len;
     a.out = out;
     a.row_status = params->row_status;

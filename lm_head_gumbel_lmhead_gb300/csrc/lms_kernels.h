@@ -34,6 +34,13 @@ struct SampleArgs {
 };
 
 // Speculative-decoding verification over materialised logits (see verify.cu).
+// A batch row's verification decision.
+struct VerifyDecision {
+    int j;                     // first rejection (k: none)
+    int mode;                  // 0 finished, 1 race at j pending
+    float lt, ld;              // log2 normalisers of target and draft at j (ld: j < k)
+};
+
 struct VerifyArgs {
     const void* target;        // [B][k + 1] rows of ld elements (fp32 or bf16)
     const void* draft;         // [B][k] rows of ld elements
@@ -49,22 +56,20 @@ struct VerifyArgs {
     int64_t nc;                // partials chunks per row
     int64_t ncr;               // race chunks per row
     // workspace
-    float* pmax;               // [B (2k + 1)][nc] online-softmax partials
+    float* pmax;               // [B (2k + 1)][nc][8] softmax partials, one per warp
     float* psum;
     int* parg;
-    int* dec_j;                // [B] first rejection (k: none)
-    int* dec_mode;             // [B] 0 finished, 1 race at j pending
-    float* dec_lt;             // [B] target log-normaliser at j
-    float* dec_ld;             // [B] draft log-normaliser at j (j < k)
+    VerifyDecision* dec;       // [B]
     float* c_s;                // [B][ncr][2] race candidates: residual, target
     int* c_i;
+    int* cnt_r;                // [B] race blocks done (zeroed by the decision kernel)
     // outputs
     int64_t* accept_len;       // [B]
     int64_t* out;              // [B][k + 1]
     int32_t* row_status;       // [B] or null
 };
 
-void verify_chunks(int64_t V, int64_t* partial_chunks, int64_t* race_chunks);
+void verify_chunks(int64_t V, bool bf16, int64_t* partial_chunks, int64_t* race_chunks);
 cudaError_t launch_verify(const VerifyArgs& a, bool bf16, bool wide, cudaStream_t stream);
 
 // The filtered race (a cluster per row; writes tokens and statuses directly).

@@ -133,13 +133,15 @@ def test_verify_host_validation(L):
     assert call(p=_params(path=lms.PATH_GEMV)) == lms.LMS_ERR_INVALID_ARG
     assert call(p=_params(seeds=0x1000)) == lms.LMS_ERR_INVALID_ARG     # seeds without positions
     need = L.lms_workspace_bytes_verify(4, 3, 1000)
+    r256 = lambda x: -(-x // 256) * 256
     assert need > 0 and call(ws_bytes=need - 1) == lms.LMS_ERR_WORKSPACE
     assert L.lms_workspace_bytes_verify(4, 0, 1000) == 0
     assert L.lms_workspace_bytes_verify(4, 3, 2**31) == 0
     # partials of 2k+1 rows per batch row (three arrays), decisions, two candidates per chunk
-    # (partials over chunks of 8192 entries, race candidates over chunks of 4096)
-    assert need == 3 * 256 + 4 * 256 + 2 * 256
+    # (sized for fp32 logits: one partial per warp over chunks of 8192 entries, 16-byte row
+    # decisions, race candidates over chunks of 4096), and a per-row completion counter
+    assert need == 3 * r256(4 * 7 * 8 * 4) + 256 + 2 * 256 + 256
     big = L.lms_workspace_bytes_verify(64, 4, 151936)
     nc, ncr = -(-151936 // 8192), -(-151936 // 4096)
     r256 = lambda x: -(-x // 256) * 256
-    assert big == 3 * r256(64 * 9 * nc * 4) + 4 * r256(64 * 4) + 2 * r256(64 * ncr * 8)
+    assert big == 3 * r256(64 * 9 * nc * 8 * 4) + r256(64 * 16) + 2 * r256(64 * ncr * 8) + r256(64 * 4)
