@@ -38,8 +38,9 @@
  * Conventions: all data pointers are DEVICE memory owned by the caller; the library never
  * allocates, frees or retains them.  Calls are asynchronous on `stream` (a cudaStream_t; NULL =
  * the legacy default stream).  Host-detectable errors return a non-zero lms_status before
- * anything is launched; lms_last_error() then holds a message (thread-local).  The library keeps
- * no state between calls.
+ * anything is launched; lms_last_error() then holds a message (thread-local).  Between calls the
+ * library keeps only per-device launch settings (kernel attributes and occupancy checks, set once
+ * under a lock) and, for lms_lmhead_sample_noalloc, its static scratch; no call's data outlives it.
  */
 #ifndef LMS_H_
 #define LMS_H_
