@@ -173,7 +173,8 @@ lms_status lms_lmhead_sample_fp8(const void* H, int64_t ldh, const void* W8, int
  *   out      int64 [B][k] (device): vocabulary indices; -1 past a row's finite scores
  *   scores   fp32 [B][k] (device) or NULL: the perturbed scores (-inf where out is -1)
  *   workspace  lms_workspace_bytes_topk(B, V, k) bytes: ordered key lists, one per row, tile
- *              and quarter of the tile's 128 rows, uint64 [B][ceil(V / 128)][4][k]
+ *              and quarter of the tile's 128 rows, uint64 [B][ceil(V / 128)][4][k]; then, at
+ *              the next 256-byte boundary, Stage 2's per-row part lists uint64 [B][32][k]
  * Row statuses as for lms_lmhead_sample (1: no finite score, 2: invalid T, 3: a bounded wait ran
  * out).  Requirements as for lms_lmhead_sample; path AUTO or TCGEN05 (bf16 H and W). */
 #define LMS_TOPK_MAX 16

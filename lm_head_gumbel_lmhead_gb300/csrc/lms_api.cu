@@ -296,8 +296,9 @@ lms_status lms_lmhead_sample(const void* H, int64_t ldh, const void* W, int64_t 
 size_t lms_workspace_bytes_topk(int64_t B, int64_t V, int32_t k) {
     if (B <= 0 || V <= 0 || V > kMaxV || k < 1 || k > LMS_TOPK_MAX) return 0;
     const int64_t nt = (V + LMS_FUSED_TILE_V - 1) / LMS_FUSED_TILE_V;
-    // per row and tile, one ordered list of k keys per TMEM quadrant (4)
-    return round_up(static_cast<size_t>(B) * static_cast<size_t>(nt) * 4 * static_cast<size_t>(k) * 8, 256);
+    // per row and tile, one ordered list of k keys per TMEM quadrant (4); then Stage 2's part lists
+    return round_up(static_cast<size_t>(B) * static_cast<size_t>(nt) * 4 * static_cast<size_t>(k) * 8, 256) +
+           round_up(lms::stage2_topk_part_bytes(B, k), 256);
 }
 
 lms_status lms_lmhead_sample_topk(const void* H, int64_t ldh, const void* W, int64_t ldw, int64_t B,
@@ -346,8 +347,11 @@ lms_status lms_lmhead_sample_topk(const void* H, int64_t ldh, const void* W, int
                                                     params->debug_flags, ac, s);
         if (e != cudaSuccess) return cuda_fail(e, "tcgen05 top-k Stage-1 launch");
     }
+    unsigned long long* part = reinterpret_cast<unsigned long long*>(
+        static_cast<char*>(workspace) +
+        round_up(static_cast<size_t>(B) * static_cast<size_t>(t.n_tiles) * 4 * static_cast<size_t>(k) * 8, 256));
     const cudaError_t e = lms::launch_stage2_topk(a.cand_keys, 4 * t.n_tiles, k, B, params->temperature,
-                                                  out, scores, params->row_status, s);
+                                                  out, scores, params->row_status, part, s);
     if (e != cudaSuccess) return cuda_fail(e, "top-k Stage-2 launch");
     return LMS_OK;
 }

@@ -102,9 +102,11 @@ cudaError_t launch_stage2(const float* cand_score, const int* cand_index, int64_
 
 // Stage 2 of Gumbel-top-k: per row, the k best of n_lists ordered key lists of k keys
 // (cand_keys [B][n_lists][k]); out [B][k] indices (-1 past the finite ones), scores [B][k] or null.
+// part_keys is scratch of stage2_topk_part_bytes(B, k) bytes.
+size_t stage2_topk_part_bytes(int64_t B, int k);
 cudaError_t launch_stage2_topk(const unsigned long long* cand_keys, int64_t n_lists, int k, int64_t B,
                                const float* temperature, int64_t* out, float* scores,
-                               int32_t* row_status, cudaStream_t stream);
+                               int32_t* row_status, unsigned long long* part_keys, cudaStream_t stream);
 
 cudaError_t launch_lmhead_gemv(const uint16_t* H, int64_t ldh, const uint16_t* W, int64_t ldw,
                                int64_t D, bool wide, const SampleArgs& a, cudaStream_t stream);
