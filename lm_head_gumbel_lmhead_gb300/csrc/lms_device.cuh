@@ -26,16 +26,15 @@ __device__ __forceinline__ Words philox4x32_10(uint32_t x0, uint32_t x1, uint32_
                                                uint32_t ka, uint32_t kb) {
 #pragma unroll
     for (int round = 0; round < 10; ++round) {
-        const uint64_t pa = static_cast<uint64_t>(kPhiloxMulA) * x0;
-        const uint64_t pb = static_cast<uint64_t>(kPhiloxMulB) * x2;
-        const uint32_t n0 = static_cast<uint32_t>(pb >> 32) ^ x1 ^ ka;
-        const uint32_t n2 = static_cast<uint32_t>(pa >> 32) ^ x3 ^ kb;
-        x1 = static_cast<uint32_t>(pb);
-        x3 = static_cast<uint32_t>(pa);
+        // the two products as separate high and low halves (32-bit multiplies)
+        const uint32_t hi_a = __umulhi(kPhiloxMulA, x0), lo_a = kPhiloxMulA * x0;
+        const uint32_t hi_b = __umulhi(kPhiloxMulB, x2), lo_b = kPhiloxMulB * x2;
+        const uint32_t n0 = hi_b ^ x1 ^ (ka + static_cast<uint32_t>(round) * kWeylA);
+        const uint32_t n2 = hi_a ^ x3 ^ (kb + static_cast<uint32_t>(round) * kWeylB);
+        x1 = lo_b;
+        x3 = lo_a;
         x0 = n0;
         x2 = n2;
-        ka += kWeylA;
-        kb += kWeylB;
     }
     return {x0, x1, x2, x3};
 }
@@ -80,41 +79,55 @@ __device__ __forceinline__ Words row_call(const RowKey& k, uint32_t n) {
 // ---------------------------------------------------------------------------------------------
 // Uniform -> E = -log u -> g = -log E, in fp32.
 //
-// u = (k + 1/2) / 2^m is written as n / 2^(m+1) with n = 2k + 1 odd.  Below one half, u itself
-// is formed (exact for m = 24; one rounding for m = 52) and E = -log u.  Above one half the
-// complement c = 1 - u = (2^(m+1) - n) / 2^(m+1) is formed from integers the same way and
-// E = -log(1 - c) is evaluated from c, so the tail (u -> 1, E -> 0, the largest g) keeps full
-// relative precision: E reaches 2^-25 (fp32 noise) and 2^-53 (wide noise), the ranges the
-// Megatron-LM PR gives.
+// u = (k + 1/2) / 2^m is written as n / 2^(m+1) with n = 2k + 1 odd, and its complement
+// c = 1 - u = j / 2^(m+1) with j = 2^(m+1) - n, both from integers.  Two evaluations of E, one
+// kept:
+//  * c >= 3/8 (u <= 5/8, E >= 0.47): E = -ln2 * log2(u) with the hardware base-2 logarithm,
+//    whose absolute error near 1 is about 2^-22, i.e. at most 2^-21 relative to E here;
+//  * c < 3/8: E = -log(1 - c) = 2 atanh(z) with z = c / (2 - c) = j / (2^(m+2) - j) < 3/13,
+//    summed to z^9/9 (the first omitted term, z^11/11, is below 2^-24 z).
+// The tail (u -> 1, E -> 0, the largest g) therefore keeps full relative precision: E reaches
+// 2^-25 (fp32 noise) and 2^-53 (wide noise), the ranges the Megatron-LM PR gives.
 // ---------------------------------------------------------------------------------------------
 
-// -log(1 - c) for 0 < c <= 1/2 with relative error about 2^-22: the series
-// -log(1 - c) = 2 atanh(z) = 2 (z + z^3/3 + z^5/5 + ...), z = c / (2 - c) <= 1/3, summed to
-// z^15/15 (the first omitted term is below z * 2^-29 for z <= 1/3).
-__device__ __forceinline__ float neg_log_one_minus(float c) {
-    const float z = __fdividef(c, 2.0f - c);
+// Hardware base-2 logarithm and reciprocal (PTX lg2.approx / rcp.approx, flush-to-zero forms).
+// Every argument passed to them here is a normal float (at least 2^-53), so the subnormal
+// handling of the non-ftz forms is not needed.
+__device__ __forceinline__ float lg2_approx(float x) {
+    float r;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+constexpr float kLn2f = 0.693147180559945309f;
+
+// -log(1 - c) = 2 atanh(z) from z = c / (2 - c) <= 3/13: 2 z (1 + z^2/3 + z^4/5 + z^6/7 + z^8/9).
+__device__ __forceinline__ float two_atanh_series(float z) {
     const float z2 = z * z;
-    float p = 1.0f / 15.0f;
-    p = fmaf(p, z2, 1.0f / 13.0f);
-    p = fmaf(p, z2, 1.0f / 11.0f);
-    p = fmaf(p, z2, 1.0f / 9.0f);
-    p = fmaf(p, z2, 1.0f / 7.0f);
-    p = fmaf(p, z2, 1.0f / 5.0f);
-    p = fmaf(p, z2, 1.0f / 3.0f);
-    p = fmaf(p, z2, 1.0f);
-    return 2.0f * z * p;
+    float p = 2.0f / 9.0f;
+    p = fmaf(p, z2, 2.0f / 7.0f);
+    p = fmaf(p, z2, 2.0f / 5.0f);
+    p = fmaf(p, z2, 2.0f / 3.0f);
+    p = fmaf(p, z2, 2.0f);
+    return z * p;
 }
 
 // E from the entry's word, fp32 noise: n = 2 (w >> 8) + 1, u = n / 2^25.
 __device__ __forceinline__ float exponential_fp32(uint32_t w) {
-    const uint32_t n = ((w >> 8) << 1) | 1u;
-    const float lower = -__logf(static_cast<float>(n) * 0x1p-25f);                       // u < 1/2
-    const float upper = neg_log_one_minus(static_cast<float>((1u << 25) - n) * 0x1p-25f); // c <= 1/2
-    return n < (1u << 24) ? lower : upper;
+    const uint32_t n = (w >> 7) | 1u;
+    const uint32_t j = (1u << 25) - n;
+    const float from_u = -kLn2f * lg2_approx(static_cast<float>(n) * 0x1p-25f);
+    const float jf = static_cast<float>(j);                       // exact when it is used
+    const float from_c = two_atanh_series(jf * rcp_approx(0x1p26f - jf));
+    return j < (3u << 22) ? from_c : from_u;
 }
 
-// A 53-bit odd integer to fp32 (one rounding of the low part, then one of the sum).
-__device__ __forceinline__ float odd53_to_float(uint64_t n) {
+// A 53-bit integer to fp32 (one rounding of the low part, then one of the sum).
+__device__ __forceinline__ float int53_to_float(uint64_t n) {
     return fmaf(static_cast<float>(static_cast<uint32_t>(n >> 32)), 0x1p32f,
                 static_cast<float>(static_cast<uint32_t>(n)));
 }
@@ -122,14 +135,15 @@ __device__ __forceinline__ float odd53_to_float(uint64_t n) {
 // E from the entry's two words, wide noise: n = 2 k + 1 with k = ((hi << 32) | lo) >> 12,
 // u = n / 2^53.
 __device__ __forceinline__ float exponential_wide(uint32_t lo, uint32_t hi) {
-    const uint64_t k = ((static_cast<uint64_t>(hi) << 32) | lo) >> 12;
-    const uint64_t n = (k << 1) | 1ull;
-    const float lower = -__logf(odd53_to_float(n) * 0x1p-53f);
-    const float upper = neg_log_one_minus(odd53_to_float((1ull << 53) - n) * 0x1p-53f);
-    return n < (1ull << 52) ? lower : upper;
+    const uint64_t n = (((static_cast<uint64_t>(hi) << 32) | lo) >> 11) | 1ull;
+    const uint64_t j = (1ull << 53) - n;
+    const float from_u = -kLn2f * lg2_approx(int53_to_float(n) * 0x1p-53f);
+    const float jf = int53_to_float(j);
+    const float from_c = two_atanh_series(jf * rcp_approx(0x1p54f - jf));
+    return j < (3ull << 50) ? from_c : from_u;
 }
 
-__device__ __forceinline__ float gumbel_from_exponential(float E) { return -__logf(E); }
+__device__ __forceinline__ float gumbel_from_exponential(float E) { return -kLn2f * lg2_approx(E); }
 
 // Gumbel noise of one entry (a whole call per entry: for kernels that visit entries one by one).
 template <bool kWide>

@@ -35,7 +35,10 @@ __device__ __forceinline__ void load_unit(const T* p, int64_t n_valid, float (&y
     }
 }
 
-template <typename T, int kUnit, bool kVector, bool kWide>
+// kPlain: no bias and no mask in this launch.  A sampled row then takes the fast loop: whole
+// units with 32-bit indices and no per-entry checks.  NaN needs no test there: a NaN score never
+// compares above the running best, so it loses to everything, as -inf does.
+template <typename T, int kUnit, bool kVector, bool kWide, bool kPlain>
 __global__ void __launch_bounds__(kThreads) logits_stage1_kernel(const T* __restrict__ logits,
                                                                  int64_t ld, int tile_v,
                                                                  SampleArgs a) {
@@ -49,31 +52,52 @@ __global__ void __launch_bounds__(kThreads) logits_stage1_kernel(const T* __rest
     int best_i = kNoIndex;
     if (!(p.flags & kRowInvalid)) {
         const T* y_row = logits + row * ld;
-        const float* bias_row = a.bias ? a.bias + row * a.ld_bias : nullptr;
-        const uint32_t* mask_row = a.mask ? a.mask + row * a.ld_mask : nullptr;
-        const int64_t v_tile = t * tile_v;
-        const int64_t v_end = (v_tile + tile_v < a.V) ? v_tile + tile_v : a.V;
-        // Units are strided by the CTA so that each thread visits its entries in increasing v
-        // (strict '>' then keeps the smallest index among equal scores within the thread).
-        for (int64_t v0 = v_tile + static_cast<int64_t>(threadIdx.x) * kUnit; v0 < v_end;
-             v0 += static_cast<int64_t>(kThreads) * kUnit) {
-            float y[kUnit];
-            load_unit<T, kUnit, kVector>(y_row + v0, v_end - v0, y);
-            float g[kUnit];
-            if (p.flags & kRowGreedy) {
+        const uint32_t v_tile = static_cast<uint32_t>(t * tile_v);
+        const uint32_t v_end = static_cast<uint32_t>((t * tile_v + tile_v < a.V) ? t * tile_v + tile_v : a.V);
+        if (kPlain && !(p.flags & kRowGreedy)) {
+            // Units are strided by the CTA so that each thread visits its entries in increasing v
+            // (strict '>' then keeps the smallest index among equal scores within the thread).
+            for (uint32_t v0 = v_tile + threadIdx.x * kUnit; v0 < v_end; v0 += kThreads * kUnit) {
+                float y[kUnit];
+                load_unit<T, kUnit, kVector>(y_row + v0, v_end - v0, y);
+                float g[kUnit];
+                gumbel_run<kWide, kUnit>(p.key, v0, g);
+                if (v0 + kUnit <= v_end) {
 #pragma unroll
-                for (int j = 0; j < kUnit; ++j) g[j] = 0.0f;
-            } else {
-                gumbel_run<kWide, kUnit>(p.key, static_cast<uint32_t>(v0), g);
+                    for (int j = 0; j < kUnit; ++j) {
+                        const float s = fmaf(y[j], p.inv_t, g[j]);
+                        if (s > best_s) { best_s = s; best_i = static_cast<int>(v0 + j); }
+                    }
+                } else {
+                    const uint32_t n = v_end - v0;
+#pragma unroll
+                    for (int j = 0; j < kUnit; ++j) {
+                        const float s = fmaf(y[j], p.inv_t, g[j]);
+                        if (j < n && s > best_s) { best_s = s; best_i = static_cast<int>(v0 + j); }
+                    }
+                }
             }
+        } else {
+            const float* bias_row = a.bias ? a.bias + row * a.ld_bias : nullptr;
+            const uint32_t* mask_row = a.mask ? a.mask + row * a.ld_mask : nullptr;
+            for (uint32_t v0 = v_tile + threadIdx.x * kUnit; v0 < v_end; v0 += kThreads * kUnit) {
+                float y[kUnit];
+                load_unit<T, kUnit, kVector>(y_row + v0, v_end - v0, y);
+                float g[kUnit];
+                if (p.flags & kRowGreedy) {
 #pragma unroll
-            for (int j = 0; j < kUnit; ++j) {
-                const int64_t v = v0 + j;
-                if (v < v_end) {
-                    const uint32_t vv = static_cast<uint32_t>(v);
-                    const float bias = bias_row ? __ldg(bias_row + v) : 0.0f;
-                    const float s = perturb(p, y[j], bias, allowed(mask_row, vv), g[j]);
-                    if (s > best_s) { best_s = s; best_i = static_cast<int>(vv); }
+                    for (int j = 0; j < kUnit; ++j) g[j] = 0.0f;
+                } else {
+                    gumbel_run<kWide, kUnit>(p.key, v0, g);
+                }
+#pragma unroll
+                for (int j = 0; j < kUnit; ++j) {
+                    const uint32_t v = v0 + j;
+                    if (v < v_end) {
+                        const float bias = bias_row ? __ldg(bias_row + v) : 0.0f;
+                        const float s = perturb(p, y[j], bias, allowed(mask_row, v), g[j]);
+                        if (s > best_s) { best_s = s; best_i = static_cast<int>(v); }
+                    }
                 }
             }
         }
@@ -95,15 +119,26 @@ __global__ void __launch_bounds__(kThreads) logits_stage1_kernel(const T* __rest
     pdl_launch_dependents();
 }
 
+template <typename T, int kUnit, bool kVector, bool kWide>
+void launch_noise(const T* y, int64_t ld, int tile_v, bool plain, const SampleArgs& a,
+                  unsigned grid, cudaStream_t stream) {
+    if (plain) {
+        logits_stage1_kernel<T, kUnit, kVector, kWide, true><<<grid, kThreads, 0, stream>>>(y, ld, tile_v, a);
+    } else {
+        logits_stage1_kernel<T, kUnit, kVector, kWide, false><<<grid, kThreads, 0, stream>>>(y, ld, tile_v, a);
+    }
+}
+
 template <typename T, int kUnit, bool kVector>
 cudaError_t launch_typed(const void* logits, int64_t ld, int tile_v, bool wide, const SampleArgs& a,
                          cudaStream_t stream) {
-    const int64_t grid = a.B * a.n_tiles;
+    const unsigned grid = static_cast<unsigned>(a.B * a.n_tiles);
     const T* y = static_cast<const T*>(logits);
+    const bool plain = a.bias == nullptr && a.mask == nullptr;
     if (wide) {
-        logits_stage1_kernel<T, kUnit, kVector, true><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(y, ld, tile_v, a);
+        launch_noise<T, kUnit, kVector, true>(y, ld, tile_v, plain, a, grid, stream);
     } else {
-        logits_stage1_kernel<T, kUnit, kVector, false><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(y, ld, tile_v, a);
+        launch_noise<T, kUnit, kVector, false>(y, ld, tile_v, plain, a, grid, stream);
     }
     return cudaGetLastError();
 }

@@ -78,6 +78,28 @@ def test_noise_extremes_keep_the_tail(wide):
         assert got.min() < 3 * 2.0 ** -24
 
 
+@pytest.mark.parametrize("wide", [False, True])
+def test_noise_dense_grid_matches_oracle(wide):
+    # 2^22 entries, every one against the oracle's fp64 E and g: covers both evaluations of E
+    # (from u, and from the exact complement c below 3/8) and the switch between them.
+    B, V = 16, 1 << 18
+    seeds = np.arange(B, dtype=np.int64) * 7919 + 3
+    seeds[::3] = -1
+    pos = np.arange(B, dtype=np.int64) * 11 + 2**31
+    dev = torch.device("cuda")
+    kw = dict(wide=wide, seeds=torch.from_numpy(seeds).to(dev), positions=torch.from_numpy(pos).to(dev),
+              base_seed=99, offset=5)
+    E = lms.philox_fill_noise(B, V, kind="exponential", **kw).cpu().numpy().astype(np.float64)
+    g = lms.philox_fill_noise(B, V, kind="gumbel", **kw).cpu().numpy().astype(np.float64)
+    _, ou, oE, og = oracle.noise(B, V, seeds, pos, 99, 5, wide)
+    rel = np.abs(E - oE) / oE
+    assert rel.max() <= E_RTOL, (rel.max(), ou.reshape(-1)[rel.argmax()])
+    assert np.all(np.abs(g - og) <= G_ATOL + G_RTOL * np.abs(og))
+    # both evaluations were exercised: u <= 5/8 and u > 5/8 each hold about their share
+    frac_c = np.mean(ou > 5 / 8)
+    assert 0.35 < frac_c < 0.40
+
+
 def test_replay_under_contention_and_single_row_equals_batched(rows):
     B, seeds, pos = rows
     V = 50_000
