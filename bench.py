@@ -85,9 +85,9 @@ def measured_peaks() -> dict:
             d = json.load(f)
         return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
                 "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
-                "source": "measured"}
+                "sm_max_mhz": float(d.get("sm_max_mhz", 2070.0)), "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
-            "source": "fallback"}
+            "sm_max_mhz": 2070.0, "source": "fallback"}
 
 
 def recorded_traffic(workload: str, B: int):
@@ -100,6 +100,35 @@ def recorded_traffic(workload: str, B: int):
         d = json.load(f)
     rec = d.get(f"{workload}/B={B}")
     if rec is None or rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return rec
+
+
+ALU_SOURCES = {"logits": ["lm_head_gumbel_lmhead_gb300/csrc/logits_sample.cu",
+                          "lm_head_gumbel_lmhead_gb300/csrc/stage2.cu",
+                          "lm_head_gumbel_lmhead_gb300/csrc/lms_device.cuh"],
+               "noise": ["lm_head_gumbel_lmhead_gb300/csrc/noise_fill.cu",
+                         "lm_head_gumbel_lmhead_gb300/csrc/lms_device.cuh"]}
+
+
+def alu_source_hash(workload: str) -> str:
+    h = hashlib.sha256()
+    for p in ALU_SOURCES[workload]:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_instructions(key: str, workload: str):
+    """Warp instructions per step of an ALU-bound workload from the committed ncu record, if it
+    was taken on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "alu_instructions.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    rec = d.get(key)
+    if rec is None or rec.get("source_hash") != alu_source_hash(workload):
         return None
     return rec
 
@@ -359,6 +388,7 @@ def run_gpu(args):
     B = args.batch
     extra = {}
     sampler = None
+    alu_key = None                                 # key of the ALU-bound workloads' ncu record
 
     if args.workload in FUSED:
         w = make_workload(args.workload, B, args.D, args.V)
@@ -437,6 +467,7 @@ def run_gpu(args):
                   "B": B, "V": V, "noise": "fp32", "tile_v": tv,
                   "l2": "inputs %s L2 (%.0f MB)" % ("larger than" if alg > 130e6 else "within", alg / 1e6)}
         kernel = "logits_stage1_kernel + stage2_kernel (one step, CUDA events)"
+        alu_key = f"logits/B={B}/V={V}/{args.logits_dtype}"
     elif args.workload == "filtered":
         V = args.V or 131072
         D = 0
@@ -508,6 +539,7 @@ def run_gpu(args):
         config = {"workload": f"philox_fill_noise gumbel B={B} V={V}", "B": B, "V": V,
                   "noise": "fp32", "l2": "output %.0f MB" % (alg / 1e6)}
         kernel = "noise_fill_kernel (one launch per step)"
+        alu_key = f"noise/B={B}/V={V}"
     else:
         raise SystemExit(f"unknown workload {args.workload}")
 
@@ -605,6 +637,22 @@ def run_gpu(args):
                     "algorithmic_bytes": alg}
     traffic = recorded_traffic(args.workload, B) if args.workload in FUSED else None
     roofline["traffic"] = traffic["dram_bytes_per_launch"] if traffic else None
+    inst = recorded_instructions(alu_key, args.workload) if alu_key else None
+    if inst is not None:
+        # Philox and the noise transform bound these kernels: the roofline is the SMs' issue
+        # rate (4 warp schedulers per SM, one warp instruction each per clock, at the maximum
+        # SM clock), against the step's warp instructions counted by ncu
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        issue_peak = sms * 4 * peaks["sm_max_mhz"] * 1e6 / 1e9
+        achieved_gi = inst["warp_inst_per_step"] / (us * 1e-6) / 1e9
+        roofline = {"bound": "alu", "achieved": round(achieved_gi, 1), "peak": round(issue_peak, 1),
+                    "unit": "Gwarp-inst/s", "frac": round(achieved_gi / issue_peak, 4),
+                    "peak_source": f"derived: {sms} SMs x 4 warp schedulers x 1 warp instruction per "
+                                   f"clock x {peaks['sm_max_mhz']:.0f} MHz",
+                    "warp_inst_per_step": inst["warp_inst_per_step"],
+                    "hbm": {"achieved": round(achieved_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": round(achieved_gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": alg},
+                    "traffic": inst.get("dram_bytes_per_step")}
     roofline["kernel"] = kernel
     line = {"metric": METRIC, "value": round(us, 2), "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),

@@ -124,3 +124,18 @@ def test_replay_under_contention_and_single_row_equals_batched(rows):
     u32 = lms.philox_fill_noise(B, V, kind="uniform", wide=False, seeds=sd, positions=pd, base_seed=3)
     lo, _ = oracle.entry_words(w32, np.arange(V)[None, :].repeat(B, 0), False)
     assert np.array_equal(u32.cpu().numpy(), (np.floor(lo.astype(np.float64) / 256) * 2 + 1) * 2.0 ** -25)
+
+
+@pytest.mark.parametrize("wide", [False, True])
+@pytest.mark.parametrize("kind", ["exponential", "gumbel"])
+def test_unaligned_output_buffer_matches_aligned(wide, kind):
+    # the entry point takes any 4-byte aligned buffer: one offset by 4 bytes (scalar stores)
+    # holds the same values as an aligned one (16- or 8-byte stores), for V a multiple of 4 and not
+    B = 5
+    for V in (4096, 1001):
+        ref = lms.philox_fill_noise(B, V, kind=kind, wide=wide, base_seed=11, offset=3)
+        raw = torch.empty(B * V + 1, dtype=torch.float32, device="cuda")
+        off = raw[1:].view(B, V)
+        assert off.data_ptr() % 16 == 4
+        lms.philox_fill_noise(B, V, kind=kind, wide=wide, base_seed=11, offset=3, out=off)
+        assert torch.equal(off, ref)
