@@ -77,6 +77,16 @@ __global__ void __launch_bounds__(kThreads) logits_stage1_kernel(const T* __rest
                     }
                 }
             }
+        } else if (kPlain) {
+            // greedy row, no bias and no mask: the argmax of y itself
+            for (uint32_t v0 = v_tile + threadIdx.x * kUnit; v0 < v_end; v0 += kThreads * kUnit) {
+                float y[kUnit];
+                load_unit<T, kUnit, kVector>(y_row + v0, v_end - v0, y);
+                const uint32_t n = v_end - v0;
+#pragma unroll
+                for (int j = 0; j < kUnit; ++j)
+                    if (j < n && y[j] > best_s) { best_s = y[j]; best_i = static_cast<int>(v0 + j); }
+            }
         } else {
             const float* bias_row = a.bias ? a.bias + row * a.ld_bias : nullptr;
             const uint32_t* mask_row = a.mask ? a.mask + row * a.ld_mask : nullptr;

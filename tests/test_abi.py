@@ -51,6 +51,8 @@ def test_tile_info(L):
     assert tv == 8192 and nt == 16
     tv, nt, _, _ = lms.tile_info(lms.OP_LOGITS, 1, 0, 131072)
     assert tv == 1024 and nt == 128
+    tv, nt, _, _ = lms.tile_info(lms.OP_LOGITS, 8, 0, 131072)
+    assert tv == 2048 and nt == 64
     assert lms.tile_info(lms.OP_LOGITS, 3, 0, 1000, 256)[:2] == (256, 4)
     assert lms.workspace_bytes(lms.OP_LMHEAD, 0, 4096, 100) == 0
 

@@ -195,3 +195,26 @@ def test_seeded_rows_batch_position_invariant(wide):
         assert one.item() == full[b].item()
     again = lms.sample_from_logits(logits, temperature=T, seeds=seeds, positions=pos, wide=wide, base_seed=5)
     assert torch.equal(again, full)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_plain_launch_greedy_and_sampled_rows(dtype):
+    # no bias and no mask: sampled rows take the fast loop, greedy rows (T = 0) the plain argmax,
+    # invalid rows report status 2; ties in the greedy argmax go to the smallest index
+    B, V = 12, 9001
+    logits = workloads.logits_normal(B, V, std=2.0, seed=31, dtype=dtype)
+    logits[3, 100] = logits[3, 7000] = 50.0          # a greedy tie across tiles
+    T = np.full(B, 0.9, np.float32)
+    T[[0, 3, 8]] = 0.0
+    T[5] = np.nan
+    seeds = np.arange(B, dtype=np.int64) + 40
+    seeds[::4] = -1
+    pos = np.arange(B, dtype=np.int64) * 3
+    kw = dict(temperature=T, seeds=seeds, positions=pos, base_seed=17, offset=2)
+    out, st, cs, ci, tv = run_gpu(logits.to(DEV), tile_v=1024, **kw)
+    orc = oracle.sample_from_logits(logits.double().numpy(), tile_v=tv, want_scores=True,
+                                    **{**kw, "temperature": T.astype(np.float64)})
+    check_rows(out, st, orc, lambda i, v: orc.scores[i, v])
+    check_tiles(cs, ci, orc, lambda i, v: orc.scores[i, v])
+    assert out[3] == 100 and st[5] == 2
+    assert out[0] == int(np.argmax(logits[0].double().numpy()))
