@@ -71,7 +71,7 @@ struct SmemLayout {
     }
 };
 
-template <int kEpiWarps, bool kWide, bool kFp8, bool kTopK>
+template <int kEpiWarps, bool kWide, bool kFp8, bool kTopK, bool kPlain>
 __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     lmhead_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
                      const TcParams prm) {
@@ -249,8 +249,8 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
                 epilogue_tile_topk<kEpiWarps, kWide>(a, rows, tr, thr, n_pad, t_row, tile, quad,
                                                      col_group, lane, B);
             } else {
-                epilogue_tile_columns<kEpiWarps, kWide>(a, rows, red, tr, t_row, tile, quad, col_group,
-                                                        lane, B);
+                epilogue_tile_columns<kEpiWarps, kWide, kPlain>(a, rows, red, tr, t_row, tile, quad,
+                                                                col_group, lane, B);
             }
             // The accumulator buffer is free for the MMA of tile i+2.
             tc_fence_before_sync();
@@ -280,10 +280,10 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     }
 }
 
-template <int kEpiWarps, bool kWide, bool kFp8, bool kTopK = false>
+template <int kEpiWarps, bool kWide, bool kFp8, bool kTopK = false, bool kPlain = false>
 cudaError_t launch_variant(const CUtensorMap& tmW, const CUtensorMap& tmH, const TcParams& prm,
                            size_t smem, int grid, cudaStream_t stream) {
-    auto kern = lmhead_tc_kernel<kEpiWarps, kWide, kFp8, kTopK>;
+    auto kern = lmhead_tc_kernel<kEpiWarps, kWide, kFp8, kTopK, kPlain>;
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     if (!kFp8) {
@@ -336,9 +336,18 @@ cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int
         return wide ? launch_variant<kEpilogueWarps, true, false, true>(tmW, tmH, prm, smem, grid, stream)
                     : launch_variant<kEpilogueWarps, false, false, true>(tmW, tmH, prm, smem, grid, stream);
     }
-    if (fp8)
+    // no bias and no mask: the race epilogue without per-entry bias, mask and bounds tests
+    const bool plain = a.bias == nullptr && a.mask == nullptr;
+    if (fp8) {
+        if (plain)
+            return wide ? launch_variant<kEpilogueWarps, true, true, false, true>(tmW, tmH, prm, smem, grid, stream)
+                        : launch_variant<kEpilogueWarps, false, true, false, true>(tmW, tmH, prm, smem, grid, stream);
         return wide ? launch_variant<kEpilogueWarps, true, true>(tmW, tmH, prm, smem, grid, stream)
                     : launch_variant<kEpilogueWarps, false, true>(tmW, tmH, prm, smem, grid, stream);
+    }
+    if (plain)
+        return wide ? launch_variant<kEpilogueWarps, true, false, false, true>(tmW, tmH, prm, smem, grid, stream)
+                    : launch_variant<kEpilogueWarps, false, false, false, true>(tmW, tmH, prm, smem, grid, stream);
     return wide ? launch_variant<kEpilogueWarps, true, false>(tmW, tmH, prm, smem, grid, stream)
                 : launch_variant<kEpilogueWarps, false, false>(tmW, tmH, prm, smem, grid, stream);
 }

@@ -220,7 +220,7 @@ constexpr uint32_t kTrWarpBytes = 8 * kTrStride * 4;
 // each thread owns 8 consecutive rows of one column, add bias / mask / temperature and the
 // Philox Gumbel noise (2 calls fp32, 4 wide), take the argmax, combine the 4 threads sharing
 // the column, and fold the result into red[b] (the tile's best key per column) with atomicMax.
-template <int kEpiWarps, bool kWide>
+template <int kEpiWarps, bool kWide, bool kPlain = false>
 __device__ __forceinline__ void epilogue_tile_columns(const SampleArgs& a, const RowParams* rows,
                                                       unsigned long long* red, float* tr,
                                                       uint32_t t_row, int64_t tile, int quad,
@@ -262,17 +262,38 @@ __device__ __forceinline__ void epilogue_tile_columns(const SampleArgs& a, const
                     for (int e = 0; e < 8; ++e)
                         if (v0 + e < a.V) y[e] *= ldexpf(__ldg(a.w_scale + v0 + e), eh);
                 }
-                const float* brow = a.bias ? a.bias + row * a.ld_bias : nullptr;
-                // the eight entries share one mask word (v0 is a multiple of 8)
-                const uint32_t mword =
-                    a.mask ? (__ldg(a.mask + row * a.ld_mask + (v0 >> 5)) >> (v0 & 31)) : 0xffu;
+                if constexpr (kPlain) {
+                    // no bias and no mask in this launch: s = y / T + g (greedy: y), no per-entry
+                    // tests on a whole chunk; a NaN score never compares above the running best,
+                    // so it loses as -inf does
+                    const float scale = (p.flags & kRowGreedy) ? 1.0f : p.inv_t;
+                    const int v0i = static_cast<int>(v0);
+                    if (v0 + 8 <= a.V) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int64_t v = v0 + e;
-                    if (v < a.V) {
-                        const float bias = brow ? __ldg(brow + v) : 0.0f;
-                        const float sc = perturb(p, y[e], bias, (mword >> e) & 1u, g[e]);
-                        if (sc > best_s) { best_s = sc; best_i = static_cast<int>(v); }
+                        for (int e = 0; e < 8; ++e) {
+                            const float sc = fmaf(y[e], scale, g[e]);
+                            if (sc > best_s) { best_s = sc; best_i = v0i + e; }
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float sc = fmaf(y[e], scale, g[e]);
+                            if (v0 + e < a.V && sc > best_s) { best_s = sc; best_i = v0i + e; }
+                        }
+                    }
+                } else {
+                    const float* brow = a.bias ? a.bias + row * a.ld_bias : nullptr;
+                    // the eight entries share one mask word (v0 is a multiple of 8)
+                    const uint32_t mword =
+                        a.mask ? (__ldg(a.mask + row * a.ld_mask + (v0 >> 5)) >> (v0 & 31)) : 0xffu;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int64_t v = v0 + e;
+                        if (v < a.V) {
+                            const float bias = brow ? __ldg(brow + v) : 0.0f;
+                            const float sc = perturb(p, y[e], bias, (mword >> e) & 1u, g[e]);
+                            if (sc > best_s) { best_s = sc; best_i = static_cast<int>(v); }
+                        }
                     }
                 }
             }

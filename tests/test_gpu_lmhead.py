@@ -106,6 +106,16 @@ def test_tcgen05_without_optional_inputs():
     full_parity(_ragged(33, 256, 2500, seed=5, features=False), lms.PATH_TCGEN05)
 
 
+@pytest.mark.parametrize("wide", [False, True])
+def test_tcgen05_plain_launch_greedy_invalid_and_ragged(wide):
+    # no bias and no mask: the plain epilogue, with greedy, invalid and unseeded rows and a last
+    # vocabulary tile that ends inside an 8-row chunk (V = 2500 = 19 * 128 + 68)
+    w = _ragged(37, 256, 2500, seed=9, wide=wide)
+    w = workloads.Workload(w.name, w.B, w.D, w.V, w.H, w.W, w.temperature, w.seeds, w.positions,
+                           None, None, w.noise_mode, base_seed=w.base_seed, offset=w.offset)
+    full_parity(w, lms.PATH_TCGEN05)
+
+
 def sampled_parity(w, rows, path=lms.PATH_AUTO):
     d = to_dev(w)
     out, st, cs, ci = run_fused(w, d, path)
