@@ -246,8 +246,8 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
                                    static_cast<uint32_t>(ab * n_pad);
             if constexpr (kTopK) {
                 unsigned long long* thr = reinterpret_cast<unsigned long long*>(base + L.run_off);
-                epilogue_tile_topk<kEpiWarps, kWide>(a, rows, tr, thr, n_pad, t_row, tile, quad,
-                                                     col_group, lane, B);
+                epilogue_tile_topk<kEpiWarps, kWide, kPlain>(a, rows, tr, thr, n_pad, t_row, tile,
+                                                             quad, col_group, lane, B);
             } else {
                 epilogue_tile_columns<kEpiWarps, kWide, kPlain>(a, rows, red, tr, t_row, tile, quad,
                                                                 col_group, lane, B);
@@ -331,13 +331,16 @@ cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int
     const size_t smem = L.total + 1024;
     int sms = device_sm_count();
     int grid = static_cast<int>(a.n_tiles < sms ? a.n_tiles : sms);
+    // no bias and no mask: the epilogues without per-entry bias, mask and bounds tests
+    const bool plain = a.bias == nullptr && a.mask == nullptr;
     if (a.topk > 0) {
         if (fp8 || a.topk > kMaxTopK || a.cand_keys == nullptr) return cudaErrorInvalidValue;
+        if (plain)
+            return wide ? launch_variant<kEpilogueWarps, true, false, true, true>(tmW, tmH, prm, smem, grid, stream)
+                        : launch_variant<kEpilogueWarps, false, false, true, true>(tmW, tmH, prm, smem, grid, stream);
         return wide ? launch_variant<kEpilogueWarps, true, false, true>(tmW, tmH, prm, smem, grid, stream)
                     : launch_variant<kEpilogueWarps, false, false, true>(tmW, tmH, prm, smem, grid, stream);
     }
-    // no bias and no mask: the race epilogue without per-entry bias, mask and bounds tests
-    const bool plain = a.bias == nullptr && a.mask == nullptr;
     if (fp8) {
         if (plain)
             return wide ? launch_variant<kEpilogueWarps, true, true, false, true>(tmW, tmH, prm, smem, grid, stream)

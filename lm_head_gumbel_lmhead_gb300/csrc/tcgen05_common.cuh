@@ -286,13 +286,37 @@ __device__ __forceinline__ void epilogue_tile_columns(const SampleArgs& a, const
                     // the eight entries share one mask word (v0 is a multiple of 8)
                     const uint32_t mword =
                         a.mask ? (__ldg(a.mask + row * a.ld_mask + (v0 >> 5)) >> (v0 & 31)) : 0xffu;
+                    const float scale = (p.flags & kRowGreedy) ? 1.0f : p.inv_t;
+                    if (v0 + 8 <= a.V) {
+                        // a whole chunk: the bias as two 16-byte loads when the row allows it;
+                        // s = (y + bias) / T + g, masked entries -inf; a NaN score never
+                        // compares above the running best, so it loses as -inf does
+                        float bias[8];
+                        if (brow != nullptr && (reinterpret_cast<uintptr_t>(brow + v0) & 15u) == 0) {
+                            const float4 b0 = __ldg(reinterpret_cast<const float4*>(brow + v0));
+                            const float4 b1 = __ldg(reinterpret_cast<const float4*>(brow + v0) + 1);
+                            bias[0] = b0.x; bias[1] = b0.y; bias[2] = b0.z; bias[3] = b0.w;
+                            bias[4] = b1.x; bias[5] = b1.y; bias[6] = b1.z; bias[7] = b1.w;
+                        } else {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int64_t v = v0 + e;
-                        if (v < a.V) {
-                            const float bias = brow ? __ldg(brow + v) : 0.0f;
-                            const float sc = perturb(p, y[e], bias, (mword >> e) & 1u, g[e]);
-                            if (sc > best_s) { best_s = sc; best_i = static_cast<int>(v); }
+                            for (int e = 0; e < 8; ++e) bias[e] = brow ? __ldg(brow + v0 + e) : 0.0f;
+                        }
+                        const int v0i = static_cast<int>(v0);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float t = fmaf(y[e] + bias[e], scale, g[e]);
+                            const float sc = ((mword >> e) & 1u) ? t : -CUDART_INF_F;
+                            if (sc > best_s) { best_s = sc; best_i = v0i + e; }
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int64_t v = v0 + e;
+                            if (v < a.V) {
+                                const float bias = brow ? __ldg(brow + v) : 0.0f;
+                                const float sc = perturb(p, y[e], bias, (mword >> e) & 1u, g[e]);
+                                if (sc > best_s) { best_s = sc; best_i = static_cast<int>(v); }
+                            }
                         }
                     }
                 }
@@ -326,7 +350,7 @@ constexpr unsigned long long kPoisonKey = ~0ull;
 // the row lie above it, so entries not above it cannot be among the row's k best and are dropped
 // before the rounds, which stop once no column of the warp has a key left.  Every key among the
 // row's k best therefore reaches some list; Stage 2 merges them.  No step crosses warps.
-template <int kEpiWarps, bool kWide>
+template <int kEpiWarps, bool kWide, bool kPlain = false>
 __device__ __forceinline__ void epilogue_tile_topk(const SampleArgs& a, const RowParams* rows,
                                                    float* tr, unsigned long long* thr, int n_pad,
                                                    uint32_t t_row, int64_t tile, int quad,
@@ -366,17 +390,31 @@ __device__ __forceinline__ void epilogue_tile_topk(const SampleArgs& a, const Ro
                     gumbel_run<kWide, 8>(p.key, static_cast<uint32_t>(v0), g);
                 }
                 const int64_t row = a.row0 + b;
-                const float* brow = a.bias ? a.bias + row * a.ld_bias : nullptr;
-                const uint32_t mword =
-                    a.mask ? (__ldg(a.mask + row * a.ld_mask + (v0 >> 5)) >> (v0 & 31)) : 0xffu;
+                if constexpr (kPlain) {
+                    // no bias and no mask in this launch: s = y / T + g (greedy: y); a NaN score
+                    // fails the -inf test below and gets no key, as a masked entry
+                    const float scale = (p.flags & kRowGreedy) ? 1.0f : p.inv_t;
+                    const int v0i = static_cast<int>(v0);
+                    const int n_in = (a.V - v0 < 8) ? static_cast<int>(a.V - v0) : 8;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int64_t v = v0 + e;
-                    if (v < a.V) {
-                        const float bias = brow ? __ldg(brow + v) : 0.0f;
-                        const float sc = perturb(p, y[e], bias, (mword >> e) & 1u, g[e]);
-                        const unsigned long long key = pack_candidate(sc, static_cast<int>(v));
-                        ky[e] = (sc > -CUDART_INF_F && key > theta) ? key : 0ull;
+                    for (int e = 0; e < 8; ++e) {
+                        const float sc = fmaf(y[e], scale, g[e]);
+                        const unsigned long long key = pack_candidate(sc, v0i + e);
+                        ky[e] = (e < n_in && sc > -CUDART_INF_F && key > theta) ? key : 0ull;
+                    }
+                } else {
+                    const float* brow = a.bias ? a.bias + row * a.ld_bias : nullptr;
+                    const uint32_t mword =
+                        a.mask ? (__ldg(a.mask + row * a.ld_mask + (v0 >> 5)) >> (v0 & 31)) : 0xffu;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int64_t v = v0 + e;
+                        if (v < a.V) {
+                            const float bias = brow ? __ldg(brow + v) : 0.0f;
+                            const float sc = perturb(p, y[e], bias, (mword >> e) & 1u, g[e]);
+                            const unsigned long long key = pack_candidate(sc, static_cast<int>(v));
+                            ky[e] = (sc > -CUDART_INF_F && key > theta) ? key : 0ull;
+                        }
                     }
                 }
             }

@@ -67,6 +67,24 @@ def test_topk_ragged(B, D, V, wide, k):
     full_topk_parity(_ragged(B, D, V, seed=B * 11 + D, wide=wide), k)
 
 
+@pytest.mark.parametrize("wide,k", [(False, 8), (True, 16)])
+def test_topk_plain_launch_greedy_invalid_and_ragged(wide, k):
+    # no bias and no mask (the plain epilogue), with greedy, invalid and unseeded rows and a
+    # last vocabulary tile that ends inside an 8-row chunk (V = 2500 = 19 * 128 + 68); entry 0
+    # is the plain race's token
+    w = _ragged(37, 256, 2500, seed=19, wide=wide)
+    w = workloads.Workload(w.name, w.B, w.D, w.V, w.H, w.W, w.temperature, w.seeds, w.positions,
+                           None, None, w.noise_mode, base_seed=w.base_seed, offset=w.offset)
+    full_topk_parity(w, k)
+    d = to_dev(w)
+    g_idx, _, g_st = run_topk(w, d, k)
+    race = lms.lmhead_sample(d["H"], d["W"], temperature=d["temperature"], seeds=d["seeds"],
+                             positions=d["positions"], base_seed=w.base_seed, offset=w.offset,
+                             wide=wide)
+    torch.cuda.synchronize()
+    assert np.array_equal(g_idx[:, 0], race.cpu().numpy())
+
+
 @pytest.mark.parametrize("wide", [False, True])
 def test_topk_tiny_every_output(wide):
     w = workloads.tiny()
