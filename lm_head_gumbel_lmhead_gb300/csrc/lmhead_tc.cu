@@ -31,7 +31,10 @@ namespace lms {
 namespace {
 
 using namespace tc;
-constexpr int kMaxStages = 12;
+// At most 8 stages in flight per SM: more lets each SM keep more W loads outstanding, which
+// measured slower on GB300 (Qwen3-8B shape, B = 1: 194.9 us with 11 stages, 188.8 with 10, 186.4
+// with 8, 189.4 with 6; B = 64 takes 8 either way).
+constexpr int kMaxStages = 8;
 #ifndef LMS_TC_EPILOGUE_WARPS
 #define LMS_TC_EPILOGUE_WARPS 16
 #endif
