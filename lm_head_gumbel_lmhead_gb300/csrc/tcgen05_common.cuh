@@ -257,10 +257,22 @@ __device__ __forceinline__ void epilogue_tile_columns(const SampleArgs& a, const
                 }
                 const int64_t row = a.row0 + b;
                 if (a.w_scale) {                 // FP8 inputs: logits = acc * 2^e_h * w_scale
+                    // w_scale * 2^e_h is exact while 2^e_h is a normal float, so the product
+                    // equals ldexpf(w_scale, e_h); below that range ldexpf per entry keeps it
                     const int eh = a.h_exp[row];
+                    const float* ws = a.w_scale + v0;
+                    if (eh >= -126 && eh <= 127 && v0 + 8 <= a.V &&
+                        (reinterpret_cast<uintptr_t>(ws) & 15u) == 0) {
+                        const float hs = __int_as_float((eh + 127) << 23);
+                        const float4 w0 = __ldg(reinterpret_cast<const float4*>(ws));
+                        const float4 w1 = __ldg(reinterpret_cast<const float4*>(ws) + 1);
+                        y[0] *= w0.x * hs; y[1] *= w0.y * hs; y[2] *= w0.z * hs; y[3] *= w0.w * hs;
+                        y[4] *= w1.x * hs; y[5] *= w1.y * hs; y[6] *= w1.z * hs; y[7] *= w1.w * hs;
+                    } else {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        if (v0 + e < a.V) y[e] *= ldexpf(__ldg(a.w_scale + v0 + e), eh);
+                        for (int e = 0; e < 8; ++e)
+                            if (v0 + e < a.V) y[e] *= ldexpf(__ldg(ws + e), eh);
+                    }
                 }
                 if constexpr (kPlain) {
                     // no bias and no mask in this launch: s = y / T + g (greedy: y), no per-entry
