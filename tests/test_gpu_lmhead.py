@@ -102,6 +102,15 @@ def test_tcgen05_ragged(B, D, V, wide):
     full_parity(_ragged(B, D, V, seed=B * 7 + D, wide=wide), lms.PATH_TCGEN05)
 
 
+@pytest.mark.parametrize("B,D,V,wide,features", [(700, 128, 1300, False, True),
+                                                 (1100, 64, 2100, True, True),
+                                                 (520, 96, 1500, False, False)])
+def test_tcgen05_row_groups(B, D, V, wide, features):
+    # above 256 rows one launch serves up to four row groups of 256 whose CTAs walk the vocabulary
+    # tiles together: 3 groups (700), 4 groups then 1 (1100), 3 groups with a 8-row last one (520)
+    full_parity(_ragged(B, D, V, seed=B + V, wide=wide, features=features), lms.PATH_TCGEN05)
+
+
 def test_tcgen05_without_optional_inputs():
     full_parity(_ragged(33, 256, 2500, seed=5, features=False), lms.PATH_TCGEN05)
 
