@@ -45,7 +45,8 @@ static_assert(kEpilogueWarps % 4 == 0, "epilogue warps come in groups of four");
 
 struct TcParams {
     SampleArgs a;        // rows [a.row0, a.row0 + a.B) of the batch
-    int n_groups;        // row groups of kGroupRows rows in this launch (CTA c serves group c % n_groups)
+    int n_groups;        // row groups in this launch (CTA c serves group c % n_groups)
+    int group_rows;      // batch rows per group (the last may have fewer)
     int nk;              // number of K chunks, ceil(D / 64)
     int n_pad;           // MMA N: batch rows padded to a multiple of 16 (16..256)
     int stages;
@@ -85,7 +86,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     uint8_t* base = smem_raw + (base_addr - raw_addr);
     const SmemLayout L(prm.stages, prm.stage_bytes, prm.n_pad, kEpiWarps, kTopK ? prm.a.topk : 0);
 
-    // This CTA's row group: CTA c serves rows [g * kGroupRows, (g + 1) * kGroupRows) of the
+    // This CTA's row group: CTA c serves rows [g * group_rows, (g + 1) * group_rows) of the
     // launch's rows, g = c mod n_groups, and visits the vocabulary tiles c / n_groups,
     // c / n_groups + gridDim.x / n_groups, ...; the CTAs of a group set walk the same tiles at the
     // same pace, so all but the first read of each W tile come from L2.
@@ -94,8 +95,8 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     const int64_t tile_step = gridDim.x / static_cast<unsigned>(prm.n_groups);
     SampleArgs a = prm.a;
     {
-        const int64_t r = static_cast<int64_t>(group) * kGroupRows;
-        a.B = (prm.a.B - r < kGroupRows) ? prm.a.B - r : kGroupRows;
+        const int64_t r = static_cast<int64_t>(group) * prm.group_rows;
+        a.B = (prm.a.B - r < prm.group_rows) ? prm.a.B - r : prm.group_rows;
         a.row0 = prm.a.row0 + r;
         a.cand_score = prm.a.cand_score ? prm.a.cand_score + r * prm.a.n_tiles : nullptr;
         a.cand_index = prm.a.cand_index ? prm.a.cand_index + r * prm.a.n_tiles : nullptr;
@@ -331,11 +332,13 @@ cudaError_t launch_variant(const CUtensorMap& tmW, const CUtensorMap& tmH, const
 cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int64_t D, int n_pad,
                              bool wide, uint32_t timeout_ms, uint32_t debug_flags,
                              const SampleArgs& a, cudaStream_t stream, bool fp8, int n_groups) {
-    if (n_groups < 1 || n_groups > kMaxGroups || a.B > static_cast<int64_t>(n_groups) * kGroupRows)
+    // groups of n_pad rows (one MMA N each); a single group may hold fewer rows than n_pad
+    if (n_groups < 1 || n_groups > kMaxGroups || a.B > static_cast<int64_t>(n_groups) * n_pad)
         return cudaErrorInvalidValue;
     TcParams prm;
     prm.a = a;
     prm.n_groups = n_groups;
+    prm.group_rows = n_pad;
     const int64_t k_per_stage = fp8 ? 2 * kBK : kBK;
     prm.nk = static_cast<int>((D + k_per_stage - 1) / k_per_stage);
     prm.n_pad = n_pad;
