@@ -410,7 +410,7 @@ def run_gpu(args):
         wide = w.noise_mode == 1
         kw = dict(temperature=T, seeds=seeds, bias=bias, mask=mask, base_seed=w.base_seed,
                   offset=w.offset, wide=wide, out=out, workspace=workspace)
-        launches_per_step = (1 + (B - 1) // 1024 if path == lms.PATH_TCGEN05 else 1) + 1
+        launches_per_step = (1 + (B - 1) // 256 if path == lms.PATH_TCGEN05 else 1) + 1
         if fp8:
             W8_h, wsc_h = workloads.quantize_weight_e4m3(w.W)
             W8, wsc = W8_h.to(dev), wsc_h.to(dev)

@@ -44,9 +44,7 @@ constexpr int kEpilogueWarps = LMS_TC_EPILOGUE_WARPS;
 static_assert(kEpilogueWarps % 4 == 0, "epilogue warps come in groups of four");
 
 struct TcParams {
-    SampleArgs a;        // rows [a.row0, a.row0 + a.B) of the batch
-    int n_groups;        // row groups in this launch (CTA c serves group c % n_groups)
-    int group_rows;      // batch rows per group (the last may have fewer)
+    SampleArgs a;
     int nk;              // number of K chunks, ceil(D / 64)
     int n_pad;           // MMA N: batch rows padded to a multiple of 16 (16..256)
     int stages;
@@ -86,22 +84,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     uint8_t* base = smem_raw + (base_addr - raw_addr);
     const SmemLayout L(prm.stages, prm.stage_bytes, prm.n_pad, kEpiWarps, kTopK ? prm.a.topk : 0);
 
-    // This CTA's row group: CTA c serves rows [g * group_rows, (g + 1) * group_rows) of the
-    // launch's rows, g = c mod n_groups, and visits the vocabulary tiles c / n_groups,
-    // c / n_groups + gridDim.x / n_groups, ...; the CTAs of a group set walk the same tiles at the
-    // same pace, so all but the first read of each W tile come from L2.
-    const int group = static_cast<int>(blockIdx.x % static_cast<unsigned>(prm.n_groups));
-    const int64_t tile0 = blockIdx.x / static_cast<unsigned>(prm.n_groups);
-    const int64_t tile_step = gridDim.x / static_cast<unsigned>(prm.n_groups);
-    SampleArgs a = prm.a;
-    {
-        const int64_t r = static_cast<int64_t>(group) * prm.group_rows;
-        a.B = (prm.a.B - r < prm.group_rows) ? prm.a.B - r : prm.group_rows;
-        a.row0 = prm.a.row0 + r;
-        a.cand_score = prm.a.cand_score ? prm.a.cand_score + r * prm.a.n_tiles : nullptr;
-        a.cand_index = prm.a.cand_index ? prm.a.cand_index + r * prm.a.n_tiles : nullptr;
-        if (kTopK) a.cand_keys = prm.a.cand_keys + r * prm.a.n_tiles * 4 * prm.a.topk;
-    }
+    const SampleArgs& a = prm.a;
     const int S = prm.stages;
     const int n_pad = prm.n_pad;
     const int B = static_cast<int>(a.B);
@@ -158,15 +141,13 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
         if (lane == 0) {
             // FP8 inputs: H8 is written by the quantisation kernel this launch may overlap
             if (kFp8) pdl_wait_primary();
-            // W: read once per launch with one row group; with several, the group's partners
-            // read each W tile again shortly after, so it is kept at normal priority
-            const uint64_t pol_w = prm.n_groups > 1 ? l2_policy_evict_normal() : l2_policy_evict_first();
+            const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_h = l2_policy_evict_last();
             uint32_t issued = 0, issued_parity = 0;   // per-stage: load in flight, its phase
             int stage = 0;
             uint32_t phase = 0;
             bool first = true;
-            for (int64_t tile = tile0; tile < nt && *err == 0; tile += tile_step) {
+            for (int64_t tile = blockIdx.x; tile < nt && *err == 0; tile += gridDim.x) {
                 for (int kc = 0; kc < prm.nk; ++kc) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, prm.timeout_ns, err)) {
                         *err = 1;
@@ -203,7 +184,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
             uint32_t phase = 0;
             int i = 0;
             bool ok = true;
-            for (int64_t tile = tile0; tile < nt && ok; tile += tile_step, ++i) {
+            for (int64_t tile = blockIdx.x; tile < nt && ok; tile += gridDim.x, ++i) {
                 const int ab = i & 1;
                 const uint32_t use_parity = (i >> 1) & 1;
                 if (!mbar_wait(acce_bar(ab), use_parity ^ 1u, prm.timeout_ns, err)) { ok = false; break; }
@@ -244,7 +225,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
         float* tr = reinterpret_cast<float*>(base + L.tr_off + (warp - 2) * kTrWarpBytes);
         int i = 0;
         bool ok = true;
-        for (int64_t tile = tile0; tile < nt; tile += tile_step, ++i) {
+        for (int64_t tile = blockIdx.x; tile < nt; tile += gridDim.x, ++i) {
             const int ab = i & 1;
             const uint32_t use_parity = (i >> 1) & 1;
             if (ok) ok = mbar_wait(accf_bar(ab), use_parity, prm.timeout_ns, err);
@@ -331,14 +312,9 @@ cudaError_t launch_variant(const CUtensorMap& tmW, const CUtensorMap& tmH, const
 
 cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int64_t D, int n_pad,
                              bool wide, uint32_t timeout_ms, uint32_t debug_flags,
-                             const SampleArgs& a, cudaStream_t stream, bool fp8, int n_groups) {
-    // groups of n_pad rows (one MMA N each); a single group may hold fewer rows than n_pad
-    if (n_groups < 1 || n_groups > kMaxGroups || a.B > static_cast<int64_t>(n_groups) * n_pad)
-        return cudaErrorInvalidValue;
+                             const SampleArgs& a, cudaStream_t stream, bool fp8) {
     TcParams prm;
     prm.a = a;
-    prm.n_groups = n_groups;
-    prm.group_rows = n_pad;
     const int64_t k_per_stage = fp8 ? 2 * kBK : kBK;
     prm.nk = static_cast<int>((D + k_per_stage - 1) / k_per_stage);
     prm.n_pad = n_pad;
@@ -356,12 +332,8 @@ cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int
     prm.debug_flags = debug_flags;
     const SmemLayout L(stages, prm.stage_bytes, n_pad, kEpilogueWarps, a.topk);
     const size_t smem = L.total + 1024;
-    // one CTA per SM, a whole number of CTAs per row group
-    const int sms = device_sm_count();
-    const int64_t want = a.n_tiles * n_groups;
-    int grid = static_cast<int>(want < sms ? want : sms);
-    grid -= grid % n_groups;
-    if (grid < n_groups) return cudaErrorInvalidValue;
+    int sms = device_sm_count();
+    int grid = static_cast<int>(a.n_tiles < sms ? a.n_tiles : sms);
     // no bias and no mask: the epilogues without per-entry bias, mask and bounds tests
     const bool plain = a.bias == nullptr && a.mask == nullptr;
     if (a.topk > 0) {

@@ -31,24 +31,7 @@ lms_status cuda_fail(cudaError_t e, const char* what) {
 }
 
 constexpr int64_t kMaxV = (int64_t{1} << 31) - 1;
-// Rows of one fused launch starting at row r0: up to lms::kMaxGroups row groups of at most 256
-// rows (grouped) or one group, of equal size but the last; MMA N is the group's rows padded to 16.
-struct LaunchRows {
-    int64_t nb;
-    int n_groups;
-    int n_pad;
-};
-// (Two groups of 128 rows for B = 256 measured slower, 351 against 269 us at the Qwen3-8B shape:
-// there the W tiles' second reads missed L2.)
-LaunchRows fused_launch_rows(int64_t B, int64_t r0, bool grouped) {
-    const int64_t per = grouped ? int64_t{lms::kGroupRows} * lms::kMaxGroups : int64_t{lms::kGroupRows};
-    LaunchRows L;
-    L.nb = (B - r0 < per) ? B - r0 : per;
-    L.n_groups = static_cast<int>((L.nb + lms::kGroupRows - 1) / lms::kGroupRows);
-    const int64_t rows = (L.nb + L.n_groups - 1) / L.n_groups;      // balanced groups
-    L.n_pad = static_cast<int>(rows < 16 ? 16 : (rows + 15) / 16 * 16);
-    return L;
-}
+constexpr int kTcMaxBatchPerLaunch = 256;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -287,25 +270,23 @@ lms_status lms_lmhead_sample(const void* H, int64_t ldh, const void* W, int64_t 
         CUtensorMap tmW;
         if ((st = encode_bf16_map(&tmW, W, V, D, ldw, 128)) != LMS_OK) return st;
         const uint32_t timeout_ms = params->timeout_ms ? params->timeout_ms : 2000u;
-        // Batches above 256 rows: one launch serves up to 4 row groups of 256 rows (one MMA N
-        // each) whose CTAs walk the vocabulary tiles together, so W streams from HBM about once
-        // per launch; the pair path runs one launch per 256 rows.
-        const bool pair = path == LMS_PATH_TCGEN05_PAIR;
-        for (int64_t r0 = 0; r0 < B;) {
-            const LaunchRows L = fused_launch_rows(B, r0, !pair);
+        // Batches above 256 rows run as several launches of <= 256 rows (one MMA N each).
+        for (int64_t r0 = 0; r0 < B; r0 += kTcMaxBatchPerLaunch) {
+            const int64_t nb = (B - r0 < kTcMaxBatchPerLaunch) ? B - r0 : kTcMaxBatchPerLaunch;
+            const int n_pad = static_cast<int>(nb < 16 ? 16 : (nb + 15) / 16 * 16);
+            const bool pair = path == LMS_PATH_TCGEN05_PAIR;
             CUtensorMap tmH;
-            if ((st = encode_bf16_map(&tmH, H, B, D, ldh, pair ? L.n_pad / 2 : L.n_pad)) != LMS_OK) return st;
+            if ((st = encode_bf16_map(&tmH, H, B, D, ldh, pair ? n_pad / 2 : n_pad)) != LMS_OK) return st;
             lms::SampleArgs ac = a;
-            ac.B = L.nb;
+            ac.B = nb;
             ac.row0 = r0;
             ac.cand_score = a.cand_score + r0 * t.n_tiles;
             ac.cand_index = a.cand_index + r0 * t.n_tiles;
-            e = pair ? lms::launch_lmhead_tc_pair(tmW, tmH, D, L.n_pad, wide, timeout_ms,
+            e = pair ? lms::launch_lmhead_tc_pair(tmW, tmH, D, n_pad, wide, timeout_ms,
                                                   params->debug_flags, ac, s)
-                     : lms::launch_lmhead_tc(tmW, tmH, D, L.n_pad, wide, timeout_ms,
-                                             params->debug_flags, ac, s, false, L.n_groups);
+                     : lms::launch_lmhead_tc(tmW, tmH, D, n_pad, wide, timeout_ms,
+                                             params->debug_flags, ac, s);
             if (e != cudaSuccess) return cuda_fail(e, pair ? "tcgen05 pair Stage-1 launch" : "tcgen05 Stage-1 launch");
-            r0 += L.nb;
         }
     }
     e = lms::launch_stage2(a.cand_score, a.cand_index, t.n_tiles, B, params->temperature, out,
@@ -355,18 +336,18 @@ lms_status lms_lmhead_sample_topk(const void* H, int64_t ldh, const void* W, int
     CUtensorMap tmW;
     if ((st = encode_bf16_map(&tmW, W, V, D, ldw, 128)) != LMS_OK) return st;
     const uint32_t timeout_ms = params->timeout_ms ? params->timeout_ms : 2000u;
-    for (int64_t r0 = 0; r0 < B;) {
-        const LaunchRows L = fused_launch_rows(B, r0, true);
+    for (int64_t r0 = 0; r0 < B; r0 += kTcMaxBatchPerLaunch) {
+        const int64_t nb = (B - r0 < kTcMaxBatchPerLaunch) ? B - r0 : kTcMaxBatchPerLaunch;
+        const int n_pad = static_cast<int>(nb < 16 ? 16 : (nb + 15) / 16 * 16);
         CUtensorMap tmH;
-        if ((st = encode_bf16_map(&tmH, H, B, D, ldh, L.n_pad)) != LMS_OK) return st;
+        if ((st = encode_bf16_map(&tmH, H, B, D, ldh, n_pad)) != LMS_OK) return st;
         lms::SampleArgs ac = a;
-        ac.B = L.nb;
+        ac.B = nb;
         ac.row0 = r0;
         ac.cand_keys = a.cand_keys + r0 * t.n_tiles * 4 * k;
-        const cudaError_t e = lms::launch_lmhead_tc(tmW, tmH, D, L.n_pad, wide, timeout_ms,
-                                                    params->debug_flags, ac, s, false, L.n_groups);
+        const cudaError_t e = lms::launch_lmhead_tc(tmW, tmH, D, n_pad, wide, timeout_ms,
+                                                    params->debug_flags, ac, s);
         if (e != cudaSuccess) return cuda_fail(e, "tcgen05 top-k Stage-1 launch");
-        r0 += L.nb;
     }
     unsigned long long* part = reinterpret_cast<unsigned long long*>(
         static_cast<char*>(workspace) +
@@ -492,19 +473,18 @@ lms_status lms_lmhead_sample_fp8(const void* H, int64_t ldh, const void* W8, int
     if ((st = encode_map(&tmW, W8, V, D, ldw8, 128, true)) != LMS_OK) return st;
     const bool wide = params->noise_mode == LMS_NOISE_WIDE53;
     const uint32_t timeout_ms = params->timeout_ms ? params->timeout_ms : 2000u;
-    for (int64_t r0 = 0; r0 < B;) {
-        const LaunchRows L = fused_launch_rows(B, r0, true);
+    for (int64_t r0 = 0; r0 < B; r0 += kTcMaxBatchPerLaunch) {
+        const int64_t nb = (B - r0 < kTcMaxBatchPerLaunch) ? B - r0 : kTcMaxBatchPerLaunch;
+        const int n_pad = static_cast<int>(nb < 16 ? 16 : (nb + 15) / 16 * 16);
         CUtensorMap tmH;
-        if ((st = encode_map(&tmH, q, B, D, ldq, L.n_pad, true)) != LMS_OK) return st;
+        if ((st = encode_map(&tmH, q, B, D, ldq, n_pad, true)) != LMS_OK) return st;
         lms::SampleArgs ac = a;
-        ac.B = L.nb;
+        ac.B = nb;
         ac.row0 = r0;
         ac.cand_score = a.cand_score + r0 * t.n_tiles;
         ac.cand_index = a.cand_index + r0 * t.n_tiles;
-        e = lms::launch_lmhead_tc(tmW, tmH, D, L.n_pad, wide, timeout_ms, params->debug_flags, ac, s, true,
-                                  L.n_groups);
+        e = lms::launch_lmhead_tc(tmW, tmH, D, n_pad, wide, timeout_ms, params->debug_flags, ac, s, true);
         if (e != cudaSuccess) return cuda_fail(e, "tcgen05 FP8 Stage-1 launch");
-        r0 += L.nb;
     }
     e = lms::launch_stage2(a.cand_score, a.cand_index, t.n_tiles, B, params->temperature, out,
                            params->row_status, s);

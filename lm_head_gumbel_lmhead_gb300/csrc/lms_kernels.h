@@ -114,17 +114,9 @@ cudaError_t launch_lmhead_gemv(const uint16_t* H, int64_t ldh, const uint16_t* W
 // The tcgen05 path.  tmW / tmH are TMA descriptors (bf16, 128-byte swizzle, boxes of 64 x 128
 // for W and 64 x n_pad for H).  B <= 256 per launch.
 // fp8: E4M3 operands (kind::f8f6f4), boxes of 128 x 128 / 128 x n_pad bytes; a.h_exp / a.w_scale set.
-// Batch rows of one fused-kernel row group at most (the largest MMA N), and the row groups one
-// launch serves.
-constexpr int kGroupRows = 256;
-constexpr int kMaxGroups = 4;
-
-// a.B rows (up to n_groups * n_pad) in one launch: the CTAs are split into n_groups sets of n_pad
-// rows that walk the vocabulary tiles together, so each W tile streams from HBM about once.
 cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int64_t D, int n_pad,
                              bool wide, uint32_t timeout_ms, uint32_t debug_flags,
-                             const SampleArgs& a, cudaStream_t stream, bool fp8 = false,
-                             int n_groups = 1);
+                             const SampleArgs& a, cudaStream_t stream, bool fp8 = false);
 // (a.topk > 0 selects the Gumbel-top-k epilogue: bf16 only.)
 
 // The CTA-pair tcgen05 path (cta_group::2, M = 256): tmH boxes are 64 x (n_pad / 2).

@@ -105,9 +105,9 @@ def test_tcgen05_ragged(B, D, V, wide):
 @pytest.mark.parametrize("B,D,V,wide,features", [(700, 128, 1300, False, True),
                                                  (1100, 64, 2100, True, True),
                                                  (520, 96, 1500, False, False)])
-def test_tcgen05_row_groups(B, D, V, wide, features):
-    # above 256 rows one launch serves up to four row groups of 256 whose CTAs walk the vocabulary
-    # tiles together: 3 groups (700), 4 groups then 1 (1100), 3 groups with a 8-row last one (520)
+def test_tcgen05_batches_above_256(B, D, V, wide, features):
+    # above 256 rows the tcgen05 path runs one launch per 256 rows: 3 launches (700), 5 (1100), and
+    # 3 with an 8-row last one (520)
     full_parity(_ragged(B, D, V, seed=B + V, wide=wide, features=features), lms.PATH_TCGEN05)
 
 
