@@ -1,5 +1,6 @@
 """Host-side logic of bench.py: the max-over-ranks reduction across replicas (gloo, world size
-2, CPU), the reference arm's JSON line, and the algorithmic byte count."""
+2, CPU), the reference arm's JSON line, the algorithmic byte count, and the rule that recorded ncu
+counters are used only on the kernel sources they were taken on."""
 import json
 import os
 import socket
@@ -63,3 +64,22 @@ def test_algorithmic_bytes_qwen_b64():
     b = bench.algorithmic_bytes(64, 4096, 151936, 1187)
     assert b == 151936 * 4096 * 2 + 64 * 4096 * 2 + 2 * 64 * 1187 * 8 + 64 * 28
     assert abs(b / 1e9 - 1.2464) < 1e-3
+
+
+def test_recorded_counters_follow_the_kernel_sources(tmp_path, monkeypatch):
+    # ncu records (DRAM bytes of the fused kernel, warp instructions of the ALU-bound workloads) are
+    # used only while they were taken on the current kernel sources
+    sys.path.insert(0, ROOT)
+    import bench
+    rec = bench.recorded_traffic("qwen3-8b", 64)
+    assert rec is not None and rec["kernel_source_hash"] == bench.kernel_source_hash()
+    assert rec["dram_bytes_per_launch"] == rec["dram_bytes_read"] + rec["dram_bytes_write"]
+    assert bench.recorded_traffic("qwen3-8b", 3) is None
+    for key, wl in (("logits/B=64/V=131072/bf16", "logits"), ("noise/B=64/V=151936", "noise")):
+        r = bench.recorded_instructions(key, wl)
+        assert r is not None and r["warp_inst_per_step"] == sum(k["warp_inst"] for k in r["kernels"].values())
+    # a changed source invalidates the records
+    fake = tmp_path / "noise_fill.cu"
+    fake.write_text("// another kernel\n")
+    monkeypatch.setitem(bench.ALU_SOURCES, "noise", [str(fake)])
+    assert bench.recorded_instructions("noise/B=64/V=151936", "noise") is None
