@@ -147,3 +147,41 @@ def test_verify_host_validation(L):
     nc, ncr = -(-151936 // 8192), -(-151936 // 4096)
     r256 = lambda x: -(-x // 256) * 256
     assert big == 3 * r256(64 * 9 * nc * 8 * 4) + r256(64 * 16) + 2 * r256(64 * ncr * 8) + r256(64 * 4)
+
+
+def test_topk_fp8_filtered_noalloc_host_validation(L):
+    INV, UNS, WS = lms.LMS_ERR_INVALID_ARG, lms.LMS_ERR_UNSUPPORTED, lms.LMS_ERR_WORKSPACE
+
+    def topk(k=4, D=64, H=FAKE, ws_bytes=1 << 24, p=None):
+        p = _params() if p is None else p
+        return L.lms_lmhead_sample_topk(H, 64, FAKE, 64, 4, D, 1000, k, ctypes.byref(p), FAKE, None,
+                                        FAKE, ws_bytes, None)
+    assert topk(k=0) == INV and topk(k=17) == INV
+    assert topk(D=60) == UNS and topk(H=ctypes.c_void_p(0x100008)) == UNS
+    assert topk(p=_params(path=lms.PATH_GEMV)) == UNS
+    assert topk(ws_bytes=L.lms_workspace_bytes_topk(4, 1000, 4) - 1) == WS
+
+    def fp8(w_scale=FAKE, D=64, ldw8=64, ws_bytes=1 << 24):
+        p = _params()
+        return L.lms_lmhead_sample_fp8(FAKE, 64, FAKE, ldw8, w_scale, 4, D, 1000, ctypes.byref(p), FAKE,
+                                       FAKE, ws_bytes, None)
+    assert fp8(w_scale=None) == INV
+    assert fp8(D=24, ldw8=24) == UNS                    # D must be a multiple of 16
+    assert fp8(ldw8=72) == UNS                          # ldw8 must be a multiple of 16
+    assert fp8(ws_bytes=16) == WS
+
+    def filtered(filters=True, k_max=1024, p=None, ld=0):
+        p = _params() if p is None else p
+        f = lms.FilterParams()
+        f.k_max = k_max
+        return L.lms_sample_from_logits_filtered(FAKE, 1, ld, 4, 1000, ctypes.byref(p),
+                                                 ctypes.byref(f) if filters else None, FAKE, None)
+    assert filtered(filters=False) == INV
+    assert filtered(k_max=1025) == INV and filtered(k_max=-1) == INV
+    assert filtered(p=_params(tile_v=256)) == INV
+    assert filtered(ld=999) == INV
+
+    # the allocation-free entry: B * ceil(V / 128) candidates beyond its static scratch are rejected
+    p = _params()
+    st = L.lms_lmhead_sample_noalloc(FAKE, 4096, FAKE, 4096, 65536, 4096, 151936, ctypes.byref(p), FAKE, None)
+    assert st == WS and b"static scratch" in L.lms_last_error()
