@@ -182,45 +182,66 @@ def max_over_ranks(x: float, device=None) -> float:
 # clocks during the timed region
 # ------------------------------------------------------------------------------------------
 class ClockSampler:
-    FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw",
+    """nvidia-smi sampling the SM clock, its maximum, power and the throttle reasons every 50 ms,
+    read on a thread as the lines arrive (each stamped with the host time it came in).  Started
+    before the workload is set up; the caller waits for the first sample before it times."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw",
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: int):
+        import threading
+        self.rows = []
+        self.first = threading.Event()
         self.proc = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + ",".join(self.FIELDS),
                  "--format=csv,noheader,nounits", "-lms", "50"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
 
-    def stop(self, t0: float, t1: float) -> dict:
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        rows = []
-        for r in csv.reader(io.StringIO(out)):
+    def _read(self):
+        for line in self.proc.stdout:
+            r = [x.strip() for x in line.split(",")]
             if len(r) < len(self.FIELDS):
                 continue
             try:
-                ts = time.mktime(time.strptime(r[0].strip().split(".")[0], "%Y/%m/%d %H:%M:%S"))
-                rows.append((ts, float(r[1]), float(r[2]), [x.strip() for x in r[4:8]]))
+                self.rows.append((time.time(), float(r[0]), float(r[1]), r[3:7]))
             except ValueError:
                 continue
-        inside = [x for x in rows if t0 - 1 <= x[0] <= t1 + 1]
-        window = "timed" if inside else "warmup+timed"
-        use = inside or rows
+            self.first.set()
+
+    def wait_first(self, timeout_s: float = 15.0):
+        if self.proc is not None:
+            self.first.wait(timeout_s)
+
+    def stop(self, t0: float, t1: float) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            self.proc.wait()
+        self.thread.join(timeout=5)
+        rows = list(self.rows)
+        # samples that came in during the timed region (a line arrives within one period of its
+        # sample); a short region may hold none, then those within a second of it
+        use = [x for x in rows if t0 <= x[0] <= t1 + 0.05]
+        window = "timed"
+        if not use:
+            use = [x for x in rows if t0 - 1.0 <= x[0] <= t1 + 1.0]
+            window = "within 1 s of the timed region (the region is shorter than the sampling period)"
         if not use:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for x in use for i, v in enumerate(x[3]) if v == "Active"})
+        reasons = sorted({self.NAMES[i] for x in use for i, v in enumerate(x[3]) if v == "Active"})
         return {"sm_mhz": statistics.median(x[1] for x in use), "sm_max_mhz": max(x[2] for x in use),
                 "reasons": reasons, "samples": len(use), "window": window}
 
@@ -290,18 +311,41 @@ def oracle_verify_time(tgt, dft, tokens, rows: int):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(w, target_s: float = 10.0):
-    import oracle  # noqa: F401  (test infrastructure: CPU baseline only)
-    threads = os.cpu_count() or 1
-    v = 1024
+def _scaled_oracle_us(w, threads: int, target_s: float):
+    """(us per full step, vocabulary rows timed, seconds) for the oracle's fused path on all B
+    rows: the first v rows of the vocabulary, v sized for about target_s seconds (the whole
+    vocabulary when it fits), scaled linearly to the full vocabulary."""
+    v = min(1024, w.V)
     t = oracle_sample_time(w, v, threads)
     v2 = int(min(w.V, max(v, v * target_s / max(t, 1e-3))))
-    v2 = max(128, v2 // 128 * 128)
+    v2 = w.V if v2 >= w.V else max(128, v2 // 128 * 128)
     t2 = oracle_sample_time(w, v2, threads)
-    us = t2 / v2 * w.V * 1e6
+    return t2 / v2 * w.V * 1e6, v2, t2
+
+
+def cpu_baseline(w, target_s: float = 10.0):
+    """The oracle on the host cores: all threads (the headline figure) and one thread, on a
+    bounded vocabulary slice of this workload, plus the small workloads it runs in full."""
+    import oracle  # noqa: F401  (test infrastructure: CPU baseline only)
+    from lm_head_gumbel_lmhead_gb300 import workloads
+    threads = os.cpu_count() or 1
+    us, v2, t2 = _scaled_oracle_us(w, threads, target_s)
+    us1, v1, t1 = _scaled_oracle_us(w, 1, target_s / 4)
+    full = {}
+    for name, wl in (("tiny B=4 D=512 V=8192", workloads.tiny()),
+                     ("qwen3-8b B=1", workloads.qwen3_8b(1)),
+                     ("qwen3-8b B=8", workloads.qwen3_8b(8))):
+        if wl.D != w.D and name.startswith("qwen"):
+            continue
+        full[name] = {"us_per_step_all_threads": round(oracle_sample_time(wl, wl.V, threads) * 1e6, 1)}
     return {"value": us, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"B={w.B} rows x first {v2} of {w.V} vocabulary rows (D={w.D}), fp64 GEMM + "
-                      f"Philox noise + argmax, {t2:.1f} s wall, scaled linearly to the full vocabulary"}
+                      f"Philox noise + argmax, {t2:.1f} s wall on {threads} threads"
+                      + ("" if v2 == w.V else ", scaled linearly to the full vocabulary"),
+            "single_thread": {"value": us1, "unit": UNIT, "cores": 1,
+                              "sample": f"B={w.B} rows x first {v1} of {w.V} vocabulary rows, "
+                                        f"{t1:.1f} s wall, scaled linearly to the full vocabulary"},
+            "full_workloads": full}
 
 
 def run_reference(args):
@@ -314,20 +358,34 @@ def run_reference(args):
         return
     w = make_workload(args.workload, args.batch, args.D, args.V)
     threads = os.cpu_count() or 1
-    v_slice = min(args.ref_vslice, w.V)
+    # each step runs the whole workload when all steps fit in the budget, else the first v_slice
+    # vocabulary rows, scaled linearly (the slice and its measured time are in the line)
+    probe_v = min(2048, w.V)
+    probe = oracle_sample_time(w, probe_v, threads)
+    est_full = probe / probe_v * w.V
+    v_slice = w.V
+    if est_full * args.steps > args.ref_budget_s:
+        v_slice = int(w.V * args.ref_budget_s / (est_full * args.steps))
+        v_slice = max(128, min(w.V, v_slice // 128 * 128))
     for _ in range(args.warmup):
         oracle_sample_time(w, min(v_slice, 512), threads)
     times = [oracle_sample_time(w, v_slice, threads) for _ in range(args.steps)]
-    us = statistics.mean(times) / v_slice * w.V * 1e6
+    step_s = statistics.mean(times)
+    us = step_s / v_slice * w.V * 1e6
+    config = {"workload": w.name, "B": w.B, "D": w.D, "V": w.V,
+              "noise": "wide53" if w.noise_mode else "fp32", "tile_v": 128,
+              "parallelism": "replicas" if ws > 1 else "single-gpu"}
+    sample = (f"each step: B={w.B} rows x all {w.V} vocabulary rows" if v_slice == w.V else
+              f"each step: B={w.B} rows x first {v_slice} of {w.V} vocabulary rows, scaled linearly "
+              f"to the full vocabulary")
     line = {"impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "D": w.D, "V": w.V,
-                       "noise": "wide53" if w.noise_mode else "fp32", "parallelism": "replicas"},
+            "data": "synthetic", "config": config,
+            "measured_seconds_per_step": step_s, "vocab_rows_per_step": v_slice,
+            "extrapolated_from_v": None if v_slice == w.V else v_slice,
             "cpu_baseline": {"value": us, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": f"each step: B={w.B} rows x first {v_slice} of {w.V} "
-                                       f"vocabulary rows, scaled linearly to the full vocabulary"},
+                             "sample": sample},
             "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -387,7 +445,9 @@ def run_gpu(args):
     peaks = measured_peaks()
     B = args.batch
     extra = {}
-    sampler = None
+    # the clock sampler starts before the workload is set up, so that it runs by the time the
+    # timed region starts, and keeps sampling through the e2e phase
+    sampler = ClockSampler(local) if rank == 0 else None
     alu_key = None                                 # key of the ALU-bound workloads' ncu record
 
     if args.workload in FUSED:
@@ -552,10 +612,9 @@ def run_gpu(args):
         config["l2"] = "inputs %.0f MB; a 256 MB buffer written between timed steps" % (alg / 1e6)
     elif "l2" not in config:
         config["l2"] = "inputs %.0f MB, larger than L2, no flush" % (alg / 1e6)
-    if rank == 0:
-        sampler = ClockSampler(local)
+    if sampler is not None:
+        sampler.wait_first()
     avg_ms, per_ms, t0, t1 = _time_steps(step, args.warmup, args.steps, dev, stream, flush=flush)
-    clocks = sampler.stop(t0, t1) if sampler else None
     ms_per_step = max_over_ranks(avg_ms, dev)
     us = ms_per_step * 1e3
 
@@ -563,8 +622,10 @@ def run_gpu(args):
     if args.workload in FUSED:
         # e2e: the step's per-request inputs from pinned host memory, the tokens back to pinned
         # host memory; W is a resident weight.  The inputs of a step (H, T, seeds, positions and
-        # the optional bias and mask) sit in one pinned staging block and go over in one copy;
-        # a ring of blocks lets the host write step i's positions while earlier copies run.
+        # the optional bias and mask) sit in one pinned staging block and go over in one copy.
+        # The copies run on a copy stream: step i's inputs go over while step i-1's kernels run,
+        # and step i's tokens come back while step i+1's run.  Device inputs and outputs are
+        # double-buffered; events order every reuse.
         host = {"H": w.H, "T": w.temperature, "seeds": w.seeds, "positions": w.positions}
         if w.bias is not None:
             host["bias"] = w.bias
@@ -585,34 +646,71 @@ def run_gpu(args):
         for blk in stage:
             for k, v in host.items():
                 view(blk, k).copy_(v)
-        staged = [torch.cuda.Event() for _ in range(ring)]
-        dblk = torch.empty(total, dtype=torch.uint8, device=dev)
-        devb = {k: view(dblk, k) for k in host}
+        copy_stream = torch.cuda.Stream(dev)
+        h2d_done = [torch.cuda.Event() for _ in range(ring)]      # pinned block i % ring read
+        dblk = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
+        devb = [{k: view(b, k) for k in host} for b in dblk]
+        outs = [torch.empty_like(out) for _ in range(2)]
+        ready = [torch.cuda.Event() for _ in range(2)]            # inputs of the slot landed
+        computed = [torch.cuda.Event() for _ in range(2)]         # the slot's kernels finished
+        fetched = [torch.cuda.Event() for _ in range(2)]          # the slot's tokens are back
         pos_h = pos_all.cpu()
-        out_h = torch.empty(tuple(out.shape), dtype=torch.int64).pin_memory()
+        out_h = [torch.empty(tuple(out.shape), dtype=torch.int64).pin_memory() for _ in range(ring)]
+        for ev in computed + fetched:
+            ev.record(stream)
 
         def e2e_step(i):
-            blk = stage[i % ring]
-            staged[i % ring].synchronize()        # the copy that last read this block is done
+            j, slot = i % ring, i % 2
+            blk = stage[j]
+            h2d_done[j].synchronize()              # the copy that last read this block is done
             view(blk, "positions").copy_(pos_h[i])
-            dblk.copy_(blk, non_blocking=True)
-            staged[i % ring].record(stream)
-            ekw = dict(temperature=devb["T"], seeds=devb["seeds"], positions=devb["positions"],
-                       bias=devb.get("bias"), mask=devb.get("mask"), base_seed=w.base_seed,
-                       offset=w.offset, wide=wide, out=out, workspace=workspace)
+            with torch.cuda.stream(copy_stream):
+                copy_stream.wait_event(computed[slot])   # step i-2's kernels read this slot
+                dblk[slot].copy_(blk, non_blocking=True)
+                h2d_done[j].record(copy_stream)
+                ready[slot].record(copy_stream)
+            stream.wait_event(ready[slot])
+            stream.wait_event(fetched[slot])       # step i-2's tokens have left this slot
+            b = devb[slot]
+            ekw = dict(temperature=b["T"], seeds=b["seeds"], positions=b["positions"],
+                       bias=b.get("bias"), mask=b.get("mask"), base_seed=w.base_seed,
+                       offset=w.offset, wide=wide, out=outs[slot], workspace=workspace)
             if fp8:
-                lms.lmhead_sample_fp8(devb["H"], W8, wsc, **ekw)
+                lms.lmhead_sample_fp8(b["H"], W8, wsc, **ekw)
             elif topk:
-                lms.lmhead_sample_topk(devb["H"], W, topk, scores=scores_k, **ekw)
+                lms.lmhead_sample_topk(b["H"], W, topk, scores=scores_k, **ekw)
             else:
-                lms.lmhead_sample(devb["H"], W, **ekw)
-            out_h.copy_(out, non_blocking=True)
+                lms.lmhead_sample(b["H"], W, **ekw)
+            computed[slot].record(stream)
+            with torch.cuda.stream(copy_stream):
+                copy_stream.wait_event(computed[slot])
+                out_h[j].copy_(outs[slot], non_blocking=True)
+                fetched[slot].record(copy_stream)
 
-        e2e_ms, _, _, _ = _time_steps(e2e_step, args.warmup, args.steps, dev, stream)
+        def e2e_time(n_warm, n_steps):
+            for i in range(n_warm):
+                e2e_step(i)
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            barrier()
+            torch.cuda.synchronize(dev)
+            e0.record(stream)
+            for k in range(n_steps):
+                e2e_step(n_warm + k)
+            stream.wait_event(fetched[(n_warm + n_steps - 1) % 2])   # the last tokens are back
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            barrier()
+            return e0.elapsed_time(e1) / n_steps
+
+        e2e_ms = e2e_time(args.warmup, args.steps)
         e2e = {"value": round(max_over_ranks(e2e_ms, dev) * 1e3, 2), "unit": UNIT,
                "h2d_bytes_per_step": total,
-               "d2h_bytes_per_step": out.numel() * 8}
+               "d2h_bytes_per_step": out.numel() * 8,
+               "copies": "pinned host <-> device on a copy stream, overlapped with the previous "
+                         "and next steps' kernels"}
 
+    clocks = sampler.stop(t0, t1) if sampler else None
     if rank != 0:
         return
     achieved_gbs = alg / (us * 1e-6) / 1e9
@@ -709,7 +807,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--ref-vslice", type=int, default=4096)
+    ap.add_argument("--ref-budget-s", type=float, default=120.0,
+                    help="seconds of oracle time the reference arm's timed steps may take")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -21,12 +21,20 @@
  *    masked / out-of-range entries are -inf.
  *
  * Exact definitions used by every entry point (identical on all paths):
- *   key/counter  seeded row b (seeds[b] >= 0): key = (seed lo32, seed hi32),
- *                counter = (v, pos lo32, pos hi32, 0); unseeded row b: key = (base_seed lo32,
- *                base_seed hi32), counter = (v, offset lo32, offset hi32, 0x80000000 | b).
- *   Philox       Philox4x32, 10 rounds (Salmon et al., SC'11); words w0..w3.
- *   uniform      FP32 noise: k = w0 >> 8, u = (k + 1/2) / 2^24.
- *                WIDE53 noise: k = ((w1 << 32) | w0) >> 12, u = (k + 1/2) / 2^52.
+ *   Philox       Philox4x32, 10 rounds (Salmon et al., SC'11): call(key, counter) -> words
+ *                w0..w3.  key = (k0, k1), counter = (c0, c1, c2, c3), all 32-bit.
+ *   key/counter  seeded row b (seeds[b] >= 0): key = (seed lo32, seed hi32), and call n has
+ *                counter (n, pos lo32, pos hi32, 0) with pos = positions[b]; unseeded row b:
+ *                key = (base_seed lo32, base_seed hi32), and call n has counter
+ *                (n, offset lo32, offset hi32, 0x80000000 | b), b the row's index in the call.
+ *   entry words  one call serves several consecutive vocabulary entries, and no word is
+ *                dropped.  FP32 noise: entry v takes word w[v & 3] of call n = v >> 2.
+ *                WIDE53 noise: entry v takes lo = w[2 (v & 1)] and hi = w[2 (v & 1) + 1] of
+ *                call n = v >> 1.  The variate of entry v is thus a function of (key, counter
+ *                words 1..3, v) alone: a seeded row's noise depends on (seed, position, v), not
+ *                on the row's place in the batch.
+ *   uniform      FP32 noise: k = w >> 8 (w the entry's word), u = (k + 1/2) / 2^24 = (2k + 1) / 2^25.
+ *                WIDE53 noise: k = ((hi << 32) | lo) >> 12, u = (k + 1/2) / 2^52 = (2k + 1) / 2^53.
  *   noise        E = -log u, g = -log E (computed in fp32 from exact integer-derived u or 1 - u).
  *   transform    masked -> -inf; T == 0 -> s = y + bias (greedy, no noise);
  *                T > 0 -> s = (y + bias) / T + g;  NaN scores count as -inf.
@@ -57,13 +65,16 @@ typedef enum {
     LMS_ERR_INVALID_ARG = 1,  /* null required pointer, size <= 0 or too large, bad enum value */
     LMS_ERR_UNSUPPORTED = 2,  /* alignment / shape the kernels do not handle (see each call)    */
     LMS_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than lms_workspace_bytes()           */
-    LMS_ERR_CUDA = 4          /* a CUDA runtime / driver call failed (message in last_error)   */
+    LMS_ERR_CUDA = 4,         /* a CUDA runtime / driver call failed (message in last_error)   */
+    LMS_ERR_TIMEOUT = 5       /* lms_read_status only: a device-side wait of the call ran out
+                                 of time (some row ended with status 3)                       */
 } lms_status;
 
 typedef enum { LMS_NOISE_FP32 = 0, LMS_NOISE_WIDE53 = 1 } lms_noise_mode;
 typedef enum { LMS_DTYPE_F32 = 0, LMS_DTYPE_BF16 = 1 } lms_dtype;
 typedef enum {
-    LMS_NOISE_OUT_WORDS = 0,      /* uint32 [B][V][4]: the four Philox words                   */
+    LMS_NOISE_OUT_WORDS = 0,      /* uint32 [B][V][4]: the four words of the Philox call entry v
+                                     draws from (entries served by one call repeat them)       */
     LMS_NOISE_OUT_UNIFORM = 1,    /* double [B][V]: u, exact                                    */
     LMS_NOISE_OUT_EXPONENTIAL = 2,/* float  [B][V]: E = -log u as the sampling kernels compute it */
     LMS_NOISE_OUT_GUMBEL = 3      /* float  [B][V]: g = -log E as the sampling kernels compute it */
@@ -127,10 +138,24 @@ lms_status lms_tile_info(int32_t op, int64_t B, int64_t D, int64_t V, int32_t ti
                          int32_t* tile_v_out, int64_t* n_tiles_out, size_t* workspace_bytes_out,
                          int32_t* path_out);
 
-/* Workspace bytes for a call of these sizes (0 if the sizes are invalid).  Layout, for tests
- * that read the Stage-1 candidates: float score[B][nt] at offset 0, then int32 index[B][nt]
- * at offset round_up(4*B*nt, 256).  index -1 = tile had no entry above -inf. */
+/* Workspace bytes for a call of these sizes (0 if the sizes are invalid).  Every workspace (of
+ * every entry point that takes one) starts with a 256-byte status block: uint32 status word at
+ * offset 0 (see lms_read_status), the rest reserved.  Then, for LMS_OP_LMHEAD and LMS_OP_LOGITS,
+ * for tests that read the Stage-1 candidates: float score[B][nt] at offset 256, then int32
+ * index[B][nt] at offset 256 + round_up(4*B*nt, 256).  index -1 = tile had no entry above -inf.
+ * Nothing in a workspace has to be initialised by the caller. */
 size_t lms_workspace_bytes(int32_t op, int64_t B, int64_t D, int64_t V, int32_t tile_v_req);
+
+/* The status of the last call that used `workspace` (any entry point that takes a workspace),
+ * for callers that pass row_status = NULL.  Synchronises `stream` (the call's stream), then reads
+ * the status word that the call left at the head of the workspace: bit s is set when at least
+ * one row ended with row status s (1 no finite score, 2 invalid T, 3 a device-side wait ran out);
+ * 0 when every row is OK.  *status_bits receives the word (status_bits may be NULL).  Returns
+ * LMS_ERR_TIMEOUT when bit 3 is set, LMS_OK otherwise (LMS_ERR_CUDA if the synchronisation or
+ * the 4-byte copy fails).  Allocates nothing.  (FlashSampling "Limitations": the kernel assumes
+ * at least one finite logit per row; status 1 reports a row without one, and this call lets a
+ * caller without a row_status buffer see it.) */
+lms_status lms_read_status(const void* workspace, void* stream, uint32_t* status_bits);
 
 /* Fused LM-head projection + Gumbel-max sampling (FlashSampling Stage 1 + Stage 2).
  *   H   bf16 [B][ldh] hidden states (row-major), W bf16 [V][ldw] LM-head weight (row-major, the
@@ -154,9 +179,9 @@ lms_status lms_lmhead_sample(const void* H, int64_t ldh, const void* W, int64_t 
  *           (ties to even).  The power-of-two scale makes the scaling exact.
  * Logits y[b][v] = 2^e_b * w_scale[v] * sum_d E4M3(H8[b][d]) E4M3(W8[v][d]) (tcgen05.mma
  * kind::f8f6f4, fp32 accumulation); everything after that is lms_lmhead_sample's.  W streams at
- * one byte per weight.  Workspace (lms_workspace_bytes(LMS_OP_LMHEAD_FP8, ...)): the candidates,
- * then the quantised activations [B][round_up(D, 16)] bytes, then e_b int32 [B], each at a
- * 256-byte aligned offset.  Requirements: D % 16 == 0, ldw8 >= D and % 16 == 0, ldh as for
+ * one byte per weight.  Workspace (lms_workspace_bytes(LMS_OP_LMHEAD_FP8, ...)): the status block
+ * and the candidates as for lms_lmhead_sample, then the quantised activations [B][round_up(D, 16)]
+ * bytes, then e_b int32 [B], each at a 256-byte aligned offset.  Requirements: D % 16 == 0, ldw8 >= D and % 16 == 0, ldh as for
  * lms_lmhead_sample, H and W8 16-byte aligned; path AUTO or TCGEN05. */
 lms_status lms_lmhead_sample_fp8(const void* H, int64_t ldh, const void* W8, int64_t ldw8,
                                  const float* w_scale, int64_t B, int64_t D, int64_t V,
@@ -172,9 +197,10 @@ lms_status lms_lmhead_sample_fp8(const void* H, int64_t ldh, const void* W8, int
  *   k        1 <= k <= LMS_TOPK_MAX
  *   out      int64 [B][k] (device): vocabulary indices; -1 past a row's finite scores
  *   scores   fp32 [B][k] (device) or NULL: the perturbed scores (-inf where out is -1)
- *   workspace  lms_workspace_bytes_topk(B, V, k) bytes: ordered key lists, one per row, tile
- *              and quarter of the tile's 128 rows, uint64 [B][ceil(V / 128)][4][k]; then, at
- *              the next 256-byte boundary, Stage 2's per-row part lists uint64 [B][32][k]
+ *   workspace  lms_workspace_bytes_topk(B, V, k) bytes: the 256-byte status block; ordered key
+ *              lists, one per row, tile and quarter of the tile's 128 rows,
+ *              uint64 [B][ceil(V / 128)][4][k]; then, at the next 256-byte boundary, Stage 2's
+ *              per-row part lists uint64 [B][32][k]
  * Row statuses as for lms_lmhead_sample (1: no finite score, 2: invalid T, 3: a bounded wait ran
  * out).  Requirements as for lms_lmhead_sample; path AUTO or TCGEN05 (bf16 H and W). */
 #define LMS_TOPK_MAX 16
@@ -237,9 +263,16 @@ typedef struct {
     int32_t reserved;           /* must be 0 */
 } lms_filter_params;
 
-/* The filtered race over materialised logits [B][ld] (fp32 or bf16; ld == 0 broadcasts one row):
- * one CTA per row selects (radix select), sorts (bitonic, in shared memory) and cuts the
- * candidates, then races them.  out int64 [B] (-1 when row status != 0); no workspace.
+/* The filtered race over materialised logits [B][ld] (fp32 or bf16; ld == 0 broadcasts one row).
+ * One thread-block cluster per row (up to 16 CTAs of 512 threads; CTA c owns one contiguous
+ * slice of the row): each CTA keys its slice's t = (y + bias) / T in shared memory, the cluster
+ * finds the top-k boundary by a radix select over histograms merged through distributed shared
+ * memory, every CTA appends its surviving entries to the leader CTA, and the leader cuts top-p
+ * (a radix select over exact fixed-point masses) and min-p (a threshold) and races what is left.
+ * Nothing is sorted.  The leader's candidate list holds at most 2048 entries: the k_max best, or
+ * the entries above the bin of the k-th one plus that whole bin when it holds at most 256 (ties
+ * at the k-th value are then ranked among themselves).  out int64 [B] (-1 when row status != 0);
+ * statuses through params->row_status only (no workspace).
  * Requirements: 1 <= B < 2^31, 1 <= V < 2^31. */
 lms_status lms_sample_from_logits_filtered(const void* logits, int32_t dtype, int64_t ld, int64_t B,
                                            int64_t V, const lms_sample_params* params,
@@ -254,11 +287,15 @@ lms_status lms_sample_from_logits_filtered(const void* logits, int32_t dtype, in
  * candidates go to a 4 MiB file-scope device array that is part of the library image (every
  * GPU that loads the library holds it until the process exits), so B * ceil(V / 128) must be
  * <= 524288; larger calls return LMS_ERR_WORKSPACE before any launch.  Calls no cudaMalloc,
- * cudaFree or allocating library routine.  The first call on each device looks up the array's
- * device address (cudaGetSymbolAddress, with that device current): make that first call before
- * any stream capture.  Every call shares the array and leaves its candidates in it; nothing in
- * it has to start at zero (each call writes every candidate it reads), but calls whose kernels
- * overlap on the GPU (concurrent streams or threads) race on it: serialise them. */
+ * cudaFree or allocating library routine.  Each call made outside stream capture looks up the
+ * array's device address (cudaGetSymbolAddress, with the call's device current), so a module
+ * reloaded at a new address after cudaDeviceReset or in another context is picked up; calls made
+ * while `stream` is capturing use the address the last uncaptured call on that device found, so
+ * make a first call on each device (and again after a device reset or a context switch) before
+ * any stream capture -- a captured first call returns LMS_ERR_CUDA.  Every call shares the array
+ * and leaves its candidates in it; nothing in it has to start at zero (each call writes every
+ * candidate it reads), but calls whose kernels overlap on the GPU (concurrent streams or threads)
+ * race on it: serialise them.  Row statuses come through params->row_status only. */
 lms_status lms_lmhead_sample_noalloc(const void* H, int64_t ldh, const void* W, int64_t ldw,
                                      int64_t B, int64_t D, int64_t V,
                                      const lms_sample_params* params, int64_t* out, void* stream);

@@ -22,7 +22,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "liblms.so")
 
-LMS_OK, LMS_ERR_INVALID_ARG, LMS_ERR_UNSUPPORTED, LMS_ERR_WORKSPACE, LMS_ERR_CUDA = range(5)
+LMS_OK, LMS_ERR_INVALID_ARG, LMS_ERR_UNSUPPORTED, LMS_ERR_WORKSPACE, LMS_ERR_CUDA, LMS_ERR_TIMEOUT = range(6)
 NOISE_FP32, NOISE_WIDE53 = 0, 1
 DTYPE_F32, DTYPE_BF16 = 0, 1
 OP_LMHEAD, OP_LOGITS, OP_LMHEAD_FP8 = 0, 1, 2
@@ -117,6 +117,8 @@ def lib() -> ctypes.CDLL:
             L.lms_verify_from_logits.restype = i32
             L.lms_philox_fill_noise.argtypes = [P, i32, i32, i64, i64, P, P, u64, u64, P]
             L.lms_philox_fill_noise.restype = i32
+            L.lms_read_status.argtypes = [P, P, P]
+            L.lms_read_status.restype = i32
             _lib = L
     return _lib
 
@@ -169,14 +171,28 @@ def workspace_bytes(op: int, B: int, D: int, V: int, tile_v: int = 0) -> int:
     return int(lib().lms_workspace_bytes(op, B, D, V, tile_v))
 
 
+STATUS_BLOCK_BYTES = 256   # every workspace starts with the call's status word
+
+
 def split_workspace(ws: torch.Tensor, B: int, n_tiles: int):
     """Views of the Stage-1 candidates in a workspace: (score f32 [B, nt], index i32 [B, nt])."""
     n = B * n_tiles
-    off = (4 * n + 255) // 256 * 256
+    off = STATUS_BLOCK_BYTES + (4 * n + 255) // 256 * 256
     raw = ws.view(torch.uint8)
-    score = raw[: 4 * n].view(torch.float32).view(B, n_tiles)
+    score = raw[STATUS_BLOCK_BYTES: STATUS_BLOCK_BYTES + 4 * n].view(torch.float32).view(B, n_tiles)
     index = raw[off: off + 4 * n].view(torch.int32).view(B, n_tiles)
     return score, index
+
+
+def read_status(workspace: torch.Tensor, stream=None):
+    """(lms_status, status_bits) of the last call that used `workspace`: synchronises the stream
+    and reads the status word (bit s set when some row ended with row status s).  Returns
+    LMS_ERR_TIMEOUT as the status when a device-side wait ran out; raises on other errors."""
+    bits = ctypes.c_uint32(0)
+    st = lib().lms_read_status(_ptr(workspace), _stream(stream), ctypes.byref(bits))
+    if st not in (LMS_OK, LMS_ERR_TIMEOUT):
+        _check(st)
+    return st, bits.value
 
 
 def _params(B, device, temperature, seeds, positions, bias, mask, base_seed, offset, wide, tile_v,
@@ -319,7 +335,7 @@ def split_workspace_fp8(ws: torch.Tensor, B: int, D: int, n_tiles: int):
     of an FP8-path workspace."""
     score, index = split_workspace(ws, B, n_tiles)
     n = B * n_tiles
-    off = 2 * ((4 * n + 255) // 256 * 256)
+    off = STATUS_BLOCK_BYTES + 2 * ((4 * n + 255) // 256 * 256)
     ldq = (D + 15) // 16 * 16
     raw = ws.view(torch.uint8)
     q = raw[off: off + B * ldq].view(B, ldq)

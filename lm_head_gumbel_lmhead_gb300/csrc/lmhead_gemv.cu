@@ -38,6 +38,7 @@ __global__ void __launch_bounds__(kThreads) lmhead_gemv_kernel(const uint16_t* _
     const int B = static_cast<int>(a.B);
     const int tile = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    clear_status_bits(a.status_bits, a.row0);
 
     // Stage H (B rows of D bf16) into shared memory, 16 bytes at a time.
     const int chunks_per_row = D / 8;

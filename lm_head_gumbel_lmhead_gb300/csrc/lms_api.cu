@@ -35,6 +35,10 @@ constexpr int kTcMaxBatchPerLaunch = 256;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Every workspace starts with a status block: the call's status word (bit s set when a row ended
+// with row status s != 0), then reserved bytes up to a 256-byte boundary.
+constexpr size_t kStatusBlock = 256;
+
 struct Tiling {
     int32_t tile_v;
     int64_t n_tiles;
@@ -86,7 +90,7 @@ lms_status make_tiling(int32_t op, int64_t B, int64_t D, int64_t V, int32_t tile
     if (op == LMS_OP_LOGITS && grid > (int64_t{1} << 31) - 1)
         return fail(LMS_ERR_UNSUPPORTED, "B * n_tiles exceeds the launch grid limit");
     const size_t cand = static_cast<size_t>(B) * static_cast<size_t>(out->n_tiles) * 4;
-    out->workspace = round_up(cand, 256) + round_up(cand, 256);
+    out->workspace = kStatusBlock + round_up(cand, 256) + round_up(cand, 256);
     if (op == LMS_OP_LMHEAD_FP8) {
         // + quantised activations [B][round_up(D, 16)] bytes + their exponents [B]
         out->workspace += round_up(static_cast<size_t>(B) * round_up(static_cast<size_t>(D), 16), 256) +
@@ -130,8 +134,10 @@ lms::SampleArgs make_args(const lms_sample_params* p, int64_t B, int64_t V, cons
     a.V = V;
     a.n_tiles = t.n_tiles;
     const size_t cand = static_cast<size_t>(B) * static_cast<size_t>(t.n_tiles) * 4;
-    a.cand_score = static_cast<float*>(workspace);
-    a.cand_index = reinterpret_cast<int*>(static_cast<char*>(workspace) + round_up(cand, 256));
+    char* w = static_cast<char*>(workspace);
+    a.status_bits = reinterpret_cast<uint32_t*>(w);
+    a.cand_score = reinterpret_cast<float*>(w + kStatusBlock);
+    a.cand_index = reinterpret_cast<int*>(w + kStatusBlock + round_up(cand, 256));
     a.h_exp = nullptr;
     a.w_scale = nullptr;
     return a;
@@ -290,7 +296,7 @@ lms_status lms_lmhead_sample(const void* H, int64_t ldh, const void* W, int64_t 
         }
     }
     e = lms::launch_stage2(a.cand_score, a.cand_index, t.n_tiles, B, params->temperature, out,
-                           params->row_status, s);
+                           params->row_status, a.status_bits, s);
     if (e != cudaSuccess) return cuda_fail(e, "Stage-2 launch");
     return LMS_OK;
 }
@@ -299,7 +305,8 @@ size_t lms_workspace_bytes_topk(int64_t B, int64_t V, int32_t k) {
     if (B <= 0 || V <= 0 || V > kMaxV || k < 1 || k > LMS_TOPK_MAX) return 0;
     const int64_t nt = (V + LMS_FUSED_TILE_V - 1) / LMS_FUSED_TILE_V;
     // per row and tile, one ordered list of k keys per TMEM quadrant (4); then Stage 2's part lists
-    return round_up(static_cast<size_t>(B) * static_cast<size_t>(nt) * 4 * static_cast<size_t>(k) * 8, 256) +
+    return kStatusBlock +
+           round_up(static_cast<size_t>(B) * static_cast<size_t>(nt) * 4 * static_cast<size_t>(k) * 8, 256) +
            round_up(lms::stage2_topk_part_bytes(B, k), 256);
 }
 
@@ -331,7 +338,7 @@ lms_status lms_lmhead_sample_topk(const void* H, int64_t ldh, const void* W, int
     lms::SampleArgs a = make_args(params, B, V, t, workspace);
     a.cand_score = nullptr;
     a.cand_index = nullptr;
-    a.cand_keys = static_cast<unsigned long long*>(workspace);
+    a.cand_keys = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + kStatusBlock);
     a.topk = k;
     CUtensorMap tmW;
     if ((st = encode_bf16_map(&tmW, W, V, D, ldw, 128)) != LMS_OK) return st;
@@ -350,10 +357,10 @@ lms_status lms_lmhead_sample_topk(const void* H, int64_t ldh, const void* W, int
         if (e != cudaSuccess) return cuda_fail(e, "tcgen05 top-k Stage-1 launch");
     }
     unsigned long long* part = reinterpret_cast<unsigned long long*>(
-        static_cast<char*>(workspace) +
+        static_cast<char*>(workspace) + kStatusBlock +
         round_up(static_cast<size_t>(B) * static_cast<size_t>(t.n_tiles) * 4 * static_cast<size_t>(k) * 8, 256));
     const cudaError_t e = lms::launch_stage2_topk(a.cand_keys, 4 * t.n_tiles, k, B, params->temperature,
-                                                  out, scores, params->row_status, part, s);
+                                                  out, scores, params->row_status, a.status_bits, part, s);
     if (e != cudaSuccess) return cuda_fail(e, "top-k Stage-2 launch");
     return LMS_OK;
 }
@@ -373,7 +380,7 @@ struct VerifyLayout {
         dec = round_up(static_cast<size_t>(B) * sizeof(lms::VerifyDecision), 256);
         cand = round_up(static_cast<size_t>(B) * static_cast<size_t>(ncr32) * 2 * 4, 256);  // c_s, c_i
         cnt = round_up(static_cast<size_t>(B) * 4, 256);                // cnt_r
-        total = 3 * part + dec + 2 * cand + cnt;
+        total = kStatusBlock + 3 * part + dec + 2 * cand + cnt;
     }
 };
 constexpr int kVerifyMaxK = 32;
@@ -405,8 +412,9 @@ lms_status lms_verify_from_logits(const void* target, const void* draft, int32_t
     const VerifyLayout L(B, k, V, dtype == LMS_DTYPE_BF16);
     if (workspace == nullptr || workspace_bytes < L.total)
         return fail(LMS_ERR_WORKSPACE, "workspace of %zu bytes needed", L.total);
-    char* w = static_cast<char*>(workspace);
+    char* w = static_cast<char*>(workspace) + kStatusBlock;
     lms::VerifyArgs a;
+    a.status_bits = static_cast<uint32_t*>(workspace);
     a.target = target;
     a.draft = draft;
     a.ld = ld;
@@ -463,7 +471,7 @@ lms_status lms_lmhead_sample_fp8(const void* H, int64_t ldh, const void* W8, int
     lms::SampleArgs a = make_args(params, B, V, t, workspace);
     const size_t cand = static_cast<size_t>(B) * static_cast<size_t>(t.n_tiles) * 4;
     const int64_t ldq = static_cast<int64_t>(round_up(static_cast<size_t>(D), 16));
-    uint8_t* q = static_cast<uint8_t*>(workspace) + 2 * round_up(cand, 256);
+    uint8_t* q = static_cast<uint8_t*>(workspace) + kStatusBlock + 2 * round_up(cand, 256);
     int32_t* h_exp = reinterpret_cast<int32_t*>(q + round_up(static_cast<size_t>(B) * ldq, 256));
     a.h_exp = h_exp;
     a.w_scale = w_scale;
@@ -487,7 +495,7 @@ lms_status lms_lmhead_sample_fp8(const void* H, int64_t ldh, const void* W8, int
         if (e != cudaSuccess) return cuda_fail(e, "tcgen05 FP8 Stage-1 launch");
     }
     e = lms::launch_stage2(a.cand_score, a.cand_index, t.n_tiles, B, params->temperature, out,
-                           params->row_status, s);
+                           params->row_status, a.status_bits, s);
     if (e != cudaSuccess) return cuda_fail(e, "Stage-2 launch");
     return LMS_OK;
 }
@@ -514,7 +522,7 @@ lms_status lms_sample_from_logits(const void* logits, int32_t dtype, int64_t ld,
                                               params->noise_mode == LMS_NOISE_WIDE53, a, s);
     if (e != cudaSuccess) return cuda_fail(e, "logits Stage-1 launch");
     e = lms::launch_stage2(a.cand_score, a.cand_index, t.n_tiles, B, params->temperature, out,
-                           params->row_status, s);
+                           params->row_status, a.status_bits, s);
     if (e != cudaSuccess) return cuda_fail(e, "Stage-2 launch");
     return LMS_OK;
 }
@@ -586,6 +594,21 @@ lms_status lms_philox_fill_noise(void* out, int32_t kind, int32_t noise_mode, in
     const cudaError_t e = lms::launch_noise_fill(out, kind, noise_mode == LMS_NOISE_WIDE53, B, V, seeds,
                                                  positions, base_seed, offset, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "noise-fill launch");
+    return LMS_OK;
+}
+
+lms_status lms_read_status(const void* workspace, void* stream, uint32_t* status_bits) {
+    g_last_error[0] = '\0';
+    if (workspace == nullptr) return fail(LMS_ERR_INVALID_ARG, "workspace is required");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "lms_read_status: stream synchronisation");
+    uint32_t bits = 0;
+    e = cudaMemcpy(&bits, workspace, sizeof bits, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "lms_read_status: status copy");
+    if (status_bits) *status_bits = bits;
+    if (bits & (1u << LMS_ROW_DEVICE_TIMEOUT))
+        return fail(LMS_ERR_TIMEOUT, "a device-side wait ran out of time (row status 3)");
     return LMS_OK;
 }
 

@@ -326,6 +326,18 @@ __device__ __forceinline__ int candidate_index(float s, int i) {
 // Index written by a CTA whose device-side wait ran out of time.
 constexpr int kPoisonIndex = -2;
 
+// The call's status word: bit s is set when some row of the call ended with row status s != 0.
+// Stage 1 of the call's first launch clears it (block 0, thread 0 of the launch that starts at
+// row 0: stream order puts it after the previous call's Stage 2); Stage 2 sets the bits.
+__device__ __forceinline__ void clear_status_bits(uint32_t* bits, int64_t row0) {
+    if (bits != nullptr && row0 == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 &&
+        threadIdx.x == 0)
+        *bits = 0u;
+}
+__device__ __forceinline__ void note_row_status(uint32_t* bits, int status) {
+    if (bits != nullptr && status != 0) atomicOr(bits, 1u << status);
+}
+
 // Programmatic dependent launch: let the dependent grid start launching / wait for the primary.
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -31,6 +31,9 @@ struct SampleArgs {
     // and TMEM quadrant
     unsigned long long* cand_keys = nullptr;
     int topk = 0;
+    // the call's status word (the head of the workspace) or null: Stage 1 of the launch with
+    // row0 == 0 clears it, Stage 2 sets bit s for every row that ends with status s != 0
+    uint32_t* status_bits = nullptr;
 };
 
 // Speculative-decoding verification over materialised logits (see verify.cu).
@@ -67,6 +70,7 @@ struct VerifyArgs {
     int64_t* accept_len;       // [B]
     int64_t* out;              // [B][k + 1]
     int32_t* row_status;       // [B] or null
+    uint32_t* status_bits;     // the call's status word (cleared by the first partials launch)
 };
 
 void verify_chunks(int64_t V, bool bf16, int64_t* partial_chunks, int64_t* race_chunks);
@@ -98,7 +102,7 @@ cudaError_t launch_logits_stage1(const void* logits, bool bf16, int64_t ld, int 
 
 cudaError_t launch_stage2(const float* cand_score, const int* cand_index, int64_t n_tiles,
                           int64_t B, const float* temperature, int64_t* out, int32_t* row_status,
-                          cudaStream_t stream);
+                          uint32_t* status_bits, cudaStream_t stream);
 
 // Stage 2 of Gumbel-top-k: per row, the k best of n_lists ordered key lists of k keys
 // (cand_keys [B][n_lists][k]); out [B][k] indices (-1 past the finite ones), scores [B][k] or null.
@@ -106,7 +110,8 @@ cudaError_t launch_stage2(const float* cand_score, const int* cand_index, int64_
 size_t stage2_topk_part_bytes(int64_t B, int k);
 cudaError_t launch_stage2_topk(const unsigned long long* cand_keys, int64_t n_lists, int k, int64_t B,
                                const float* temperature, int64_t* out, float* scores,
-                               int32_t* row_status, unsigned long long* part_keys, cudaStream_t stream);
+                               int32_t* row_status, uint32_t* status_bits,
+                               unsigned long long* part_keys, cudaStream_t stream);
 
 cudaError_t launch_lmhead_gemv(const uint16_t* H, int64_t ldh, const uint16_t* W, int64_t ldw,
                                int64_t D, bool wide, const SampleArgs& a, cudaStream_t stream);

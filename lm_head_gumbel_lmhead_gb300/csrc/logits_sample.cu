@@ -46,6 +46,7 @@ __global__ void __launch_bounds__(kThreads) logits_stage1_kernel(const T* __rest
     const int64_t b = cta / a.n_tiles;             // local row
     const int64_t t = cta - b * a.n_tiles;         // tile
     const int64_t row = a.row0 + b;
+    clear_status_bits(a.status_bits, a.row0);
     const RowParams p = make_row_params(a.temperature, a.seeds, a.positions, a.base_seed,
                                         a.offset, row);
     float best_s = -CUDART_INF_F;

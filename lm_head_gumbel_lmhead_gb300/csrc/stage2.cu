@@ -13,7 +13,8 @@ constexpr int kStage2PerThread = 8;   // candidates a thread loads before it com
 
 __global__ void __launch_bounds__(kStage2Threads) stage2_kernel(
     const float* __restrict__ cand_score, const int* __restrict__ cand_index, int64_t n_tiles,
-    const float* __restrict__ temperature, int64_t* __restrict__ out, int32_t* __restrict__ row_status) {
+    const float* __restrict__ temperature, int64_t* __restrict__ out, int32_t* __restrict__ row_status,
+    uint32_t* __restrict__ status_bits) {
     const int64_t b = blockIdx.x;
     // T is an input of the step, not a Stage-1 result: read it before the wait.
     const float T = temperature ? temperature[b] : 1.0f;
@@ -71,6 +72,7 @@ __global__ void __launch_bounds__(kStage2Threads) stage2_kernel(
         }
         out[b] = token;
         if (row_status) row_status[b] = status;
+        note_row_status(status_bits, status);
     }
 }
 
@@ -188,7 +190,7 @@ template <int kM>
 __global__ void __launch_bounds__(256) stage2_topk_final(
     const unsigned long long* __restrict__ part_keys, int S, int k, int64_t B,
     const float* __restrict__ temperature, int64_t* __restrict__ out, float* __restrict__ scores,
-    int32_t* __restrict__ row_status) {
+    int32_t* __restrict__ row_status, uint32_t* __restrict__ status_bits) {
     pdl_wait_primary();
     const int64_t b = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     if (b >= B) return;                            // warp-uniform
@@ -237,7 +239,11 @@ __global__ void __launch_bounds__(256) stage2_topk_final(
         if (scores) scores[b * k + lane] = sc;
     }
     const int found = __popc(__ballot_sync(0xffffffffu, lane < k && idx >= 0));
-    if (lane == 0 && row_status) row_status[b] = poisoned ? 3 : invalid ? 2 : (found > 0 ? 0 : 1);
+    if (lane == 0) {
+        const int status = poisoned ? 3 : invalid ? 2 : (found > 0 ? 0 : 1);
+        if (row_status) row_status[b] = status;
+        note_row_status(status_bits, status);
+    }
 }
 
 }  // namespace
@@ -254,7 +260,8 @@ size_t stage2_topk_part_bytes(int64_t B, int k) {
 
 cudaError_t launch_stage2_topk(const unsigned long long* cand_keys, int64_t n_lists, int k, int64_t B,
                                const float* temperature, int64_t* out, float* scores,
-                               int32_t* row_status, unsigned long long* part_keys, cudaStream_t stream) {
+                               int32_t* row_status, uint32_t* status_bits,
+                               unsigned long long* part_keys, cudaStream_t stream) {
     if (k < 1 || k > tc::kMaxTopK) return cudaErrorInvalidValue;
     const size_t smem = static_cast<size_t>(kTopKThreads) * k * sizeof(unsigned long long);
     for (const void* f : {reinterpret_cast<const void*>(stage2_topk_part<1>),
@@ -285,12 +292,12 @@ cudaError_t launch_stage2_topk(const unsigned long long* cand_keys, int64_t n_li
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, fin, static_cast<const unsigned long long*>(part_keys), S, k, B,
-                              temperature, out, scores, row_status);
+                              temperature, out, scores, row_status, status_bits);
 }
 
 cudaError_t launch_stage2(const float* cand_score, const int* cand_index, int64_t n_tiles,
                           int64_t B, const float* temperature, int64_t* out, int32_t* row_status,
-                          cudaStream_t stream) {
+                          uint32_t* status_bits, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(B));
     cfg.blockDim = dim3(kStage2Threads);
@@ -302,7 +309,7 @@ cudaError_t launch_stage2(const float* cand_score, const int* cand_index, int64_
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, stage2_kernel, cand_score, cand_index, n_tiles, temperature,
-                              out, row_status);
+                              out, row_status, status_bits);
 }
 
 }  // namespace lms

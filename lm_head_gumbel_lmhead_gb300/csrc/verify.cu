@@ -312,6 +312,7 @@ struct PartItem {
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 4) verify_partials(VerifyArgs a, int64_t b_base) {
     pdl_launch_dependents();                       // the decision kernel may take its slots now
+    clear_status_bits(a.status_bits, b_base);
     const int c = blockIdx.x, q = blockIdx.y;
     const int64_t b = b_base + blockIdx.z;
     bool greedy, invalid;
@@ -364,6 +365,7 @@ __global__ void __launch_bounds__(kThreads) verify_decide(VerifyArgs a, int64_t 
             if (lane == 0) {
                 a.accept_len[b] = 0;
                 if (a.row_status) a.row_status[b] = 2;
+                note_row_status(a.status_bits, 2);
                 a.dec[b] = d;
             }
         }
@@ -405,6 +407,7 @@ __global__ void __launch_bounds__(kThreads) verify_decide(VerifyArgs a, int64_t 
     if (lane == 0) {
         a.accept_len[b] = none ? 0 : j;
         if ((greedy || none) && a.row_status) a.row_status[b] = none ? 1 : 0;
+        if (none) note_row_status(a.status_bits, 1);
         d.j = j;
         if (!greedy && !none) {
             d.mode = kModeRace;
@@ -437,6 +440,7 @@ __device__ __forceinline__ void finalize_row(const VerifyArgs& a, int64_t b, int
         const int64_t tok = (j < a.k && ri >= 0) ? ri : ti;
         a.out[b * (a.k + 1) + j] = tok;
         if (a.row_status) a.row_status[b] = tok >= 0 ? 0 : 1;
+        if (tok < 0) note_row_status(a.status_bits, 1);
     }
 }
 

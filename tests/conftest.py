@@ -18,3 +18,31 @@ def golden():
     import json
     with open(os.path.join(ROOT, "tests", "golden", "pages_printed_values.json")) as f:
         return json.load(f)
+
+
+@pytest.fixture(autouse=True)
+def _parity_record_current_test(request):
+    import parity
+    parity.CURRENT[0] = request.node.nodeid
+    yield
+    parity.CURRENT[0] = "(outside a test)"
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The counts the parity checks kept: rows and tiles compared, how many fell under the
+    near-tie rule, and the tail-miss counts of the tail-rate tests."""
+    import parity
+    if not parity.RECORD:
+        return
+    terminalreporter.section("parity counts (near-tie rule, tail misses)")
+    for test, counts in sorted(parity.RECORD.items()):
+        terminalreporter.write_line(f"{test}: " + ", ".join(f"{k}={v}" for k, v in counts.items()))
+
+
+def pytest_sessionfinish(session):
+    import json
+    import parity
+    path = os.environ.get("LMS_PARITY_RECORD")
+    if path and parity.RECORD:
+        with open(path, "w") as f:
+            json.dump(parity.RECORD, f, indent=1, sort_keys=True)

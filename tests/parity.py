@@ -18,6 +18,24 @@ import numpy as np
 NEAR_TIE = 1e-3
 TILE_RTOL = 2e-4
 
+# Per-test counts of what was compared and how many comparisons fell under the near-tie rule
+# (and, through record(), other counts a test reports, such as tail misses).  conftest.py sets
+# CURRENT to the running test's id, prints the counts at the end of the session and, when
+# LMS_PARITY_RECORD names a file, writes them there as JSON.
+RECORD = {}
+CURRENT = ["(outside a test)"]
+
+
+def _add(**counts):
+    d = RECORD.setdefault(CURRENT[0], {})
+    for k, v in counts.items():
+        d[k] = d.get(k, 0) + int(v)
+
+
+def record(**facts):
+    """Attach facts (numbers, short lists) to the running test's record."""
+    RECORD.setdefault(CURRENT[0], {}).update(facts)
+
 
 def tile_tol(s):
     return TILE_RTOL * (1.0 + np.abs(s))
@@ -43,6 +61,10 @@ def check_rows(gpu_out, gpu_status, orc, score_of=None, rows=None):
         s = score_of(i, int(gpu_out[i]))
         assert s >= orc.top1[i] - NEAR_TIE, (i, gpu_out[i], s, orc.top1[i])
         near += 1
+    # rows whose top two oracle scores sit within the near-tie distance, whether or not the
+    # indices happened to agree
+    close = int(np.count_nonzero((orc.top1 - orc.top2 < NEAR_TIE) & (orc.status == 0)))
+    _add(rows=gpu_out.shape[0], rows_index_differs_near_tie=near, rows_top2_within_near_tie=close)
     return near
 
 
@@ -67,4 +89,5 @@ def check_tiles(gpu_score, gpu_index, orc, score_of=None):
         s = score_of(i, int(gpu_index[i, t]))
         assert s >= orc.tile_max[i, t] - NEAR_TIE, (i, t, gpu_index[i, t], s, orc.tile_max[i, t])
         near += 1
+    _add(tiles=int(finite.sum()), tiles_index_differs_near_tie=near)
     return near

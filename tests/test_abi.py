@@ -45,7 +45,8 @@ def test_tile_info(L):
     tv, nt, ws, path = lms.tile_info(lms.OP_LMHEAD, 64, 4096, 151936)
     assert tv == 128 and nt == 1187 and path == lms.PATH_TCGEN05
     cand = 64 * 1187 * 4
-    assert ws == 2 * ((cand + 255) // 256 * 256)
+    # the 256-byte status block, then scores and indices at 256-byte boundaries
+    assert ws == 256 + 2 * ((cand + 255) // 256 * 256)
     assert lms.tile_info(lms.OP_LMHEAD, 1, 4096, 151936)[3] == lms.PATH_TCGEN05
     tv, nt, _, _ = lms.tile_info(lms.OP_LOGITS, 8192, 0, 131072)
     assert tv == 8192 and nt == 16
@@ -141,12 +142,13 @@ def test_verify_host_validation(L):
     assert L.lms_workspace_bytes_verify(4, 3, 2**31) == 0
     # partials of 2k+1 rows per batch row (three arrays), decisions, two candidates per chunk
     # (sized for fp32 logits: one partial per warp over chunks of 8192 entries, 16-byte row
-    # decisions, race candidates over chunks of 4096), and a per-row completion counter
-    assert need == 3 * r256(4 * 7 * 8 * 4) + 256 + 2 * 256 + 256
+    # decisions, race candidates over chunks of 4096), and a per-row completion counter, after
+    # the 256-byte status block every workspace starts with
+    assert need == 256 + 3 * r256(4 * 7 * 8 * 4) + 256 + 2 * 256 + 256
     big = L.lms_workspace_bytes_verify(64, 4, 151936)
     nc, ncr = -(-151936 // 8192), -(-151936 // 4096)
     r256 = lambda x: -(-x // 256) * 256
-    assert big == 3 * r256(64 * 9 * nc * 8 * 4) + r256(64 * 16) + 2 * r256(64 * ncr * 8) + r256(64 * 4)
+    assert big == 256 + 3 * r256(64 * 9 * nc * 8 * 4) + r256(64 * 16) + 2 * r256(64 * ncr * 8) + r256(64 * 4)
 
 
 def test_topk_fp8_filtered_noalloc_host_validation(L):
@@ -185,3 +187,10 @@ def test_topk_fp8_filtered_noalloc_host_validation(L):
     p = _params()
     st = L.lms_lmhead_sample_noalloc(FAKE, 4096, FAKE, 4096, 65536, 4096, 151936, ctypes.byref(p), FAKE, None)
     assert st == WS and b"static scratch" in L.lms_last_error()
+
+
+def test_read_status_rejects_a_missing_workspace(L):
+    bits = ctypes.c_uint32(7)
+    assert L.lms_read_status(None, None, ctypes.byref(bits)) == lms.LMS_ERR_INVALID_ARG
+    assert bits.value == 7
+    assert b"workspace" in L.lms_last_error()

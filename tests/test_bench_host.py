@@ -46,16 +46,31 @@ def test_max_over_ranks_gloo_world2():
     assert res == {0: 15.0, 1: 15.0}
 
 
-def test_reference_arm_prints_contract_line():
+def _reference_line(*extra):
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                        "--steps", "1", "--warmup", "3", "--batch", "4", "--D", "256", "--V", "4096",
-                        "--ref-vslice", "1024"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+                        "--steps", "2", "--warmup", "3", "--batch", "4", "--D", "256", "--V", "4096",
+                        *extra], capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
-    line = json.loads(r.stdout.strip().splitlines()[-1])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def test_reference_arm_prints_contract_line():
+    line = _reference_line()
     assert line["impl"] == "reference" and line["unit"] == "us/step" and line["value"] > 0
     assert line["higher_is_better"] is False
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+    # the GPU arm's config keys for a single-GPU run; a small workload runs in full each step
+    assert line["config"]["parallelism"] == "single-gpu" and line["config"]["tile_v"] == 128
+    assert line["vocab_rows_per_step"] == 4096 and line["extrapolated_from_v"] is None
+    assert abs(line["measured_seconds_per_step"] * 1e6 - line["value"]) <= 1e-6 * line["value"] + 100
+
+
+def test_reference_arm_states_its_slice_when_the_budget_is_short():
+    line = _reference_line("--ref-budget-s", "0.000001")
+    assert line["extrapolated_from_v"] == line["vocab_rows_per_step"] == 128
+    per_row = line["measured_seconds_per_step"] / 128
+    assert abs(per_row * 4096 * 1e6 - line["value"]) <= 1e-3 * line["value"]
 
 
 def test_algorithmic_bytes_qwen_b64():

@@ -20,6 +20,7 @@ from scipy import stats
 import lm_head_gumbel_lmhead_gb300 as lms
 import oracle
 from lm_head_gumbel_lmhead_gb300 import workloads
+from parity import _add as count_parity
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda")
@@ -58,6 +59,7 @@ def check_filtered(gpu_out, gpu_st, y, B=None, **kw):
     out, st, kept, t1, t2 = oracle.sample_filtered(y, B=B, want_top2=True, **kw_o)
     assert np.array_equal(gpu_st, st), (np.nonzero(gpu_st != st)[0][:5], gpu_st[gpu_st != st][:5], st[gpu_st != st][:5])
     bad = np.nonzero(gpu_out != out)[0]
+    count_parity(rows=gpu_out.shape[0])
     if bad.size == 0:
         return 0
     alts = [oracle.sample_filtered(y, B=B, p_shift=ps, minp_scale=ms, **kw_o)[0]
@@ -69,6 +71,7 @@ def check_filtered(gpu_out, gpu_st, y, B=None, **kw):
         else:
             raise AssertionError(f"row {i}: gpu {gpu_out[i]} oracle {out[i]} kept {kept[i]} "
                                  f"alternatives {[a[i] for a in alts]} top-two gap {t1[i] - t2[i]:.3e}")
+    count_parity(rows_index_differs_filter_boundary_or_near_tie=accepted)
     return accepted
 
 

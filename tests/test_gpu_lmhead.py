@@ -3,8 +3,10 @@
   * every output (indices, statuses, all Stage-1 candidates) on the tiny workload and on ragged
     shapes (B not a multiple of 16, V not a multiple of 128, D not a multiple of 64, batches
     above 256 rows) for both the CUDA-core GEMV path and the tcgen05 path;
-  * sampled rows at full size (Qwen3-8B shape at B = 1, 8, 64, 256; the Llama-3 heterogeneous
-    batch; the large-vocabulary shape with wide noise) in the configuration the benchmark times;
+  * every row at full size (Qwen3-8B shape at B = 1, 8, 64, 256; the Llama-3 heterogeneous
+    batch; the large-vocabulary shape with wide noise at B = 128), and rows on both sides of
+    every 256-row launch boundary at B = 512, in the configuration the benchmark times, with
+    every Stage-1 candidate of those rows compared;
   * seeded rows invariant to batch position; repeat calls bit-equal;
   * a device-side wait that runs out of time reports row status 3 and leaves the context usable.
 """
@@ -148,12 +150,11 @@ def qwen_w():
 
 
 @pytest.mark.parametrize("B", [1, 8, 64, 256])
-def test_qwen3_8b_shape_sampled_rows(qwen_w, B):
+def test_qwen3_8b_shape_every_row(qwen_w, B):
     w = qwen_w
     sub = workloads.Workload(w.name, B, w.D, w.V, w.H[:B].contiguous(), w.W, w.temperature[:B],
                              w.seeds[:B], w.positions[:B], None, None, w.noise_mode)
-    rows = sorted(set([0, B - 1, B // 2, min(B - 1, 5)]))
-    out, st, _ = sampled_parity(sub, rows)
+    out, st, _ = sampled_parity(sub, range(B))
     assert (st == 0).all()
 
 
@@ -170,17 +171,21 @@ def test_qwen3_8b_shape_paths_agree_at_small_batch(qwen_w):
         sampled_parity(sub, [0, 1], lms.PATH_TCGEN05)
 
 
-def test_llama3_hetero_sampled_rows():
+def test_llama3_hetero_every_row():
     w = workloads.llama3_hetero()
-    rows = [0, 1, 3, 8, 15, 31, 32, 35, 40, 63]
-    out, st, _ = sampled_parity(w, rows)
+    out, st, _ = sampled_parity(w, range(w.B))
     assert (st == 0).all()
 
 
-@pytest.mark.parametrize("B", [128, 512])
-def test_large_vocab_wide_noise_sampled_rows(B):
-    w = workloads.large_vocab(B)
-    rows = [0, 77, B - 1] if B == 128 else [0, 255, 256, 511]
+def test_large_vocab_wide_noise_every_row_b128():
+    w = workloads.large_vocab(128)
+    sampled_parity(w, range(128))
+
+
+def test_large_vocab_wide_noise_b512_launch_boundaries():
+    # two launches of 256 rows: rows on both sides of the boundary and at both ends
+    w = workloads.large_vocab(512)
+    rows = list(range(0, 8)) + list(range(248, 264)) + list(range(504, 512))
     sampled_parity(w, rows)
 
 

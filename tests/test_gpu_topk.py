@@ -14,6 +14,7 @@ from scipy import stats
 import lm_head_gumbel_lmhead_gb300 as lms
 import oracle
 from lm_head_gumbel_lmhead_gb300 import workloads
+from parity import _add as count_parity
 from test_gpu_lmhead import _ragged, orc_kw, to_dev
 
 pytestmark = pytest.mark.gpu
@@ -49,6 +50,7 @@ def check_topk(g_idx, g_val, g_st, o_idx, o_val, o_st, o_scores):
         os_ = o_scores[b, gi[:m]]
         assert np.all(np.abs(g_val[b, :m] - os_) <= 2e-4 * (1 + np.abs(os_))), (b, g_val[b, :m], os_)
         assert np.all(g_val[b, m:] == -np.inf)
+    count_parity(rows=g_idx.shape[0], ranks_index_differs_near_tie=near)
     return near
 
 

@@ -23,6 +23,7 @@ from scipy import stats
 import lm_head_gumbel_lmhead_gb300 as lms
 import oracle
 from parity import NEAR_TIE
+from parity import _add as count_parity
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda")
@@ -144,6 +145,8 @@ def check_verify(g, o, t64, d64, T, k):
                 f"row {b}: gpu {a} ({scores[b, a]:.6f}) oracle {ao} ({top2[b, 0]:.6f}), "
                 f"not within the error interval")
             near_draw += 1
+    count_parity(rows=g_acc.shape[0], accept_tests_near_margin=near_accept,
+                 draws_index_differs_within_error=near_draw)
     return near_accept, near_draw
 
 

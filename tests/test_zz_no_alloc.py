@@ -1,7 +1,7 @@
 """The allocation-free fused entry point, lms_lmhead_sample_noalloc, through the C ABI.
 
 It serves callers that cannot allocate device memory (for instance code running inside an
-allocator or a memory-pool callback): its Stage-1 scratch is the library's fixed 4 MiB device
+allocator or a memory-pool callback): its Stage-1 scratch is the library's fixed device
 array instead of a caller workspace.  Its tokens and row statuses must equal those of
 lms_lmhead_sample on the same inputs, call after call (the array keeps the previous call's
 candidates, which the next call must overwrite), and calls that would not fit the array must be
@@ -86,6 +86,20 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
     assert np.array_equal(out_new, out_ref) and np.array_equal(st_new, st_ref)
 
 
+@pytest.mark.gpu
+def test_noalloc_fills_its_scratch_across_launches():
+    # B * ceil(V / 128) = 512 * 1024 = 524288 candidates: the whole array, written by two Stage-1
+    # launches of 256 rows (the second at candidate offset 256 * 1024); then a smaller call
+    L = _lib()
+    w = _case(512, 64, 131072, seed=5)
+    out_ref, st_ref, out_new, st_new = _run_both(L, w, torch.arange(w.B, dtype=torch.int64) * 3, True)
+    assert np.array_equal(st_new, st_ref) and np.array_equal(out_new, out_ref)
+    assert (st_ref >= 0).all()
+    w2 = _case(5, 64, 3000, seed=6)
+    out_ref, st_ref, out_new, st_new = _run_both(L, w2, torch.arange(5, dtype=torch.int64), False)
+    assert np.array_equal(out_new, out_ref) and np.array_equal(st_new, st_ref)
+
+
 def test_noalloc_refuses_calls_beyond_its_scratch():
     L = _lib()
     p = lms.SampleParams()
@@ -95,6 +109,9 @@ def test_noalloc_refuses_calls_beyond_its_scratch():
                                      fake, None)
     assert rc == lms.LMS_ERR_WORKSPACE
     assert b"static scratch" in L.lms_last_error()
+    # one candidate more than the array holds: 513 * 1024 = 525312
+    rc = L.lms_lmhead_sample_noalloc(fake, 64, fake, 64, 513, 64, 131072, ctypes.byref(p), fake, None)
+    assert rc == lms.LMS_ERR_WORKSPACE
     # invalid sizes get the regular entry point's checks
     assert L.lms_lmhead_sample_noalloc(fake, 64, fake, 64, 0, 64, 100, ctypes.byref(p), fake,
                                        None) == lms.LMS_ERR_INVALID_ARG
