@@ -165,3 +165,36 @@ def quantize_weight_e4m3(W: torch.Tensor, chunk_rows: int = 8192):
         scale[r0:r1] = s
         W8[r0:r1] = (w / s[:, None]).to(torch.float8_e4m3fn).view(torch.uint8)
     return W8, scale
+
+
+def quantize_weight_mxfp4(W: torch.Tensor, chunk_rows: int = 8192):
+    """Offline MXFP4 weight quantisation (Open Compute Project Microscaling: E2M1 elements, one
+    UE8M0 scale per block of 32 along D), as a model would ship its LM head.  Per block the scale
+    is 2^e with e the smallest integer such that max |w| <= 6 * 2^e (e = -127 for an all-zero
+    block), and each element is w / 2^e rounded to the nearest E2M1 magnitude (0, 0.5, 1, 1.5, 2,
+    3, 4, 6; ties to the even mantissa) with its sign.  Returns (W4 uint8 [V, D/2]: element d in
+    the low nibble of byte d/2 when d is even, the high nibble when odd; S uint8 [D/32, V]: the
+    scale code e + 127 of block d/32 of row v)."""
+    V, D = W.shape
+    assert D % 32 == 0, "MXFP4 blocks are 32 elements along D"
+    W4 = torch.empty(V, D // 2, dtype=torch.uint8)
+    S = torch.empty(D // 32, V, dtype=torch.uint8)
+    mags = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    mids = (mags[1:] + mags[:-1]) / 2
+    for r0 in range(0, V, chunk_rows):
+        r1 = min(V, r0 + chunk_rows)
+        w = W[r0:r1].double().reshape(r1 - r0, D // 32, 32)
+        amax = w.abs().amax(dim=2)
+        m, ex = torch.frexp(amax / 6.0)                 # amax / 6 = m 2^ex, m in [0.5, 1)
+        e = torch.where(m == 0.5, ex - 1, ex)           # ceil(log2(amax / 6))
+        e = torch.where(amax > 0, e, torch.full_like(e, -127)).clamp(-127, 127)
+        x = (w / torch.pow(2.0, e.double())[:, :, None]).float()
+        a = x.abs().clamp(max=6.0)
+        code = torch.searchsorted(mids, a, right=False)  # the lower magnitude at a midpoint
+        tie = (code < 7) & (a == mids[code.clamp(max=6)]) & (code % 2 == 1)
+        code = code + tie.to(code.dtype)                 # ties go to the even mantissa
+        code = code | ((x < 0) | ((x == 0) & torch.signbit(x))).to(code.dtype) * 8
+        code = code.reshape(r1 - r0, D).to(torch.uint8)
+        W4[r0:r1] = code[:, 0::2] | (code[:, 1::2] << 4)
+        S[:, r0:r1] = (e + 127).to(torch.uint8).T
+    return W4, S

@@ -80,6 +80,19 @@ def _load():
                                                   P, i64, P, i64, u64, u64, i32, i64, P, P, P, P,
                                                   P, P, i32]
             lib.orc_lmhead_sample_fp8.restype = ctypes.c_int
+            lib.orc_e2m1_decode.argtypes = [ctypes.c_uint8]
+            lib.orc_e2m1_decode.restype = ctypes.c_double
+            lib.orc_e2m1_encode.argtypes = [ctypes.c_double]
+            lib.orc_e2m1_encode.restype = ctypes.c_uint8
+            lib.orc_ue8m0_decode.argtypes = [ctypes.c_uint8]
+            lib.orc_ue8m0_decode.restype = ctypes.c_double
+            lib.orc_mxfp4_weight.argtypes = [P, i64, P, i64, i64, i64]
+            lib.orc_mxfp4_weight.restype = ctypes.c_double
+            lib.orc_lmhead_logits_mxfp4.argtypes = [P, i64, P, i64, P, i64, i64, i64, i64, P, i64, P, i32]
+            lib.orc_lmhead_sample_mxfp4.argtypes = [P, i64, P, i64, P, i64, i64, i64, i64, P, i64, P,
+                                                    P, P, P, i64, P, i64, u64, u64, i32, i64, P, P, P,
+                                                    P, P, P, i32]
+            lib.orc_lmhead_sample_mxfp4.restype = ctypes.c_int
             lib.orc_noise_row.argtypes = [i32, i64, i64, u64, u64, i64, i64, i32, P]
             lib.orc_accept_uniform.argtypes = [i32, i64, i64, u64, u64, i64, i32]
             lib.orc_accept_uniform.restype = ctypes.c_double
@@ -560,6 +573,79 @@ def lmhead_sample_fp8(H_bits, W8, w_scale, *, rows=None, temperature=None, seeds
         _ptr(H), D, _ptr(W8), D, _ptr(ws), B, D, V, _ptr(r), 0 if r is None else nb, _ptr(T),
         _ptr(seeds_a), _ptr(pos_a), _ptr(bias_a), ld_bias, _ptr(mask_a), ld_mask, base_seed,
         offset, int(bool(wide)), tile_v, *[_ptr(o) for o in outs[:6]], threads or default_threads())
+    if rc != 0:
+        raise MemoryError("oracle could not allocate")
+    return RowResult(*outs)
+
+
+# ---- MXFP4 weights (W4A16): E2M1 elements with one UE8M0 scale per block of 32 ----
+
+def e2m1_decode(codes) -> np.ndarray:
+    """E2M1 codes (4-bit, 0..15) -> fp64 values (OCP Microscaling element format)."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([lib.orc_e2m1_decode(int(x)) for x in c.ravel()]).reshape(c.shape)
+
+
+def e2m1_encode(x) -> np.ndarray:
+    """Nearest E2M1 code of fp64 values (ties to the even mantissa, saturating at +-6)."""
+    lib = _load()
+    a = np.asarray(x, dtype=np.float64)
+    return np.array([lib.orc_e2m1_encode(float(v)) for v in a.ravel()], np.uint8).reshape(a.shape)
+
+
+def ue8m0_decode(codes) -> np.ndarray:
+    """UE8M0 scale codes -> 2^(s - 127) (NaN for 255)."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([lib.orc_ue8m0_decode(int(x)) for x in c.ravel()]).reshape(c.shape)
+
+
+def mxfp4_weight(W4, S, v, d) -> float:
+    """The decoded weight W[v][d] of an MXFP4 matrix: packed codes W4 [V, D/2] (element d in the
+    low nibble of byte d/2 when d is even, the high nibble when odd), scales S [D/32, V]."""
+    W4 = _c(W4, np.uint8); S = _c(S, np.uint8)
+    return _load().orc_mxfp4_weight(_ptr(W4), W4.shape[1], _ptr(S), S.shape[1], int(v), int(d))
+
+
+def lmhead_logits_mxfp4(H_bits, W4, S, rows=None, threads=None) -> np.ndarray:
+    """y = H W^T in fp64 from bf16 H [B, D] and MXFP4 W (W4 [V, D/2], S [D/32, V])."""
+    H = _bits16(H_bits)
+    W4 = _c(W4, np.uint8); S = _c(S, np.uint8)
+    B, D = H.shape
+    V = W4.shape[0]
+    r = _c(rows, np.int64)
+    nb = B if r is None else r.shape[0]
+    y = np.empty((nb, V))
+    _load().orc_lmhead_logits_mxfp4(_ptr(H), D, _ptr(W4), W4.shape[1], _ptr(S), S.shape[1], B, D, V,
+                                    _ptr(r), 0 if r is None else nb, _ptr(y),
+                                    threads or default_threads())
+    return y
+
+
+def lmhead_sample_mxfp4(H_bits, W4, S, *, rows=None, temperature=None, seeds=None, positions=None,
+                        bias=None, mask=None, base_seed=0, offset=0, wide=False, tile_v=128,
+                        threads=None) -> RowResult:
+    """The fused MXFP4 path's result: fp64 logits from bf16 H and the decoded MXFP4 weights, then
+    the per-row race (FlashSampling Stage 1 and 2); rows = a subset of the batch (or all)."""
+    H = _bits16(H_bits)
+    B, D = H.shape
+    W4 = _c(W4, np.uint8); S = _c(S, np.uint8)
+    V = W4.shape[0]
+    r = _c(rows, np.int64)
+    nb = B if r is None else r.shape[0]
+    T = _c(temperature, np.float64)
+    bias_a = _c(bias, np.float64)
+    ld_bias = 0 if bias_a is None or bias_a.ndim == 1 else bias_a.shape[1]
+    mask_a = _c(mask, np.uint32)
+    ld_mask = 0 if mask_a is None or mask_a.ndim == 1 else mask_a.shape[1]
+    seeds_a, pos_a = _c(seeds, np.int64), _c(positions, np.int64)
+    outs = _row_outputs(nb, V, tile_v, False)
+    rc = _load().orc_lmhead_sample_mxfp4(
+        _ptr(H), D, _ptr(W4), W4.shape[1], _ptr(S), S.shape[1], B, D, V, _ptr(r),
+        0 if r is None else nb, _ptr(T), _ptr(seeds_a), _ptr(pos_a), _ptr(bias_a), ld_bias,
+        _ptr(mask_a), ld_mask, base_seed, offset, int(bool(wide)), tile_v,
+        *[_ptr(o) for o in outs[:6]], threads or default_threads())
     if rc != 0:
         raise MemoryError("oracle could not allocate")
     return RowResult(*outs)

@@ -697,3 +697,105 @@ int orc_lmhead_sample_fp8(const uint16_t* H, int64_t ldh, const uint8_t* W8, int
     free(q); free(e); free(y);
     return 0;
 }
+
+/* ------------------------------------------------------------------------------------------ */
+/* MXFP4 weights (W4A16) [FS "Limitations", "Future directions": low-precision inputs for the  */
+/* memory-bound regime].  The format is the Open Compute Project's Microscaling MXFP4: E2M1     */
+/* elements, one shared UE8M0 scale per block of 32 consecutive elements of a row.              */
+/* ------------------------------------------------------------------------------------------ */
+/* E2M1: bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa.  Exponent field 0 is the
+ * subnormal 0.5 * m; otherwise (1 + m / 2) * 2^(e - 1).  Magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6;
+ * no infinities or NaN. */
+double orc_e2m1_decode(uint8_t code) {
+    int s = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+    double v = (e == 0) ? 0.5 * (double)m : ldexp(1.0 + 0.5 * (double)m, e - 1);
+    return s ? -v : v;
+}
+
+/* UE8M0: an unsigned 8-bit exponent, 2^(s - 127); s = 255 is NaN. */
+double orc_ue8m0_decode(uint8_t s) { return s == 255 ? NAN : ldexp(1.0, (int)s - 127); }
+
+/* Nearest E2M1 code of x (ties to the code with mantissa bit 0), saturating at +-6: a search over
+ * the eight magnitudes, so it can be checked by eye. */
+uint8_t orc_e2m1_encode(double x) {
+    uint8_t sign = (x < 0.0 || (x == 0.0 && signbit(x))) ? 8 : 0;
+    double a = fabs(x);
+    uint8_t best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c < 8; ++c) {
+        double d = fabs(orc_e2m1_decode((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) { best_d = d; best = (uint8_t)c; }
+    }
+    return (uint8_t)(sign | best);
+}
+
+/* The weight W[v][d] of an MXFP4 matrix: element d of row v is the low (d even) or high (d odd)
+ * nibble of byte W4[v][d / 2]; its scale is S[d / 32][v] (block-major scales, lds >= V). */
+double orc_mxfp4_weight(const uint8_t* W4, int64_t ldw4, const uint8_t* S, int64_t lds, int64_t v,
+                        int64_t d) {
+    uint8_t byte = W4[v * ldw4 + d / 2];
+    uint8_t code = (d % 2 == 0) ? (byte & 15) : (byte >> 4);
+    return orc_e2m1_decode(code) * orc_ue8m0_decode(S[(d / 32) * lds + v]);
+}
+
+typedef struct {
+    const uint16_t* H; int64_t ldh; const uint8_t* W4; int64_t ldw4; const uint8_t* S; int64_t lds;
+    int64_t B, D, V; double* y; int64_t v0, v1; const int64_t* rows;
+} orc_gemm4_job;
+
+static void* orc_gemm4_worker(void* p) {
+    const orc_gemm4_job* j = (const orc_gemm4_job*)p;
+    double* wrow = (double*)malloc(sizeof(double) * (size_t)j->D);
+    for (int64_t v = j->v0; v < j->v1; ++v) {
+        for (int64_t d = 0; d < j->D; ++d) wrow[d] = orc_mxfp4_weight(j->W4, j->ldw4, j->S, j->lds, v, d);
+        for (int64_t i = 0; i < j->B; ++i) {
+            int64_t b = j->rows ? j->rows[i] : i;
+            double acc = 0.0;
+            for (int64_t d = 0; d < j->D; ++d) acc += orc_bf16(j->H[b * j->ldh + d]) * wrow[d];
+            j->y[i * j->V + v] = acc;
+        }
+    }
+    free(wrow);
+    return NULL;
+}
+
+/* y[b][v] = sum_d bf16(H[b][d]) * E2M1(W4[v][d]) * 2^(S[d/32][v] - 127), in fp64 (each product
+ * is exact), summed in increasing d; rows as in orc_lmhead_sample_rows (NULL = all B). */
+void orc_lmhead_logits_mxfp4(const uint16_t* H, int64_t ldh, const uint8_t* W4, int64_t ldw4,
+                             const uint8_t* S, int64_t lds, int64_t B, int64_t D, int64_t V,
+                             const int64_t* rows, int64_t n_rows, double* y, int nthreads) {
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t th[256];
+    orc_gemm4_job jobs[256];
+    int64_t nb = rows ? n_rows : B;
+    for (int i = 0; i < nthreads; ++i) {
+        orc_gemm4_job j = {H, ldh, W4, ldw4, S, lds, nb, D, V, y, V * i / nthreads,
+                           V * (i + 1) / nthreads, rows};
+        jobs[i] = j;
+        pthread_create(&th[i], NULL, orc_gemm4_worker, &jobs[i]);
+    }
+    for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+}
+
+/* The fused MXFP4 path's result for rows (NULL = all): fp64 logits from bf16 H and the decoded
+ * MXFP4 weights, then the same per-row race (tile maxima for tile_v). */
+int orc_lmhead_sample_mxfp4(const uint16_t* H, int64_t ldh, const uint8_t* W4, int64_t ldw4,
+                            const uint8_t* S, int64_t lds, int64_t B, int64_t D, int64_t V,
+                            const int64_t* rows, int64_t n_rows, const double* T,
+                            const int64_t* seeds, const int64_t* positions, const double* bias,
+                            int64_t ld_bias, const uint32_t* mask, int64_t ld_mask,
+                            uint64_t base_seed, uint64_t offset, int wide, int64_t tile_v,
+                            int64_t* out, int32_t* status, double* top1, double* top2,
+                            double* tile_max, int64_t* tile_idx, int nthreads) {
+    int64_t nb = rows ? n_rows : B;
+    double* y = (double*)malloc(sizeof(double) * (size_t)(nb * V));
+    if (!y) return 1;
+    orc_lmhead_logits_mxfp4(H, ldh, W4, ldw4, S, lds, B, D, V, rows, n_rows, y, nthreads);
+    orc_rows_args a = {y, V, B, V, T, seeds, positions, bias, ld_bias, mask, ld_mask,
+                       base_seed, offset, wide, tile_v, out, status, top1, top2,
+                       tile_max, tile_idx, NULL, rows, rows ? n_rows : 0};
+    orc_run_rows(&a, nthreads);
+    free(y);
+    return 0;
+}
