@@ -470,6 +470,11 @@ def run_gpu(args):
         wide = w.noise_mode == 1
         kw = dict(temperature=T, seeds=seeds, bias=bias, mask=mask, base_seed=w.base_seed,
                   offset=w.offset, wide=wide, out=out, workspace=workspace)
+        path_req = {"auto": lms.PATH_AUTO, "gemv": lms.PATH_GEMV, "tcgen05": lms.PATH_TCGEN05}[args.path]
+        if path_req != lms.PATH_AUTO:
+            if fp8 or topk:
+                raise SystemExit("--path applies to the bf16 race workloads")
+            path = path_req
         launches_per_step = (1 + (B - 1) // 256 if path == lms.PATH_TCGEN05 else 1) + 1
         if fp8:
             W8_h, wsc_h = workloads.quantize_weight_e4m3(w.W)
@@ -484,7 +489,7 @@ def run_gpu(args):
                 lms.lmhead_sample_topk(H, W, topk, positions=pos_all[i], scores=scores_k, **kw)
         else:
             def step(i):
-                lms.lmhead_sample(H, W, positions=pos_all[i], **kw)
+                lms.lmhead_sample(H, W, positions=pos_all[i], path=path, **kw)
 
         alg = algorithmic_bytes(B, D, V, nt, bias is not None, mask is not None)
         if fp8:
@@ -512,14 +517,14 @@ def run_gpu(args):
         T = torch.full((B,), 0.7, device=dev)
         seeds = 1000 + torch.arange(B, dtype=torch.int64, device=dev)
         pos_all = torch.arange(n_steps, dtype=torch.int64)[:, None].expand(n_steps, B).contiguous().to(dev)
-        tv, nt, ws_bytes, _ = lms.tile_info(lms.OP_LOGITS, B, 0, V)
+        tv, nt, ws_bytes, _ = lms.tile_info(lms.OP_LOGITS, B, 0, V, args.tile_v)
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         out = torch.empty(B, dtype=torch.int64, device=dev)
         launches_per_step = 2
 
         def step(i):
             lms.sample_from_logits(logits, temperature=T, seeds=seeds, positions=pos_all[i], out=out,
-                                   workspace=workspace)
+                                   workspace=workspace, tile_v=args.tile_v)
 
         alg = B * V * logits.element_size() + 2 * B * nt * 8 + B * 28
         flops = 0
@@ -623,9 +628,9 @@ def run_gpu(args):
         # e2e: the step's per-request inputs from pinned host memory, the tokens back to pinned
         # host memory; W is a resident weight.  The inputs of a step (H, T, seeds, positions and
         # the optional bias and mask) sit in one pinned staging block and go over in one copy.
-        # The copies run on a copy stream: step i's inputs go over while step i-1's kernels run,
-        # and step i's tokens come back while step i+1's run.  Device inputs and outputs are
-        # double-buffered; events order every reuse.
+        # The copies run on two copy streams, one per direction, so that step i+1's inputs go
+        # over while step i's kernels run and step i's tokens come back while step i+1's run.
+        # Device inputs and outputs are double-buffered; events order every reuse.
         host = {"H": w.H, "T": w.temperature, "seeds": w.seeds, "positions": w.positions}
         if w.bias is not None:
             host["bias"] = w.bias
@@ -646,7 +651,8 @@ def run_gpu(args):
         for blk in stage:
             for k, v in host.items():
                 view(blk, k).copy_(v)
-        copy_stream = torch.cuda.Stream(dev)
+        h2d_stream = torch.cuda.Stream(dev)
+        d2h_stream = torch.cuda.Stream(dev)
         h2d_done = [torch.cuda.Event() for _ in range(ring)]      # pinned block i % ring read
         dblk = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
         devb = [{k: view(b, k) for k in host} for b in dblk]
@@ -654,38 +660,46 @@ def run_gpu(args):
         ready = [torch.cuda.Event() for _ in range(2)]            # inputs of the slot landed
         computed = [torch.cuda.Event() for _ in range(2)]         # the slot's kernels finished
         fetched = [torch.cuda.Event() for _ in range(2)]          # the slot's tokens are back
-        pos_h = pos_all.cpu()
+        pos_np = pos_all.cpu().numpy()
+        pos_stage = [view(blk, "positions").numpy() for blk in stage]
         out_h = [torch.empty(tuple(out.shape), dtype=torch.int64).pin_memory() for _ in range(ring)]
         for ev in computed + fetched:
             ev.record(stream)
-
-        def e2e_step(i):
-            j, slot = i % ring, i % 2
-            blk = stage[j]
-            h2d_done[j].synchronize()              # the copy that last read this block is done
-            view(blk, "positions").copy_(pos_h[i])
-            with torch.cuda.stream(copy_stream):
-                copy_stream.wait_event(computed[slot])   # step i-2's kernels read this slot
-                dblk[slot].copy_(blk, non_blocking=True)
-                h2d_done[j].record(copy_stream)
-                ready[slot].record(copy_stream)
-            stream.wait_event(ready[slot])
-            stream.wait_event(fetched[slot])       # step i-2's tokens have left this slot
+        # one C-ABI call per device slot, marshalled once: a step changes the slot's contents
+        # (its inputs arrive by copy), never its addresses
+        calls = []
+        for slot in range(2):
             b = devb[slot]
             ekw = dict(temperature=b["T"], seeds=b["seeds"], positions=b["positions"],
                        bias=b.get("bias"), mask=b.get("mask"), base_seed=w.base_seed,
-                       offset=w.offset, wide=wide, out=outs[slot], workspace=workspace)
+                       offset=w.offset, wide=wide, out=outs[slot], workspace=workspace,
+                       stream=stream)
             if fp8:
-                lms.lmhead_sample_fp8(b["H"], W8, wsc, **ekw)
+                calls.append(lms.prepare_lmhead_sample_fp8(b["H"], W8, wsc, **ekw))
             elif topk:
-                lms.lmhead_sample_topk(b["H"], W, topk, scores=scores_k, **ekw)
+                calls.append(lms.prepare_lmhead_sample_topk(b["H"], W, topk, scores=scores_k, **ekw))
             else:
-                lms.lmhead_sample(b["H"], W, **ekw)
+                calls.append(lms.prepare_lmhead_sample(b["H"], W, path=path, **ekw))
+
+        def e2e_step(i):
+            j, slot = i % ring, i % 2
+            h2d_done[j].synchronize()              # the copy that last read this block is done
+            pos_stage[j][:] = pos_np[i]
+            torch.cuda.set_stream(h2d_stream)
+            h2d_stream.wait_event(computed[slot])       # step i-2's kernels read this slot
+            dblk[slot].copy_(stage[j], non_blocking=True)
+            h2d_done[j].record(h2d_stream)
+            ready[slot].record(h2d_stream)
+            torch.cuda.set_stream(stream)
+            stream.wait_event(ready[slot])
+            stream.wait_event(fetched[slot])       # step i-2's tokens have left this slot
+            calls[slot]()
             computed[slot].record(stream)
-            with torch.cuda.stream(copy_stream):
-                copy_stream.wait_event(computed[slot])
-                out_h[j].copy_(outs[slot], non_blocking=True)
-                fetched[slot].record(copy_stream)
+            torch.cuda.set_stream(d2h_stream)
+            d2h_stream.wait_event(computed[slot])
+            out_h[j].copy_(outs[slot], non_blocking=True)
+            fetched[slot].record(d2h_stream)
+            torch.cuda.set_stream(stream)
 
         def e2e_time(n_warm, n_steps):
             for i in range(n_warm):
@@ -695,20 +709,23 @@ def run_gpu(args):
             barrier()
             torch.cuda.synchronize(dev)
             e0.record(stream)
+            h0 = time.perf_counter()
             for k in range(n_steps):
                 e2e_step(n_warm + k)
+            host_us = (time.perf_counter() - h0) / n_steps * 1e6
             stream.wait_event(fetched[(n_warm + n_steps - 1) % 2])   # the last tokens are back
             e1.record(stream)
             torch.cuda.synchronize(dev)
             barrier()
-            return e0.elapsed_time(e1) / n_steps
+            return e0.elapsed_time(e1) / n_steps, host_us
 
-        e2e_ms = e2e_time(args.warmup, args.steps)
+        e2e_ms, e2e_host_us = e2e_time(args.warmup, args.steps)
         e2e = {"value": round(max_over_ranks(e2e_ms, dev) * 1e3, 2), "unit": UNIT,
                "h2d_bytes_per_step": total,
                "d2h_bytes_per_step": out.numel() * 8,
-               "copies": "pinned host <-> device on a copy stream, overlapped with the previous "
-                         "and next steps' kernels"}
+               "copies": "pinned host <-> device on one copy stream per direction, overlapped with "
+                         "the neighbouring steps' kernels",
+               "host_us_per_step": round(e2e_host_us, 2)}
 
     clocks = sampler.stop(t0, t1) if sampler else None
     if rank != 0:
@@ -799,6 +816,10 @@ def main(argv=None):
                     choices=list(FUSED) + ["logits", "noise", "filtered", "verify"])
     ap.add_argument("--batch", type=int, default=0)
     ap.add_argument("--topk", type=int, default=8, help="k of the qwen3-8b-topk workload")
+    ap.add_argument("--path", choices=["auto", "gemv", "tcgen05"], default="auto",
+                    help="Stage-1 path of the bf16 fused race workloads")
+    ap.add_argument("--tile-v", type=int, default=0,
+                    help="tile width of the logits workload (0 = the library's choice)")
     ap.add_argument("--spec-k", type=int, default=4, help="draft length k of the verify workload")
     ap.add_argument("--l2-flush", choices=["auto", "on", "off"], default="auto")
     ap.add_argument("--D", type=int, default=0)

@@ -227,6 +227,20 @@ def _params(B, device, temperature, seeds, positions, bias, mask, base_seed, off
     return p
 
 
+class Prepared:
+    """One C-ABI call with its arguments marshalled once, for a loop that repeats the call on the
+    same buffers and stream: the buffers' contents may change between calls, their addresses and
+    sizes may not, and the stream is the one given (or current) when the call was prepared.
+    Calling it makes the C call (the same one the plain wrapper makes) and returns its outputs."""
+
+    def __init__(self, fn, args, keep, result):
+        self._fn, self._args, self._keep, self._result = fn, args, keep, result
+
+    def __call__(self):
+        _check(self._fn(*self._args))
+        return self._result
+
+
 def lmhead_sample(H: torch.Tensor, W: torch.Tensor, *, temperature=None, seeds=None,
                   positions=None, bias=None, mask=None, base_seed: int = 0, offset: int = 0,
                   wide: bool = False, path: int = PATH_AUTO, out=None, workspace=None,
@@ -237,6 +251,18 @@ def lmhead_sample(H: torch.Tensor, W: torch.Tensor, *, temperature=None, seeds=N
     bf16 H and W on the GPU; per-row temperature (fp32, 0 = greedy), seeds / positions (int64,
     seed < 0 = unseeded), bias fp32 [B, V] or [V], mask int32 allow-bit words [B, ceil(V/32)].
     Returns int64 [B] (-1 on rows whose status is not 0)."""
+    return prepare_lmhead_sample(H, W, temperature=temperature, seeds=seeds, positions=positions,
+                                 bias=bias, mask=mask, base_seed=base_seed, offset=offset, wide=wide,
+                                 path=path, out=out, workspace=workspace, row_status=row_status,
+                                 timeout_ms=timeout_ms, debug_flags=debug_flags, stream=stream)()
+
+
+def prepare_lmhead_sample(H: torch.Tensor, W: torch.Tensor, *, temperature=None, seeds=None,
+                          positions=None, bias=None, mask=None, base_seed: int = 0, offset: int = 0,
+                          wide: bool = False, path: int = PATH_AUTO, out=None, workspace=None,
+                          row_status=None, timeout_ms: int = 0, debug_flags: int = 0,
+                          stream=None) -> Prepared:
+    """lmhead_sample's call, checked and marshalled once (see Prepared)."""
     if H.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
         raise TypeError("H and W must be bfloat16")
     if not H.is_cuda or W.device != H.device:
@@ -254,10 +280,10 @@ def lmhead_sample(H: torch.Tensor, W: torch.Tensor, *, temperature=None, seeds=N
         out = torch.empty(B, dtype=torch.int64, device=dev)
     if workspace is None:
         workspace = torch.empty(workspace_bytes(OP_LMHEAD, B, D, V), dtype=torch.uint8, device=dev)
-    _check(lib().lms_lmhead_sample(_ptr(H), H.stride(0), _ptr(W), W.stride(0), B, D, V,
-                                   ctypes.byref(p), _ptr(out), _ptr(workspace),
-                                   workspace.numel() * workspace.element_size(), _stream(stream)))
-    return out
+    args = (_ptr(H), H.stride(0), _ptr(W), W.stride(0), B, D, V, ctypes.byref(p), _ptr(out),
+            _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    return Prepared(lib().lms_lmhead_sample, args,
+                    (H, W, temperature, seeds, positions, bias, mask, row_status, workspace, p), out)
 
 
 TOPK_MAX = 16
@@ -271,6 +297,19 @@ def lmhead_sample_topk(H: torch.Tensor, W: torch.Tensor, k: int, *, temperature=
     """Gumbel-top-k of the fused path: per row of H [B, D], the k largest perturbed scores of
     lmhead_sample's race (k draws without replacement), larger first, then the smaller index.
     Returns (indices int64 [B, k], -1 past a row's finite scores; scores fp32 [B, k] or None)."""
+    return prepare_lmhead_sample_topk(
+        H, W, k, temperature=temperature, seeds=seeds, positions=positions, bias=bias, mask=mask,
+        base_seed=base_seed, offset=offset, wide=wide, out=out, scores=scores,
+        want_scores=want_scores, workspace=workspace, row_status=row_status,
+        timeout_ms=timeout_ms, debug_flags=debug_flags, stream=stream)()
+
+
+def prepare_lmhead_sample_topk(H: torch.Tensor, W: torch.Tensor, k: int, *, temperature=None,
+                               seeds=None, positions=None, bias=None, mask=None, base_seed: int = 0,
+                               offset: int = 0, wide: bool = False, out=None, scores=None,
+                               want_scores: bool = True, workspace=None, row_status=None,
+                               timeout_ms: int = 0, debug_flags: int = 0, stream=None) -> Prepared:
+    """lmhead_sample_topk's call, checked and marshalled once (see Prepared)."""
     if H.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
         raise TypeError("H and W must be bfloat16")
     if not H.is_cuda or W.device != H.device:
@@ -291,11 +330,12 @@ def lmhead_sample_topk(H: torch.Tensor, W: torch.Tensor, k: int, *, temperature=
     if workspace is None:
         need = lib().lms_workspace_bytes_topk(B, V, k)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-    _check(lib().lms_lmhead_sample_topk(_ptr(H), H.stride(0), _ptr(W), W.stride(0), B, D, V, k,
-                                        ctypes.byref(p), _ptr(out),
-                                        _ptr(scores) if scores is not None else None, _ptr(workspace),
-                                        workspace.numel() * workspace.element_size(), _stream(stream)))
-    return out, scores
+    args = (_ptr(H), H.stride(0), _ptr(W), W.stride(0), B, D, V, k, ctypes.byref(p), _ptr(out),
+            _ptr(scores) if scores is not None else None, _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream))
+    return Prepared(lib().lms_lmhead_sample_topk, args,
+                    (H, W, temperature, seeds, positions, bias, mask, row_status, workspace, p),
+                    (out, scores))
 
 
 def lmhead_sample_fp8(H: torch.Tensor, W8: torch.Tensor, w_scale: torch.Tensor, *, temperature=None,
@@ -305,6 +345,18 @@ def lmhead_sample_fp8(H: torch.Tensor, W8: torch.Tensor, w_scale: torch.Tensor, 
                       stream=None) -> torch.Tensor:
     """lmhead_sample with FP8 inputs: W8 E4M3 codes (uint8 or float8_e4m3fn [V, D]) with per-row
     fp32 w_scale [V]; H bf16 [B, D] is quantised per row (power-of-two scale) by the call."""
+    return prepare_lmhead_sample_fp8(
+        H, W8, w_scale, temperature=temperature, seeds=seeds, positions=positions, bias=bias,
+        mask=mask, base_seed=base_seed, offset=offset, wide=wide, out=out, workspace=workspace,
+        row_status=row_status, timeout_ms=timeout_ms, debug_flags=debug_flags, stream=stream)()
+
+
+def prepare_lmhead_sample_fp8(H: torch.Tensor, W8: torch.Tensor, w_scale: torch.Tensor, *,
+                              temperature=None, seeds=None, positions=None, bias=None, mask=None,
+                              base_seed: int = 0, offset: int = 0, wide: bool = False, out=None,
+                              workspace=None, row_status=None, timeout_ms: int = 0,
+                              debug_flags: int = 0, stream=None) -> Prepared:
+    """lmhead_sample_fp8's call, checked and marshalled once (see Prepared)."""
     if H.dtype != torch.bfloat16:
         raise TypeError("H must be bfloat16")
     if W8.dtype not in (torch.uint8, torch.float8_e4m3fn):
@@ -324,10 +376,11 @@ def lmhead_sample_fp8(H: torch.Tensor, W8: torch.Tensor, w_scale: torch.Tensor, 
         out = torch.empty(B, dtype=torch.int64, device=dev)
     if workspace is None:
         workspace = torch.empty(workspace_bytes(OP_LMHEAD_FP8, B, D, V), dtype=torch.uint8, device=dev)
-    _check(lib().lms_lmhead_sample_fp8(_ptr(H), H.stride(0), _ptr(W8), W8.stride(0), _ptr(w_scale),
-                                       B, D, V, ctypes.byref(p), _ptr(out), _ptr(workspace),
-                                       workspace.numel() * workspace.element_size(), _stream(stream)))
-    return out
+    args = (_ptr(H), H.stride(0), _ptr(W8), W8.stride(0), _ptr(w_scale), B, D, V, ctypes.byref(p),
+            _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    return Prepared(lib().lms_lmhead_sample_fp8, args,
+                    (H, W8, w_scale, temperature, seeds, positions, bias, mask, row_status,
+                     workspace, p), out)
 
 
 def split_workspace_fp8(ws: torch.Tensor, B: int, D: int, n_tiles: int):
