@@ -23,6 +23,8 @@ Workloads (synthetic, seeded; the shapes of the FlashSampling page's measurement
   to E4M3 with per-row scales, and H is quantised per row on the GPU each step (W8A8).
 - ``filtered``: ``lms_sample_from_logits_filtered`` with top-k 50 and top-p 0.9 at T = 0.7 over
   bf16 logits, V = 131072 (the Megatron-LM PR's filter settings).
+- ``qwen3-8b-mxfp4``: the Qwen3-8B shape through ``lms_lmhead_sample_mxfp4``. W is offline-quantised
+  to MXFP4 (E2M1 codes with one UE8M0 scale per block of 32), H stays bf16 (W4A16).
 - ``qwen3-8b-topk``: the Qwen3-8B shape through ``lms_lmhead_sample_topk`` (Gumbel-top-k: k
   draws without replacement per row, k = ``--topk``, default 8).
 - ``verify``: ``lms_verify_from_logits`` (speculative-decoding verification) over bf16 target
@@ -67,7 +69,7 @@ UNIT = "us/step"
 TC_SOURCES = ["lm_head_gumbel_lmhead_gb300/csrc/lmhead_tc.cu",
               "lm_head_gumbel_lmhead_gb300/csrc/tcgen05_common.cuh",
               "lm_head_gumbel_lmhead_gb300/csrc/lms_device.cuh"]
-FUSED = ("qwen3-8b", "llama3-hetero", "large-vocab", "qwen3-8b-fp8", "qwen3-8b-topk")
+FUSED = ("qwen3-8b", "llama3-hetero", "large-vocab", "qwen3-8b-fp8", "qwen3-8b-topk", "qwen3-8b-mxfp4")
 
 
 def kernel_source_hash() -> str:
@@ -251,7 +253,7 @@ class ClockSampler:
 # ------------------------------------------------------------------------------------------
 def make_workload(name: str, B: int, D: int, V: int):
     from lm_head_gumbel_lmhead_gb300 import workloads
-    if name in ("qwen3-8b", "qwen3-8b-fp8", "qwen3-8b-topk"):
+    if name in ("qwen3-8b", "qwen3-8b-fp8", "qwen3-8b-topk", "qwen3-8b-mxfp4"):
         return workloads.qwen3_8b(B, D=D or 4096, V=V or 151936)
     if name == "llama3-hetero":
         return workloads.llama3_hetero(B, D=D or 4096, V=V or 128256)
@@ -460,6 +462,7 @@ def run_gpu(args):
         # positions advance with the step: one row per step, made before timing
         pos_all = (w.positions[None, :] + torch.arange(n_steps)[:, None]).contiguous().to(dev)
         fp8 = args.workload == "qwen3-8b-fp8"
+        mx = args.workload == "qwen3-8b-mxfp4"
         topk = args.topk if args.workload == "qwen3-8b-topk" else 0
         tv, nt, ws_bytes, path = lms.tile_info(lms.OP_LMHEAD_FP8 if fp8 else lms.OP_LMHEAD, B, D, V)
         if topk:
@@ -472,7 +475,7 @@ def run_gpu(args):
                   offset=w.offset, wide=wide, out=out, workspace=workspace)
         path_req = {"auto": lms.PATH_AUTO, "gemv": lms.PATH_GEMV, "tcgen05": lms.PATH_TCGEN05}[args.path]
         if path_req != lms.PATH_AUTO:
-            if fp8 or topk:
+            if fp8 or topk or mx:
                 raise SystemExit("--path applies to the bf16 race workloads")
             path = path_req
         launches_per_step = (1 + (B - 1) // 256 if path == lms.PATH_TCGEN05 else 1) + 1
@@ -484,6 +487,13 @@ def run_gpu(args):
 
             def step(i):
                 lms.lmhead_sample_fp8(H, W8, wsc, positions=pos_all[i], **kw)
+        elif mx:
+            W4_h, S4_h = workloads.quantize_weight_mxfp4(w.W)
+            Wt = lms.mxfp4_pack(W4_h.to(dev), S4_h.to(dev))      # the one-time tiling
+            W = None                               # the bf16 copy is not needed on the device
+
+            def step(i):
+                lms.lmhead_sample_mxfp4(H, Wt, V, positions=pos_all[i], **kw)
         elif topk:
             def step(i):
                 lms.lmhead_sample_topk(H, W, topk, positions=pos_all[i], scores=scores_k, **kw)
@@ -496,18 +506,22 @@ def run_gpu(args):
             # W at one byte per weight plus its row scales; H read once, its E4M3 copy written
             # and read once
             alg = alg - V * D * 2 + V * D + V * 4 + 2 * B * D
+        if mx:
+            # W at half a byte per weight plus one scale byte per block of 32
+            alg = alg - V * D * 2 + V * D // 2 + V * D // 32
         if topk:
             # the tiles' ordered k-lists written and read instead of one candidate each, and k
             # indices and scores per row out
             alg = alg - 2 * B * nt * 8 - B * 8 + 2 * B * nt * topk * 8 + B * topk * 12
         flops = 2 * B * V * D
-        config = {"workload": w.name + (" fp8-e4m3 W8A8" if fp8 else "") +
+        config = {"workload": w.name + (" fp8-e4m3 W8A8" if fp8 else "") + (" mxfp4 W4A16" if mx else "") +
                   (f" Gumbel-top-{topk}" if topk else ""), "B": B, "D": D, "V": V,
                   "noise": "wide53" if wide else "fp32",
                   "path": {1: "gemv", 2: "tcgen05"}[path], "tile_v": tv,
-                  "l2": "inputs larger than L2 (W is %.2f GB), no flush" % (V * D * (1 if fp8 else 2) / 1e9)}
+                  "l2": "inputs larger than L2 (W is %.2f GB), no flush" % (V * D * (1 if fp8 else 0.53125 if mx else 2) / 1e9)}
         kernel = ("quantize_rows_e4m3_kernel + " if fp8 else "") + \
             ("lmhead_tc_kernel (top-k epilogue) + stage2_topk_kernel" if topk else
+             "lmhead_mx_kernel + stage2_kernel" if mx else
              "lmhead_tc_kernel + stage2_kernel") + " (one step, CUDA events)"
     elif args.workload == "logits":
         V = args.V or 131072
@@ -676,6 +690,8 @@ def run_gpu(args):
                        stream=stream)
             if fp8:
                 calls.append(lms.prepare_lmhead_sample_fp8(b["H"], W8, wsc, **ekw))
+            elif mx:
+                calls.append(lms.prepare_lmhead_sample_mxfp4(b["H"], Wt, V, **ekw))
             elif topk:
                 calls.append(lms.prepare_lmhead_sample_topk(b["H"], W, topk, scores=scores_k, **ekw))
             else:

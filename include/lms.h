@@ -188,6 +188,33 @@ lms_status lms_lmhead_sample_fp8(const void* H, int64_t ldh, const void* W8, int
                                  const lms_sample_params* params, int64_t* out, void* workspace,
                                  size_t workspace_bytes, void* stream);
 
+/* The fused path with MXFP4 weights and bf16 activations (W4A16; FlashSampling "Limitations" and
+ * "Future directions": low-precision inputs for the memory-bound regime).  The weight format is
+ * the Open Compute Project's Microscaling MXFP4.  Its logical layout, which lms_mxfp4_pack reads:
+ *   W4   uint8 [V][ldw4] (ldw4 >= D/2): element d of row v is the low nibble of byte d/2 when d
+ *        is even, the high nibble when odd; an E2M1 code (bit 3 sign, bits 2..1 exponent with
+ *        bias 1, bit 0 mantissa: 0, 0.5, 1, 1.5, 2, 3, 4, 6 and negatives).
+ *   S    uint8 [D/32][lds] (lds >= V), block-major: S[k][v] is the UE8M0 scale code of elements
+ *        32k..32k+31 of row v; the scale is 2^(S - 127).
+ *   W[v][d] = E2M1(code) * 2^(S[d/32][v] - 127).
+ * lms_mxfp4_pack rewrites a matrix once into the library's tiled device format (Wt,
+ * lms_mxfp4_tiled_bytes(V, D) bytes): one contiguous 4352-byte block per 128-row vocabulary tile
+ * and 64-element K chunk (4 KB of codes, row r at byte 32 r; then the two blocks' 128 scale codes
+ * each), so that each block streams with a single contiguous copy.  Rows past V and elements past
+ * D are zero.  lms_lmhead_sample_mxfp4 then computes logits y[b][v] = sum_d H[b][d] W[v][d] with
+ * fp32 accumulation; everything after that is lms_lmhead_sample's (same noise, transform, race,
+ * statuses and workspace: lms_workspace_bytes(LMS_OP_LMHEAD, ...)).  The weights stream at 0.53
+ * bytes each and are rebuilt on chip as exact bf16 values; that is exact for scale codes 3..252
+ * (2^-124 .. 2^125), the range any real weight matrix quantises to.
+ * Requirements: D % 32 == 0, D <= 65536; lms_lmhead_sample_mxfp4: ldh as for lms_lmhead_sample,
+ * H and Wt 16-byte aligned, Wt_bytes >= lms_mxfp4_tiled_bytes(V, D), path AUTO or TCGEN05. */
+size_t lms_mxfp4_tiled_bytes(int64_t V, int64_t D);
+lms_status lms_mxfp4_pack(const void* W4, int64_t ldw4, const void* S, int64_t lds, int64_t V, int64_t D,
+                          void* Wt, size_t Wt_bytes, void* stream);
+lms_status lms_lmhead_sample_mxfp4(const void* H, int64_t ldh, const void* Wt, size_t Wt_bytes, int64_t B,
+                                   int64_t D, int64_t V, const lms_sample_params* params, int64_t* out,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* Gumbel-top-k of the fused path: k draws without replacement per row (FlashSampling
  * "Limitations" and "Future directions": sampling without replacement by Gumbel-top-k, useful for
  * beam search).  The perturbed scores s = (y + bias) / T + g are lms_lmhead_sample's, with the

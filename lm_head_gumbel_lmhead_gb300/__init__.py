@@ -101,6 +101,13 @@ def lib() -> ctypes.CDLL:
             L.lms_lmhead_sample_fp8.argtypes = [P, i64, P, i64, P, i64, i64, i64,
                                                 ctypes.POINTER(SampleParams), P, P, sz, P]
             L.lms_lmhead_sample_fp8.restype = i32
+            L.lms_mxfp4_tiled_bytes.argtypes = [i64, i64]
+            L.lms_mxfp4_tiled_bytes.restype = sz
+            L.lms_mxfp4_pack.argtypes = [P, i64, P, i64, i64, i64, P, sz, P]
+            L.lms_mxfp4_pack.restype = i32
+            L.lms_lmhead_sample_mxfp4.argtypes = [P, i64, P, sz, i64, i64, i64,
+                                                  ctypes.POINTER(SampleParams), P, P, sz, P]
+            L.lms_lmhead_sample_mxfp4.restype = i32
             L.lms_sample_from_logits_filtered.argtypes = [P, i32, i64, i64, i64,
                                                           ctypes.POINTER(SampleParams),
                                                           ctypes.POINTER(FilterParams), P, P]
@@ -381,6 +388,60 @@ def prepare_lmhead_sample_fp8(H: torch.Tensor, W8: torch.Tensor, w_scale: torch.
     return Prepared(lib().lms_lmhead_sample_fp8, args,
                     (H, W8, w_scale, temperature, seeds, positions, bias, mask, row_status,
                      workspace, p), out)
+
+
+def mxfp4_pack(W4: torch.Tensor, S: torch.Tensor, stream=None) -> torch.Tensor:
+    """The library's tiled MXFP4 weights from the logical layout: W4 uint8 [V, D/2] packed E2M1
+    codes (element d in the low nibble of byte d/2 when d is even), S uint8 [D/32, V] UE8M0 block
+    scales (any row stride >= V), both on the GPU.  Returns uint8 [lms_mxfp4_tiled_bytes(V, D)]."""
+    if W4.dtype != torch.uint8 or S.dtype != torch.uint8 or W4.dim() != 2 or S.dim() != 2:
+        raise TypeError("W4 and S must be 2-D uint8 tensors")
+    V, D = W4.shape[0], W4.shape[1] * 2
+    if S.shape[0] * 32 != D or S.shape[1] != V:
+        raise ValueError(f"S must be [{D // 32}, {V}] for W4 [{V}, {D // 2}]")
+    if W4.stride(1) != 1 or S.stride(1) != 1 or not W4.is_cuda or S.device != W4.device:
+        raise ValueError("W4 and S must be row-major CUDA tensors on one device")
+    n = int(lib().lms_mxfp4_tiled_bytes(V, D))
+    Wt = torch.empty(max(n, 1), dtype=torch.uint8, device=W4.device)
+    _check(lib().lms_mxfp4_pack(_ptr(W4), W4.stride(0), _ptr(S), S.stride(0), V, D, _ptr(Wt), n,
+                                _stream(stream)))
+    return Wt
+
+
+def lmhead_sample_mxfp4(H: torch.Tensor, Wt: torch.Tensor, V: int, *, temperature=None, seeds=None,
+                        positions=None, bias=None, mask=None, base_seed: int = 0, offset: int = 0,
+                        wide: bool = False, out=None, workspace=None, row_status=None,
+                        timeout_ms: int = 0, debug_flags: int = 0, stream=None) -> torch.Tensor:
+    """lmhead_sample with MXFP4 weights (W4A16): Wt the tiled weights of a V x D matrix
+    (mxfp4_pack), H bf16 [B, D].  The workspace is lmhead_sample's (workspace_bytes(OP_LMHEAD, ...))."""
+    return prepare_lmhead_sample_mxfp4(
+        H, Wt, V, temperature=temperature, seeds=seeds, positions=positions, bias=bias, mask=mask,
+        base_seed=base_seed, offset=offset, wide=wide, out=out, workspace=workspace,
+        row_status=row_status, timeout_ms=timeout_ms, debug_flags=debug_flags, stream=stream)()
+
+
+def prepare_lmhead_sample_mxfp4(H: torch.Tensor, Wt: torch.Tensor, V: int, *, temperature=None,
+                                seeds=None, positions=None, bias=None, mask=None, base_seed: int = 0,
+                                offset: int = 0, wide: bool = False, out=None, workspace=None,
+                                row_status=None, timeout_ms: int = 0, debug_flags: int = 0,
+                                stream=None) -> Prepared:
+    """lmhead_sample_mxfp4's call, checked and marshalled once (see Prepared)."""
+    if H.dtype != torch.bfloat16 or H.dim() != 2 or H.stride(1) != 1:
+        raise TypeError("H must be a row-major bfloat16 [B, D] tensor")
+    if Wt.dtype != torch.uint8 or not H.is_cuda or Wt.device != H.device:
+        raise ValueError("Wt must be the uint8 tiled weights on H's device")
+    B, D = H.shape
+    dev = H.device
+    p = _params(B, dev, temperature, seeds, positions, bias, mask, base_seed, offset, wide, 0,
+                PATH_AUTO, row_status, timeout_ms, debug_flags)
+    if out is None:
+        out = torch.empty(B, dtype=torch.int64, device=dev)
+    if workspace is None:
+        workspace = torch.empty(workspace_bytes(OP_LMHEAD, B, D, V), dtype=torch.uint8, device=dev)
+    args = (_ptr(H), H.stride(0), _ptr(Wt), Wt.numel(), B, D, V, ctypes.byref(p), _ptr(out),
+            _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    return Prepared(lib().lms_lmhead_sample_mxfp4, args,
+                    (H, Wt, temperature, seeds, positions, bias, mask, row_status, workspace, p), out)
 
 
 def split_workspace_fp8(ws: torch.Tensor, B: int, D: int, n_tiles: int):

@@ -140,16 +140,30 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            // FP8 inputs: H8 is written by the quantisation kernel this launch may overlap
-            if (kFp8) pdl_wait_primary();
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_h = l2_policy_evict_last();
             uint32_t issued = 0, issued_parity = 0;   // per-stage: load in flight, its phase
             int stage = 0;
             uint32_t phase = 0;
             bool first = true;
+            // FP8 inputs: H8 is written by the quantisation kernel this launch overlaps.  The W
+            // loads do not depend on it, so the first stages of the ring are filled with W before
+            // the wait, and their H loads (each stage's barrier expects both) follow it.
+            bool h_ready = !kFp8;
+            uint32_t h_pending = 0;                   // stages whose H load waits for the quantiser
+            int h_kx[kMaxStages];
+            auto release_h = [&]() {
+                pdl_wait_primary();
+                for (int s = 0; s < S; ++s)
+                    if (h_pending & (1u << s))
+                        tma_load_2d(base_addr + L.stages_off + s * prm.stage_bytes + kWStageBytes, &tmH,
+                                    h_kx[s], static_cast<int>(a.row0), full_bar(s), pol_h);
+                h_pending = 0;
+                h_ready = true;
+            };
             for (int64_t tile = blockIdx.x; tile < nt && *err == 0; tile += gridDim.x) {
                 for (int kc = 0; kc < prm.nk; ++kc) {
+                    if (!h_ready && (h_pending & (1u << stage))) release_h();   // the ring is full
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, prm.timeout_ns, err)) {
                         *err = 1;
                         break;
@@ -164,14 +178,20 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
                         const int kx = kc * (kFp8 ? 2 * kBK : kBK);
                         tma_load_2d(dst, &tmW, kx, static_cast<int>(tile * kTileV),
                                     full_bar(stage), pol_w);
-                        tma_load_2d(dst + kWStageBytes, &tmH, kx, static_cast<int>(a.row0),
-                                    full_bar(stage), pol_h);
+                        if (h_ready) {
+                            tma_load_2d(dst + kWStageBytes, &tmH, kx, static_cast<int>(a.row0),
+                                        full_bar(stage), pol_h);
+                        } else {
+                            h_kx[stage] = kx;
+                            h_pending |= 1u << stage;
+                        }
                         issued |= 1u << stage;
                         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     }
                     if (++stage == S) { stage = 0; phase ^= 1u; }
                 }
             }
+            if (!h_ready) release_h();               // fewer loads than stages, or an error
             // Drain: every copy this thread started must land before the CTA may exit.
             for (int s = 0; s < S; ++s)
                 if (issued & (1u << s))

@@ -500,6 +500,79 @@ lms_status lms_lmhead_sample_fp8(const void* H, int64_t ldh, const void* W8, int
     return LMS_OK;
 }
 
+size_t lms_mxfp4_tiled_bytes(int64_t V, int64_t D) {
+    if (V <= 0 || V > kMaxV || D <= 0 || D > 65536 || D % 32 != 0) return 0;
+    return lms::mxfp4_tiled_bytes(V, D);
+}
+
+lms_status lms_mxfp4_pack(const void* W4, int64_t ldw4, const void* S, int64_t lds, int64_t V, int64_t D,
+                          void* Wt, size_t Wt_bytes, void* stream) {
+    g_last_error[0] = '\0';
+    if (W4 == nullptr || S == nullptr || Wt == nullptr)
+        return fail(LMS_ERR_INVALID_ARG, "W4, S and Wt are required");
+    const size_t need = lms_mxfp4_tiled_bytes(V, D);
+    if (need == 0)
+        return fail(LMS_ERR_INVALID_ARG, "need 0 < V < 2^31 and 0 < D <= 65536 with D a multiple of 32");
+    if (ldw4 < D / 2 || lds < V) return fail(LMS_ERR_INVALID_ARG, "ldw4 must be >= D/2 and lds >= V");
+    if (reinterpret_cast<uintptr_t>(Wt) % 16 != 0) return fail(LMS_ERR_UNSUPPORTED, "Wt must be 16-byte aligned");
+    if (Wt_bytes < need) return fail(LMS_ERR_WORKSPACE, "Wt needs %zu bytes", need);
+    const cudaError_t e = lms::launch_mxfp4_pack(static_cast<const uint8_t*>(W4), ldw4,
+                                                 static_cast<const uint8_t*>(S), lds, V, D,
+                                                 static_cast<uint8_t*>(Wt), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "MXFP4 pack launch");
+    return LMS_OK;
+}
+
+lms_status lms_lmhead_sample_mxfp4(const void* H, int64_t ldh, const void* Wt, size_t Wt_bytes, int64_t B,
+                                   int64_t D, int64_t V, const lms_sample_params* params, int64_t* out,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+    g_last_error[0] = '\0';
+    if (H == nullptr || Wt == nullptr || out == nullptr)
+        return fail(LMS_ERR_INVALID_ARG, "H, Wt and out are required");
+    Tiling t;
+    lms_status st = make_tiling(LMS_OP_LMHEAD, B, D, V, params ? params->tile_v : 0, &t);
+    if (st != LMS_OK) return st;
+    if ((st = check_params(params, V)) != LMS_OK) return st;
+    if (D % 32 != 0) return fail(LMS_ERR_UNSUPPORTED, "D must be a multiple of 32 (D=%lld)", (long long)D);
+    if (D > 65536) return fail(LMS_ERR_UNSUPPORTED, "D must be <= 65536");
+    if (ldh < D || ldh % 8 != 0) return fail(LMS_ERR_UNSUPPORTED, "ldh must be >= D and a multiple of 8");
+    if (Wt_bytes < lms::mxfp4_tiled_bytes(V, D))
+        return fail(LMS_ERR_INVALID_ARG, "Wt holds %zu bytes, the tiled weights of V x D need %zu", Wt_bytes,
+                    lms::mxfp4_tiled_bytes(V, D));
+    if (reinterpret_cast<uintptr_t>(H) % 16 != 0 || reinterpret_cast<uintptr_t>(Wt) % 16 != 0)
+        return fail(LMS_ERR_UNSUPPORTED, "H and Wt must be 16-byte aligned");
+    if (params->path != LMS_PATH_AUTO && params->path != LMS_PATH_TCGEN05)
+        return fail(LMS_ERR_UNSUPPORTED, "the MXFP4 path runs on the tcgen05 kernel only");
+    if (workspace == nullptr || workspace_bytes < t.workspace)
+        return fail(LMS_ERR_WORKSPACE, "workspace of %zu bytes needed", t.workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool wide = params->noise_mode == LMS_NOISE_WIDE53;
+    lms::SampleArgs a = make_args(params, B, V, t, workspace);
+    const uint32_t timeout_ms = params->timeout_ms ? params->timeout_ms : 2000u;
+    cudaError_t e;
+    // batches above 128 rows run as launches of <= 128 rows: the converted-tile and H rings of a
+    // launch fit in shared memory up to that width
+    constexpr int64_t kMxMaxBatchPerLaunch = 128;
+    for (int64_t r0 = 0; r0 < B; r0 += kMxMaxBatchPerLaunch) {
+        const int64_t nb = (B - r0 < kMxMaxBatchPerLaunch) ? B - r0 : kMxMaxBatchPerLaunch;
+        const int n_pad = static_cast<int>(nb < 16 ? 16 : (nb + 15) / 16 * 16);
+        CUtensorMap tmH;
+        if ((st = encode_bf16_map(&tmH, H, B, D, ldh, n_pad)) != LMS_OK) return st;
+        lms::SampleArgs ac = a;
+        ac.B = nb;
+        ac.row0 = r0;
+        ac.cand_score = a.cand_score + r0 * t.n_tiles;
+        ac.cand_index = a.cand_index + r0 * t.n_tiles;
+        e = lms::launch_lmhead_mx(static_cast<const uint8_t*>(Wt), tmH, D, n_pad, wide, timeout_ms,
+                                  params->debug_flags, ac, s);
+        if (e != cudaSuccess) return cuda_fail(e, "tcgen05 MXFP4 Stage-1 launch");
+    }
+    e = lms::launch_stage2(a.cand_score, a.cand_index, t.n_tiles, B, params->temperature, out,
+                           params->row_status, a.status_bits, s);
+    if (e != cudaSuccess) return cuda_fail(e, "Stage-2 launch");
+    return LMS_OK;
+}
+
 lms_status lms_sample_from_logits(const void* logits, int32_t dtype, int64_t ld, int64_t B,
                                   int64_t V, const lms_sample_params* params, int64_t* out,
                                   void* workspace, size_t workspace_bytes, void* stream) {

@@ -124,6 +124,16 @@ cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int
                              const SampleArgs& a, cudaStream_t stream, bool fp8 = false);
 // (a.topk > 0 selects the Gumbel-top-k epilogue: bf16 only.)
 
+// The MXFP4-weight path (W4A16).  Wt is the tiled format mxfp4_pack writes (mxfp4_tiled_bytes(V, D)
+// bytes: one contiguous 4352-byte block per (128-row tile, 64-element K chunk)); tmH as for
+// launch_lmhead_tc.  B <= 128 per launch.
+size_t mxfp4_tiled_bytes(int64_t V, int64_t D);
+cudaError_t launch_mxfp4_pack(const uint8_t* W4, int64_t ldw4, const uint8_t* S, int64_t lds, int64_t V,
+                              int64_t D, uint8_t* out, cudaStream_t stream);
+cudaError_t launch_lmhead_mx(const uint8_t* Wt, const CUtensorMap& tmH, int64_t D, int n_pad, bool wide,
+                             uint32_t timeout_ms, uint32_t debug_flags, const SampleArgs& a,
+                             cudaStream_t stream);
+
 // The CTA-pair tcgen05 path (cta_group::2, M = 256): tmH boxes are 64 x (n_pad / 2).
 cudaError_t launch_lmhead_tc_pair(const CUtensorMap& tmW, const CUtensorMap& tmH, int64_t D,
                                   int n_pad, bool wide, uint32_t timeout_ms, uint32_t debug_flags,

@@ -189,6 +189,31 @@ def test_topk_fp8_filtered_noalloc_host_validation(L):
     assert st == WS and b"static scratch" in L.lms_last_error()
 
 
+def test_mxfp4_host_validation(L):
+    INV, UNS, WS = lms.LMS_ERR_INVALID_ARG, lms.LMS_ERR_UNSUPPORTED, lms.LMS_ERR_WORKSPACE
+    # one 4352-byte block per (128-row tile, 64-element K chunk)
+    assert L.lms_mxfp4_tiled_bytes(1000, 96) == 8 * 2 * 4352
+    assert L.lms_mxfp4_tiled_bytes(151936, 4096) == 1187 * 64 * 4352
+    assert L.lms_mxfp4_tiled_bytes(1000, 48) == 0 and L.lms_mxfp4_tiled_bytes(0, 64) == 0
+    need = L.lms_mxfp4_tiled_bytes(1000, 64)
+
+    def pack(ldw4=32, lds=1000, Wt=FAKE, n=need, D=64):
+        return L.lms_mxfp4_pack(FAKE, ldw4, FAKE, lds, 1000, D, Wt, n, None)
+    assert pack(Wt=None) == INV and pack(D=48) == INV
+    assert pack(ldw4=31) == INV and pack(lds=999) == INV
+    assert pack(Wt=ctypes.c_void_p(0x100008)) == UNS and pack(n=need - 1) == WS
+
+    def mx(D=64, Wt=FAKE, n=need, ws_bytes=1 << 24, p=None):
+        p = _params() if p is None else p
+        return L.lms_lmhead_sample_mxfp4(FAKE, 64, Wt, n, 4, D, 1000, ctypes.byref(p), FAKE, FAKE,
+                                         ws_bytes, None)
+    assert mx(Wt=None) == INV and mx(n=need - 1) == INV
+    assert mx(D=48) == UNS                              # D must be a multiple of 32
+    assert mx(Wt=ctypes.c_void_p(0x100008)) == UNS
+    assert mx(p=_params(path=lms.PATH_GEMV)) == UNS
+    assert mx(ws_bytes=lms.workspace_bytes(lms.OP_LMHEAD, 4, 64, 1000) - 1) == WS
+
+
 def test_read_status_rejects_a_missing_workspace(L):
     bits = ctypes.c_uint32(7)
     assert L.lms_read_status(None, None, ctypes.byref(bits)) == lms.LMS_ERR_INVALID_ARG
