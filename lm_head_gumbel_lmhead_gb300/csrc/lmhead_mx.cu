@@ -5,29 +5,32 @@
 // elements, two per byte, with one UE8M0 scale per block of 32 elements along K, streamed at
 // 0.53 bytes per weight.  The activations stay bf16.  Stage 1 is the same method as the bf16
 // kernel (logits on chip, transform, Philox noise, per-tile argmax); only the weight operand
-// differs: it is rebuilt in shared memory as the exact bf16 values E2M1 x 2^(s - 127), in the
-// 128-byte-swizzled K-major layout tcgen05.mma kind::f16 reads, so the tensor cores run the same
-// bf16 x bf16 -> fp32 contraction.
+// differs: it is rebuilt as the exact bf16 values E2M1 x 2^(s - 127) in tensor memory, which
+// tcgen05.mma kind::f16 reads as its A operand (M = 128 vocabulary rows in the 128 TMEM lanes,
+// two bf16 of K per 32-bit column), so the tensor cores run the same bf16 x bf16 -> fp32
+// contraction and the rebuilt weights never pass through shared memory.
 //
 // Warp roles (one persistent CTA per SM):
 //   warp 0           bulk-copy producer of the packed weights: the library's tiled MXFP4 format
 //                    (lms_mxfp4_pack) stores each (128-row vocabulary tile, 64-element K chunk)
 //                    as one contiguous 4352-byte block, 4 KB of codes then 256 bytes of scales, so
 //                    one cp.async.bulk of contiguous bytes fills a ring-A stage.
-//   warp 1           allocates TMEM; one lane issues tcgen05.mma (M = 128 vocabulary rows,
-//                    N = n_pad batch rows, K = 16 per instruction) into two TMEM accumulators.
+//   warp 1           allocates TMEM; one lane issues tcgen05.mma (M = 128, N = n_pad batch rows,
+//                    K = 16 per instruction, A from TMEM, B = H from shared memory) into two TMEM
+//                    accumulators.
 //   warp 2           TMA producer of H [n_pad x 64] bf16 chunks into ring H.
-//   warps 3..10      converters: converter w owns the K chunks j = w, w + 8, ... of the CTA's
-//                    sequence and turns each whole chunk (ring-A stage: 128 rows x 64 codes and
-//                    their scales) into the bf16 weight tile of ring C (byte permutes and one
-//                    bf16x2 multiply per pair of weights), then a proxy fence so that the tensor
-//                    cores see it.  Eight chunks are converted at once, each by one warp.
+//   warps 3..10      converters, in two groups of four: group g takes the chunks j = g, g + 2, ...
+//                    of the CTA's sequence; within a group, warp w (w % 4 = q, the TMEM lane
+//                    quarter a warp may access) rebuilds rows 32 q .. 32 q + 31 of the chunk, one
+//                    row of 64 weights per lane (byte permutes and one bf16x2 multiply per pair),
+//                    and stores them with tcgen05.st into the chunk's TMEM slot.
 //   warps 11..18     epilogue: as in the bf16 kernel (transform, noise, argmax per tile).
 // Ring A (packed codes and scales, 4.25 KB a stage) is deep so that enough weight bytes are in
-// flight to keep HBM busy; ring C holds converted tiles (16 KB) and ring H the activations
-// (n_pad * 128 bytes).  Every wait is bounded in time; a CTA whose wait runs out flags the
-// error, drains its copies and MMAs, poisons its remaining candidates (row status 3), frees
-// TMEM and exits.
+// flight to keep HBM busy.  TMEM holds eight rebuilt-weight slots of 32 columns (four per group)
+// in columns 0..255 and the two accumulators from column 256; ring H has one activation stage per
+// slot, and one tcgen05.commit per chunk frees both.  Every wait is bounded in time; a CTA whose
+// wait runs out flags the error, drains its copies and MMAs, poisons its remaining candidates
+// (row status 3), frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -42,45 +45,47 @@ namespace {
 using namespace tc;
 
 constexpr int kMxConvWarps = 8;
+constexpr int kMxGroups = 2;                           // converter groups of four warps
 constexpr int kMxEpiWarps = 8;
 constexpr int kMxFirstConv = 3;
 constexpr int kMxFirstEpi = kMxFirstConv + kMxConvWarps;
 constexpr int kMxThreads = 32 * (kMxFirstEpi + kMxEpiWarps);
-// Ring A and ring C have a multiple of kMxConvWarps stages: then chunks j and j + S, which share a
-// slot, are converted by the same warp, in order, so no warp can wait on a slot's next phase while
-// its current one is incomplete.
-constexpr int kMaxStagesA = 16;
-constexpr int kStagesC = kMxConvWarps;
-constexpr int kMaxStagesH = 8;
+// Ring A has an even number of stages: then stage k is only ever read by group k % 2, so no
+// warp can wait on a stage's next phase while its current one is incomplete.
+constexpr int kMaxStagesA = 32;
+// TMEM: slot t (group t / 4, the group's slot t % 4) holds one rebuilt 128 x 64 bf16 chunk in
+// columns 32 t .. 32 t + 31; the accumulators start at column 256 (n_pad <= 128 each).
+constexpr int kSlotsPerGroup = 4;
+constexpr int kSlots = kMxGroups * kSlotsPerGroup;
+constexpr uint32_t kSlotCols = kBK / 2;
+constexpr uint32_t kAccCol0 = kSlots * kSlotCols;
+constexpr uint32_t kMxTmemCols = 512;
 constexpr uint32_t kW4StageBytes = kTileV * kBK / 2;   // 128 rows x 64 codes = 4 KB
 constexpr uint32_t kS4StageBytes = 2 * kTileV;         // 2 scale blocks x 128 rows
 constexpr uint32_t kAStageBytes = kW4StageBytes + kS4StageBytes;   // one tiled block
-constexpr int kUnitsPerLane = 2 * kTileV / 32;        // (row, scale block) units of a chunk per lane
 
 struct MxParams {
     SampleArgs a;
     int nk;              // K chunks of 64, ceil(D / 64)
     int n_pad;
-    int stages_a, stages_c, stages_h;
+    int stages_a;
     uint32_t h_stage_bytes;   // n_pad * 128
-    uint32_t tmem_cols;
     uint64_t timeout_ns;
     uint32_t debug_flags;
 };
 
-// Shared memory (offsets from a 1024-byte aligned base): ring C (converted 16 KB tiles) and ring H
-// (activation chunks), both 1024-aligned for the 128-byte swizzle; ring A's packed codes and
-// scales; barriers; then the epilogue's buffers.
+// Shared memory (offsets from a 1024-byte aligned base): ring H (activation chunks, one stage per
+// TMEM slot, 1024-aligned for the 128-byte swizzle); ring A's packed codes and scales; barriers;
+// then the epilogue's buffers.
 struct MxLayout {
-    uint32_t c_off, h_off, a_off, bars_off, misc_off, rows_off, red_off, tr_off, total;
-    __host__ __device__ MxLayout(int sa, int sc, int sh, uint32_t h_stage_bytes, int n_pad) {
-        c_off = 0;
-        h_off = c_off + sc * kWStageBytes;
-        a_off = h_off + sh * h_stage_bytes;
+    uint32_t h_off, a_off, bars_off, misc_off, rows_off, red_off, tr_off, total;
+    __host__ __device__ MxLayout(int sa, uint32_t h_stage_bytes, int n_pad) {
+        h_off = 0;
+        a_off = h_off + kSlots * h_stage_bytes;
         bars_off = a_off + sa * kAStageBytes;
-        // fullA, emptyA [SA]; fullC, emptyC [SC]; fullH, emptyH [SH]; acc_full[2], acc_empty[2],
-        // drain
-        misc_off = bars_off + (2 * sa + 2 * sc + 2 * sh + 5) * 8;
+        // fullA, emptyA [SA]; fullC (slot written, count 4), emptyC (slot and its H stage free,
+        // one commit), fullH [kSlots]; acc_full[2], acc_empty[2], drain
+        misc_off = bars_off + (2 * sa + 3 * kSlots + 5) * 8;
         rows_off = (misc_off + 16 + 15) & ~15u;   // misc: tmem slot, error flag
         red_off = rows_off + n_pad * static_cast<uint32_t>(sizeof(RowParams));
         tr_off = red_off + n_pad * 8;
@@ -171,6 +176,44 @@ __global__ void __launch_bounds__(256) mxfp4_pack_kernel(const uint8_t* __restri
     }
 }
 
+// 32 TMEM lanes (lane = thread) x 32 consecutive 32-bit columns <- 32 registers per thread, then
+// wait until the stores have completed.
+__device__ __forceinline__ void tmem_store_32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+        "%29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+        "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// True in exactly one lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, bf16 inputs, fp32 accumulate; A is M x 16 in TMEM (row m in
+// lane m, two K elements per 32-bit column, the lower K in the low half); issued by one thread.
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 template <bool kWide, bool kPlain>
 __global__ void __launch_bounds__(kMxThreads, 1)
     lmhead_mx_kernel(const uint8_t* __restrict__ Wt, const __grid_constant__ CUtensorMap tmH,
@@ -179,10 +222,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
     uint8_t* base = smem_raw + (base_addr - raw_addr);
-    const MxLayout L(prm.stages_a, prm.stages_c, prm.stages_h, prm.h_stage_bytes, prm.n_pad);
+    const MxLayout L(prm.stages_a, prm.h_stage_bytes, prm.n_pad);
 
     const SampleArgs& a = prm.a;
-    const int SA = prm.stages_a, SC = prm.stages_c, SH = prm.stages_h;
+    const int SA = prm.stages_a;
     const int n_pad = prm.n_pad;
     const int B = static_cast<int>(a.B);
     const int64_t nt = a.n_tiles;
@@ -191,11 +234,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     const uint32_t bar0 = base_addr + L.bars_off;
     auto fullA = [&](int s) { return bar0 + 8u * s; };
     auto emptyA = [&](int s) { return bar0 + 8u * (SA + s); };
-    auto fullC = [&](int s) { return bar0 + 8u * (2 * SA + s); };
-    auto emptyC = [&](int s) { return bar0 + 8u * (2 * SA + SC + s); };
-    auto fullH = [&](int s) { return bar0 + 8u * (2 * SA + 2 * SC + s); };
-    auto emptyH = [&](int s) { return bar0 + 8u * (2 * SA + 2 * SC + SH + s); };
-    const uint32_t acc0 = bar0 + 8u * (2 * SA + 2 * SC + 2 * SH);
+    auto fullC = [&](int t) { return bar0 + 8u * (2 * SA + t); };
+    auto emptyC = [&](int t) { return bar0 + 8u * (2 * SA + kSlots + t); };
+    auto fullH = [&](int t) { return bar0 + 8u * (2 * SA + 2 * kSlots + t); };
+    const uint32_t acc0 = bar0 + 8u * (2 * SA + 3 * kSlots);
     auto accf_bar = [&](int ab) { return acc0 + 8u * ab; };
     auto acce_bar = [&](int ab) { return acc0 + 8u * (2 + ab); };
     const uint32_t drain_bar = acc0 + 32u;
@@ -207,15 +249,12 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < SA; ++s) {
             mbar_init(fullA(s), 1);
-            mbar_init(emptyA(s), 1);
+            mbar_init(emptyA(s), 4);             // the four warps of the stage's group
         }
-        for (int s = 0; s < SC; ++s) {
-            mbar_init(fullC(s), 1);
-            mbar_init(emptyC(s), 1);
-        }
-        for (int s = 0; s < SH; ++s) {
-            mbar_init(fullH(s), 1);
-            mbar_init(emptyH(s), 1);
+        for (int t = 0; t < kSlots; ++t) {
+            mbar_init(fullC(t), 4);
+            mbar_init(emptyC(t), 1);
+            mbar_init(fullH(t), 1);
         }
         for (int ab = 0; ab < 2; ++ab) {
             mbar_init(accf_bar(ab), 1);
@@ -235,24 +274,27 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                                   a.row0 + b);
         red[b] = 0ull;
     }
-    if (warp == 1) tmem_alloc(base_addr + L.misc_off, prm.tmem_cols);
+    if (warp == 1) tmem_alloc(base_addr + L.misc_off, kMxTmemCols);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
-    // this CTA's K chunks, in order: chunk j is K chunk j % nk of its (j / nk)-th tile
+    // this CTA's K chunks, in order: chunk j is K chunk j % nk of its (j / nk)-th tile, converted
+    // by group j % 2 into that group's slots in turn.  Every role walks them with incremental
+    // counters (no division in the loops).
     const int64_t my_tiles = nt > blockIdx.x ? (nt - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     const int64_t n_chunks = my_tiles * prm.nk;
-    auto chunk_tile = [&](int64_t j) { return blockIdx.x + (j / prm.nk) * static_cast<int64_t>(gridDim.x); };
 
     if (warp == 0) {
-        // ---------------- TMA producer: packed weights and scales (ring A) ----------------
+        // ---------------- bulk-copy producer: packed weights and scales (ring A) ----------------
         if (lane == 0) {
             const uint64_t pol_w = l2_policy_evict_first();
             uint32_t issued = 0, issued_parity = 0;
+            int stage = 0;
+            uint32_t phase = 0;
+            int kc = 0;
+            int64_t tile = blockIdx.x;
             for (int64_t j = 0; j < n_chunks && *err == 0; ++j) {
-                const int stage = static_cast<int>(j % SA);
-                const uint32_t phase = static_cast<uint32_t>((j / SA) & 1);
                 if (!mbar_wait(emptyA(stage), phase ^ 1u, prm.timeout_ns, err)) {
                     *err = 1;
                     break;
@@ -260,123 +302,168 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                 const bool withhold = j == 0 && blockIdx.x == 0 &&
                                       (prm.debug_flags & LMS_DEBUG_WITHHOLD_FIRST_LOAD);
                 if (!withhold) {
-                    const int64_t block = chunk_tile(j) * prm.nk + j % prm.nk;
+                    const int64_t block = tile * prm.nk + kc;
                     mbar_arrive_expect_tx(fullA(stage), kAStageBytes);
                     bulk_load(base_addr + L.a_off + stage * kAStageBytes, Wt + block * kAStageBytes,
                               kAStageBytes, fullA(stage), pol_w);
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                 }
+                if (++stage == SA) { stage = 0; phase ^= 1u; }
+                if (++kc == prm.nk) { kc = 0; tile += gridDim.x; }
             }
             for (int s = 0; s < SA; ++s)
                 if (issued & (1u << s))
                     mbar_wait(fullA(s), (issued_parity >> s) & 1u, prm.timeout_ns, nullptr);
         }
     } else if (warp == 2) {
-        // ---------------- TMA producer: activations (ring H) ----------------
+        // ---------------- TMA producer: activations (ring H, one stage per TMEM slot) ----------------
         if (lane == 0) {
             const uint64_t pol_h = l2_policy_evict_last();
             uint32_t issued = 0, issued_parity = 0;
+            // slot and phase of each group's next chunk (group 0's in t0/p0, group 1's in t1/p1)
+            int t0 = 0, t1 = kSlotsPerGroup;
+            uint32_t p0 = 0, p1 = 0;
+            int kc = 0;
             for (int64_t j = 0; j < n_chunks && *err == 0; ++j) {
-                const int stage = static_cast<int>(j % SH);
-                const uint32_t phase = static_cast<uint32_t>((j / SH) & 1);
-                if (!mbar_wait(emptyH(stage), phase ^ 1u, prm.timeout_ns, err)) {
+                const bool g1 = (j & 1) != 0;
+                const int t = g1 ? t1 : t0;
+                const uint32_t pt = g1 ? p1 : p0;
+                // the slot's previous chunk has been consumed by the tensor cores
+                if (!mbar_wait(emptyC(t), pt ^ 1u, prm.timeout_ns, err)) {
                     *err = 1;
                     break;
                 }
-                mbar_arrive_expect_tx(fullH(stage), prm.h_stage_bytes);
-                tma_load_2d(base_addr + L.h_off + stage * prm.h_stage_bytes, &tmH,
-                            static_cast<int>(j % prm.nk) * kBK, static_cast<int>(a.row0), fullH(stage), pol_h);
-                issued |= 1u << stage;
-                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                mbar_arrive_expect_tx(fullH(t), prm.h_stage_bytes);
+                tma_load_2d(base_addr + L.h_off + t * prm.h_stage_bytes, &tmH, kc * kBK,
+                            static_cast<int>(a.row0), fullH(t), pol_h);
+                issued |= 1u << t;
+                issued_parity = (issued_parity & ~(1u << t)) | (pt << t);
+                if (g1) {
+                    if (++t1 == kSlots) { t1 = kSlotsPerGroup; p1 ^= 1u; }
+                } else {
+                    if (++t0 == kSlotsPerGroup) { t0 = 0; p0 ^= 1u; }
+                }
+                if (++kc == prm.nk) kc = 0;
             }
-            for (int s = 0; s < SH; ++s)
-                if (issued & (1u << s))
-                    mbar_wait(fullH(s), (issued_parity >> s) & 1u, prm.timeout_ns, nullptr);
+            for (int t = 0; t < kSlots; ++t)
+                if (issued & (1u << t))
+                    mbar_wait(fullH(t), (issued_parity >> t) & 1u, prm.timeout_ns, nullptr);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            const uint32_t idesc = mma_idesc_bf16(n_pad, kTileV);
-            bool ok = true;
-            for (int64_t i = 0; i < my_tiles && ok; ++i) {
-                const int ab = static_cast<int>(i & 1);
-                const uint32_t use_parity = static_cast<uint32_t>((i >> 1) & 1);
-                if (!mbar_wait(acce_bar(ab), use_parity ^ 1u, prm.timeout_ns, err)) { ok = false; break; }
+        // The whole warp walks the loop, converged, so that the slot counters, TMEM addresses and
+        // descriptors stay warp-uniform; one elected lane issues the tcgen05 instructions.
+        const bool leader = elect_one();
+        const uint32_t idesc = mma_idesc_bf16(n_pad, kTileV);
+        bool ok = true;
+        int t0 = 0, t1 = kSlotsPerGroup;       // as in the activation producer
+        uint32_t p0 = 0, p1 = 0;
+        bool g1 = false;
+        for (int64_t i = 0; i < my_tiles && ok; ++i) {
+            const int ab = static_cast<int>(i & 1);
+            const uint32_t use_parity = static_cast<uint32_t>((i >> 1) & 1);
+            if (!__all_sync(0xffffffffu, mbar_wait(acce_bar(ab), use_parity ^ 1u, prm.timeout_ns, err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t d_tmem = tmem_base + kAccCol0 + static_cast<uint32_t>(ab * n_pad);
+            for (int kc = 0; kc < prm.nk; ++kc) {
+                const int t = g1 ? t1 : t0;
+                // the group announces the slot once its rebuilt weights are stored and the
+                // chunk's activations have landed
+                if (!__all_sync(0xffffffffu, mbar_wait(fullC(t), g1 ? p1 : p0, prm.timeout_ns, err))) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * n_pad);
-                for (int kc = 0; kc < prm.nk; ++kc) {
-                    const int64_t j = i * prm.nk + kc;
-                    const int sc = static_cast<int>(j % SC), sh = static_cast<int>(j % SH);
-                    if (!mbar_wait(fullH(sh), static_cast<uint32_t>((j / SH) & 1), prm.timeout_ns, err) ||
-                        !mbar_wait(fullC(sc), static_cast<uint32_t>((j / SC) & 1), prm.timeout_ns, err)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const uint64_t adesc = kmajor_sw128_desc(base_addr + L.c_off + sc * kWStageBytes);
-                    const uint64_t bdesc = kmajor_sw128_desc(base_addr + L.h_off + sh * prm.h_stage_bytes);
+                const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(t) * kSlotCols;
+                const uint64_t bdesc = kmajor_sw128_desc(base_addr + L.h_off + t * prm.h_stage_bytes);
+                if (leader) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kc | k) != 0 ? 1u : 0u);
-                    mma_commit(emptyC(sc));
-                    mma_commit(emptyH(sh));
+                        mma_bf16_tmem_a(d_tmem, a_tmem + 8u * k, bdesc + 2u * k, idesc,
+                                        (kc | k) != 0 ? 1u : 0u);
+                    mma_commit(emptyC(t));
                 }
-                if (!ok) break;
-                mma_commit(accf_bar(ab));
+                __syncwarp();
+                if (g1) {
+                    if (++t1 == kSlots) { t1 = kSlotsPerGroup; p1 ^= 1u; }
+                } else {
+                    if (++t0 == kSlotsPerGroup) { t0 = 0; p0 ^= 1u; }
+                }
+                g1 = !g1;
             }
-            if (!ok) *err = 1;
+            if (!ok) break;
+            if (leader) mma_commit(accf_bar(ab));
+            __syncwarp();
+        }
+        if (!ok && lane == 0) *err = 1;
+        if (leader) {
             mma_commit(drain_bar);
             mbar_wait(drain_bar, 0, prm.timeout_ns, nullptr);
         }
+        __syncwarp();
     } else if (warp < kMxFirstEpi) {
-        // ---------------- converters: one whole chunk per warp at a time ----------------
-        // Converter w takes chunks j = w, w + 8, ...  Lane l converts the (row, scale block)
-        // units u = l + 32 m (m < 8) of the chunk: row r = u / 2, block k = u % 2: 16 bytes of
-        // codes (32 weights) and one scale byte, written as four 16-byte pieces of the row's
-        // 128-byte line at the 128-byte-swizzled positions (piece p of row r goes to p ^ (r % 8)),
-        // the layout a TMA load with the 128-byte swizzle would give.
-        const int cw = warp - kMxFirstConv;
+        // ---------------- converters ----------------
+        // Group g = (warp - 3) / 4 takes the chunks j = g, g + 2, ...; the warp's TMEM lane quarter
+        // q = warp % 4 gives its rows r = 32 q + lane.  Lane r reads its row's 32 code bytes (64
+        // weights) and two scale codes from the ring-A stage, rebuilds the 64 bf16 weights as 32
+        // bf16x2 words (word c = K elements 2c, 2c + 1) and stores them into TMEM lane r, columns
+        // 32 t .. 32 t + 31 of the group's current slot t.  Ring-A stage of the group's u-th
+        // chunk: g + 2 (u % (SA / 2)), phase (u / (SA / 2)) & 1.
+        const int g = (warp - kMxFirstConv) >> 2;
+        const int q = warp & 3;
+        const int r = 32 * q + lane;
+        const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
         bool ok = true;
-        for (int64_t j = cw; j < n_chunks && ok; j += kMxConvWarps) {
-            const int sa = static_cast<int>(j % SA), sc = static_cast<int>(j % SC);
-            if (!mbar_wait(fullA(sa), static_cast<uint32_t>((j / SA) & 1), prm.timeout_ns, err) ||
-                !mbar_wait(emptyC(sc), static_cast<uint32_t>(((j / SC) & 1) ^ 1), prm.timeout_ns, err)) {
+        int sa = g, idx = 0;
+        uint32_t pa = 0, pt = 0;
+        for (int64_t j = g; j < n_chunks && ok; j += kMxGroups) {
+            // every wait's outcome is made warp-uniform: tcgen05.st needs the whole warp
+            if (!__all_sync(0xffffffffu, mbar_wait(fullA(sa), pa, prm.timeout_ns, err))) {
                 ok = false;
                 break;
             }
             const uint8_t* w4 = base + L.a_off + sa * kAStageBytes;
-            const uint8_t* sf = w4 + kW4StageBytes;
-            uint4 codes[kUnitsPerLane];
-            uint32_t scale[kUnitsPerLane];
-#pragma unroll
-            for (int m = 0; m < kUnitsPerLane; ++m) {
-                const int u = lane + 32 * m;
-                codes[m] = *reinterpret_cast<const uint4*>(w4 + u * 16);   // row u/2, block u%2
-                scale[m] = sf[(u & 1) * kTileV + (u >> 1)];
-            }
-            // the codes and scales are in registers: the ring-A stage is free for the producer
+            const uint4 c0 = *reinterpret_cast<const uint4*>(w4 + r * 32);
+            const uint4 c1 = *reinterpret_cast<const uint4*>(w4 + r * 32 + 16);
+            const uint32_t s0 = w4[kW4StageBytes + r], s1 = w4[kW4StageBytes + kTileV + r];
+            // the codes and scales are in registers: this warp is done with the ring-A stage
             __syncwarp();
             if (lane == 0) mbar_arrive(emptyA(sa));
-            uint8_t* tile = base + L.c_off + sc * kWStageBytes;
+            sa += kMxGroups;
+            if (sa >= SA) { sa = g; pa ^= 1u; }
+            uint32_t v[32];
+            {
+                const __nv_bfloat162 sc0 = ue8m0_to_bf16x2(s0), sc1 = ue8m0_to_bf16x2(s1);
+                const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-            for (int m = 0; m < kUnitsPerLane; ++m) {
-                const int u = lane + 32 * m;
-                const int r = u >> 1, blk = u & 1;
-                const __nv_bfloat162 sc2 = ue8m0_to_bf16x2(scale[m]);
-                const uint32_t cw4[4] = {codes[m].x, codes[m].y, codes[m].z, codes[m].w};
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
+                for (int wd = 0; wd < 8; ++wd) {
                     uint32_t o[4];
-                    e2m1x8_to_bf16(cw4[w], sc2, o);
-                    const int piece = (4 * blk + w) ^ (r & 7);
-                    *reinterpret_cast<uint4*>(tile + r * 128 + piece * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+                    e2m1x8_to_bf16(cw[wd], wd < 4 ? sc0 : sc1, o);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) v[4 * wd + i] = o[i];
                 }
             }
-            // generic-proxy writes made visible to the tensor cores' (async proxy) reads
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            const int t = g * kSlotsPerGroup + idx;
+            // the slot's previous chunk has been consumed by the tensor cores
+            if (!__all_sync(0xffffffffu, mbar_wait(emptyC(t), pt ^ 1u, prm.timeout_ns, err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            tmem_store_32(lane_addr + static_cast<uint32_t>(t) * kSlotCols, v);
+            // the chunk's activations must have landed too before the slot is announced
+            if (!__all_sync(0xffffffffu, mbar_wait(fullH(t), pt, prm.timeout_ns, err))) {
+                ok = false;
+                break;
+            }
+            tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(fullC(sc));
+            if (lane == 0) mbar_arrive(fullC(t));
+            if (++idx == kSlotsPerGroup) { idx = 0; pt ^= 1u; }
         }
         if (!ok) *err = 1;
     } else {
@@ -402,7 +489,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                 continue;
             }
             tc_fence_after_sync();
-            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) +
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + kAccCol0 +
                                    static_cast<uint32_t>(ab * n_pad);
             epilogue_tile_columns<kMxEpiWarps, kWide, kPlain>(a, rows, red, tr, t_row, tile, quad,
                                                               col_group, lane, B);
@@ -427,7 +514,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, prm.tmem_cols);
+        tmem_dealloc(tmem_base, kMxTmemCols);
     }
 }
 
@@ -465,27 +552,17 @@ cudaError_t launch_lmhead_mx(const uint8_t* Wt, const CUtensorMap& tmH, int64_t 
     prm.nk = static_cast<int>((D + kBK - 1) / kBK);
     prm.n_pad = n_pad;
     prm.h_stage_bytes = static_cast<uint32_t>(n_pad * kBK * 2);
+    if (n_pad > 128) return cudaErrorInvalidValue;       // two accumulators in TMEM columns 256..511
     const uint32_t budget = 227u * 1024u - 1024u;        // opt-in maximum minus alignment slack
-    const uint32_t per_a = kAStageBytes;
-    const uint32_t bar_bytes = (2 * kMaxStagesA + 2 * kStagesC + 2 * kMaxStagesH + 5) * 8;
-    const uint32_t fixed = MxLayout(0, 0, 0, prm.h_stage_bytes, n_pad).total + bar_bytes;
-    // ring C: one slot per converter warp; ring H as deep as fits, from 8 down to 4; then ring A
-    // 16 deep when there is room, else 8
-    const int sc = kStagesC;
-    int sh = kMaxStagesH, sa = kMaxStagesA;
-    auto used = [&]() { return fixed + sa * per_a + sh * prm.h_stage_bytes + sc * kWStageBytes; };
-    while (used() > budget && sa > kMxConvWarps) sa -= kMxConvWarps;
-    while (used() > budget && sh > 2) --sh;
-    if (used() > budget) return cudaErrorInvalidValue;
+    const uint32_t fixed = MxLayout(0, prm.h_stage_bytes, n_pad).total + 2u * kMaxStagesA * 8u;
+    // ring A as deep as fits, an even number of stages from 32 down to 8
+    int sa = kMaxStagesA;
+    while (fixed + sa * kAStageBytes > budget && sa > 8) sa -= 2;
+    if (fixed + sa * kAStageBytes > budget) return cudaErrorInvalidValue;
     prm.stages_a = sa;
-    prm.stages_c = sc;
-    prm.stages_h = sh;
-    uint32_t cols = 32;
-    while (cols < static_cast<uint32_t>(2 * n_pad)) cols <<= 1;
-    prm.tmem_cols = cols;
     prm.timeout_ns = static_cast<uint64_t>(timeout_ms) * 1000000ull;
     prm.debug_flags = debug_flags;
-    const MxLayout L(sa, sc, sh, prm.h_stage_bytes, n_pad);
+    const MxLayout L(sa, prm.h_stage_bytes, n_pad);
     const size_t smem = L.total + 1024;
     const int sms = device_sm_count();
     const int grid = static_cast<int>(a.n_tiles < sms ? a.n_tiles : sms);

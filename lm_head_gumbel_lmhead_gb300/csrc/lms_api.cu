@@ -550,8 +550,8 @@ lms_status lms_lmhead_sample_mxfp4(const void* H, int64_t ldh, const void* Wt, s
     lms::SampleArgs a = make_args(params, B, V, t, workspace);
     const uint32_t timeout_ms = params->timeout_ms ? params->timeout_ms : 2000u;
     cudaError_t e;
-    // batches above 128 rows run as launches of <= 128 rows: the converted-tile and H rings of a
-    // launch fit in shared memory up to that width
+    // batches above 128 rows run as launches of <= 128 rows: the two accumulators of a launch
+    // share TMEM with the rebuilt weight slots
     constexpr int64_t kMxMaxBatchPerLaunch = 128;
     for (int64_t r0 = 0; r0 < B; r0 += kMxMaxBatchPerLaunch) {
         const int64_t nb = (B - r0 < kMxMaxBatchPerLaunch) ? B - r0 : kMxMaxBatchPerLaunch;
