@@ -200,8 +200,11 @@ lms_status lms_lmhead_sample_fp8(const void* H, int64_t ldh, const void* W8, int
  * lms_mxfp4_pack rewrites a matrix once into the library's tiled device format (Wt,
  * lms_mxfp4_tiled_bytes(V, D) bytes): one contiguous 4352-byte block per 128-row vocabulary tile
  * and 64-element K chunk (4 KB of codes, row r at byte 32 r; then the two blocks' 128 scale codes
- * each), so that each block streams with a single contiguous copy.  Rows past V and elements past
- * D are zero.  lms_lmhead_sample_mxfp4 then computes logits y[b][v] = sum_d H[b][d] W[v][d] with
+ * each), so that each block streams with a single contiguous copy.  A row's 32 code bytes are
+ * eight little-endian 32-bit words of eight consecutive elements e0..e7: the magnitude bits
+ * (bits 2..0 of the code) of e_k at bits 4k..4k+2, the sign of e_k at bit 8k+7 for k < 4 and at
+ * bit 8(k-4)+3 for k >= 4, which lets the sign join its bf16 high byte with one logic operation.
+ * Rows past V and elements past D are zero.  lms_lmhead_sample_mxfp4 then computes logits y[b][v] = sum_d H[b][d] W[v][d] with
  * fp32 accumulation; everything after that is lms_lmhead_sample's (same noise, transform, race,
  * statuses and workspace: lms_workspace_bytes(LMS_OP_LMHEAD, ...)).  The weights stream at 0.53
  * bytes each and are rebuilt on chip as exact bf16 values; that is exact for scale codes 3..252

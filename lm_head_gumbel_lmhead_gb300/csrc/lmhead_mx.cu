@@ -10,27 +10,40 @@
 // two bf16 of K per 32-bit column), so the tensor cores run the same bf16 x bf16 -> fp32
 // contraction and the rebuilt weights never pass through shared memory.
 //
+// The tensor cores take about as long for one M = 128, K = 16 instruction at N = 16 as at
+// N = 128 (measured: ~105 cycles), so at decode batch sizes the weight stream is bounded by the
+// instruction rate, and any gap between a chunk's MMAs and the next (barrier wait, fence, commit)
+// leaves the tensor cores idle.  The CTA therefore runs two independent streams: stream s takes
+// the CTA's vocabulary tiles of parity s, with its own MMA warp, converter group, ring-A stages,
+// TMEM slots and accumulator, so one stream's handshakes overlap the other's MMAs.  Each tile is
+// still accumulated in a fixed order by one warp.
+//
 // Warp roles (one persistent CTA per SM):
-//   warp 0           bulk-copy producer of the packed weights: the library's tiled MXFP4 format
-//                    (lms_mxfp4_pack) stores each (128-row vocabulary tile, 64-element K chunk)
-//                    as one contiguous 4352-byte block, 4 KB of codes then 256 bytes of scales, so
-//                    one cp.async.bulk of contiguous bytes fills a ring-A stage.
-//   warp 1           allocates TMEM; one lane issues tcgen05.mma (M = 128, N = n_pad batch rows,
-//                    K = 16 per instruction, A from TMEM, B = H from shared memory) into two TMEM
-//                    accumulators.
-//   warp 2           TMA producer of H [n_pad x 64] bf16 chunks into ring H.
-//   warps 3..10      converters, in two groups of four: group g takes the chunks j = g, g + 2, ...
-//                    of the CTA's sequence; within a group, warp w (w % 4 = q, the TMEM lane
-//                    quarter a warp may access) rebuilds rows 32 q .. 32 q + 31 of the chunk, one
-//                    row of 64 weights per lane (byte permutes and one bf16x2 multiply per pair),
-//                    and stores them with tcgen05.st into the chunk's TMEM slot.
-//   warps 11..18     epilogue: as in the bf16 kernel (transform, noise, argmax per tile).
-// Ring A (packed codes and scales, 4.25 KB a stage) is deep so that enough weight bytes are in
-// flight to keep HBM busy.  TMEM holds eight rebuilt-weight slots of 32 columns (four per group)
-// in columns 0..255 and the two accumulators from column 256; ring H has one activation stage per
-// slot, and one tcgen05.commit per chunk frees both.  Every wait is bounded in time; a CTA whose
-// wait runs out flags the error, drains its copies and MMAs, poisons its remaining candidates
-// (row status 3), frees TMEM and exits.
+//   warp 0           bulk-copy producer of the packed weights for both streams: the library's
+//                    tiled MXFP4 format (lms_mxfp4_pack) stores each (128-row vocabulary tile,
+//                    64-element K chunk) as one contiguous 4352-byte block, 4 KB of codes then 256
+//                    bytes of scales, so one cp.async.bulk fills a ring-A stage.
+//   warps 1, 2       MMA warps of streams 0 and 1 (warp 1 also allocates TMEM); an elected lane
+//                    issues tcgen05.mma (M = 128, N = n_pad batch rows, K = 16 per instruction,
+//                    A from TMEM, B = H from shared memory) into the stream's accumulator.
+//   warps 3..18      converters, in four groups of four; groups 2s and 2s + 1 serve stream s,
+//                    taking its even and odd chunks.  Within a group, warp w (w % 4 = q, the TMEM
+//                    lane quarter a warp may access) rebuilds rows 32 q .. 32 q + 31 of each
+//                    chunk, one row of 64 weights per lane (byte permutes and one bf16x2 multiply
+//                    per pair), and stores them with tcgen05.st into the chunk's TMEM slot.  The
+//                    group's first warp also issues the TMA load of the chunk's activations
+//                    [n_pad x 64] bf16 into the slot's ring-H stage.  Rebuilding a chunk takes the
+//                    SM about 300 cycles of issue once eight or more warps share it, against ~420
+//                    cycles of tensor time for its four MMAs; sixteen warps leave room for each
+//                    group's barrier waits and loads to overlap the others' rebuilding.
+//   warps 19..22     epilogue: as in the bf16 kernel (transform, noise, argmax per tile), over the
+//                    tiles in order, each from its stream's accumulator.
+// Ring A (packed codes and scales, 4.25 KB a stage, half the stages per stream) is deep so that
+// enough weight bytes are in flight to keep HBM busy.  TMEM holds eight rebuilt-weight slots of 32
+// columns (four per stream) in columns 0..255 and the two accumulators from column 256; ring H has
+// one activation stage per slot, and one tcgen05.commit per chunk frees both.  Every wait is
+// bounded in time; a CTA whose wait runs out flags the error, drains its copies and MMAs, poisons
+// its remaining candidates (row status 3), frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -44,22 +57,26 @@ namespace {
 
 using namespace tc;
 
-constexpr int kMxConvWarps = 8;
-constexpr int kMxGroups = 2;                           // converter groups of four warps
-constexpr int kMxEpiWarps = 8;
+constexpr int kMxStreams = 2;
+constexpr int kMxGroups = 4;                           // converter groups of four warps, two per stream
+constexpr int kMxConvWarps = 4 * kMxGroups;
+constexpr int kMxEpiWarps = 4;
 constexpr int kMxFirstConv = 3;
 constexpr int kMxFirstEpi = kMxFirstConv + kMxConvWarps;
 constexpr int kMxThreads = 32 * (kMxFirstEpi + kMxEpiWarps);
-// Ring A has an even number of stages: then stage k is only ever read by group k % 2, so no
-// warp can wait on a stage's next phase while its current one is incomplete.
+// Ring A: stages s * SA/2 .. s * SA/2 + SA/2 - 1 belong to stream s; SA/2 is even, so stage k
+// of a stream is only ever read by one of its two groups (the one taking chunks of parity k % 2).
 constexpr int kMaxStagesA = 32;
-// TMEM: slot t (group t / 4, the group's slot t % 4) holds one rebuilt 128 x 64 bf16 chunk in
-// columns 32 t .. 32 t + 31; the accumulators start at column 256 (n_pad <= 128 each).
-constexpr int kSlotsPerGroup = 4;
-constexpr int kSlots = kMxGroups * kSlotsPerGroup;
+// TMEM: slot t (stream t / 4, the stream's slot t % 4) holds one rebuilt 128 x 64 bf16 chunk in
+// columns 32 t .. 32 t + 31; the accumulator of stream s starts at column 256 + s * n_pad
+// (n_pad <= 128).
+constexpr int kSlotsPerStream = 4;
+constexpr int kSlots = kMxStreams * kSlotsPerStream;
 constexpr uint32_t kSlotCols = kBK / 2;
 constexpr uint32_t kAccCol0 = kSlots * kSlotCols;
 constexpr uint32_t kMxTmemCols = 512;
+// Longest suspension of a waiting thread per try (it resumes as soon as the phase completes).
+constexpr uint32_t kSuspendNs = 100000;
 constexpr uint32_t kW4StageBytes = kTileV * kBK / 2;   // 128 rows x 64 codes = 4 KB
 constexpr uint32_t kS4StageBytes = 2 * kTileV;         // 2 scale blocks x 128 rows
 constexpr uint32_t kAStageBytes = kW4StageBytes + kS4StageBytes;   // one tiled block
@@ -84,8 +101,8 @@ struct MxLayout {
         a_off = h_off + kSlots * h_stage_bytes;
         bars_off = a_off + sa * kAStageBytes;
         // fullA, emptyA [SA]; fullC (slot written, count 4), emptyC (slot and its H stage free,
-        // one commit), fullH [kSlots]; acc_full[2], acc_empty[2], drain
-        misc_off = bars_off + (2 * sa + 3 * kSlots + 5) * 8;
+        // one commit), fullH [kSlots]; acc_full[2], acc_empty[2], drain[2]
+        misc_off = bars_off + (2 * sa + 3 * kSlots + 6) * 8;
         rows_off = (misc_off + 16 + 15) & ~15u;   // misc: tmem slot, error flag
         red_off = rows_off + n_pad * static_cast<uint32_t>(sizeof(RowParams));
         tr_off = red_off + n_pad * 8;
@@ -98,8 +115,12 @@ struct MxLayout {
 constexpr uint32_t kHiA = 0x3F3F3F00u, kHiB = 0x40404040u;
 constexpr uint32_t kLoA = 0xC0800000u, kLoB = 0xC0804000u;
 
-// Eight E2M1 codes (code j in bits 4j..4j+3) -> eight bf16 values (pairs in out[0..3], code 2i in
-// the low half of out[i]), times the block scale sc2 (2^(s - 127) in both halves).
+// One 32-bit word of the tiled format (eight elements e0..e7: the magnitude bits of e_k at bits
+// 4k..4k+2, the sign of e_k at bit 8k+7 for k < 4 and at bit 8(k-4)+3 for k >= 4) -> eight bf16
+// values (pairs in out[0..3], e_2i in the low half of out[i]), times the block scale sc2
+// (2^(s - 127) in both halves).  The magnitudes index two 8-entry byte tables (high and low
+// bytes of the bf16 value); the sign bits already sit at the top bit of the high byte of their
+// element, or four bits below it.
 __device__ __forceinline__ void e2m1x8_to_bf16(uint32_t x, __nv_bfloat162 sc2, uint32_t (&out)[4]) {
     const uint32_t mag = x & 0x77777777u;
     uint32_t hb0 = __byte_perm(kHiA, kHiB, mag);
@@ -107,10 +128,8 @@ __device__ __forceinline__ void e2m1x8_to_bf16(uint32_t x, __nv_bfloat162 sc2, u
     const uint32_t m1 = mag >> 16;
     uint32_t hb1 = __byte_perm(kHiA, kHiB, m1);
     const uint32_t lb1 = __byte_perm(kLoA, kLoB, m1);
-    // sign of code 2k at bit 7 of byte k of se, of code 2k + 1 at bit 7 of byte k of so
-    const uint32_t se = (x << 4) & 0x80808080u, so = x & 0x80808080u;
-    hb0 |= __byte_perm(se, so, 0x5140);
-    hb1 |= __byte_perm(se, so, 0x7362);
+    hb0 |= x & 0x80808080u;                    // signs of e0..e3
+    hb1 |= (x << 4) & 0x80808080u;             // signs of e4..e7
     const uint32_t p[4] = {__byte_perm(lb0, hb0, 0x5140), __byte_perm(lb0, hb0, 0x7362),
                            __byte_perm(lb1, hb1, 0x5140), __byte_perm(lb1, hb1, 0x7362)};
 #pragma unroll
@@ -140,11 +159,24 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
+// A word of eight E2M1 codes in the logical order (element k in bits 4k..4k+3, sign at bit
+// 4k+3) -> the tiled format's word: magnitudes in place, the sign of element k moved to bit
+// 8k+7 (k < 4) or 8(k-4)+3 (k >= 4).
+__device__ __forceinline__ uint32_t mx_tile_word(uint32_t y) {
+    uint32_t out = y & 0x77777777u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t sign = (y >> (4 * k + 3)) & 1u;
+        out |= sign << (k < 4 ? 8 * k + 7 : 8 * (k - 4) + 3);
+    }
+    return out;
+}
+
 // The tiled MXFP4 format: block (t, c) at byte (t * nk + c) * kAStageBytes holds the codes of
-// rows 128 t .. 128 t + 127 and elements 64 c .. 64 c + 63 (row r at r * 32, element 64 c + 2 i
-// in the low nibble of byte i, 64 c + 2 i + 1 in the high nibble), then the scale codes of their
-// two blocks of 32 (block k of row r at 4096 + 128 k + r); rows past V and elements past D are
-// zero.  One CTA of 256 threads writes one block.
+// rows 128 t .. 128 t + 127 and elements 64 c .. 64 c + 63 (row r at r * 32 as eight
+// little-endian words of eight elements each, in mx_tile_word's layout), then the scale codes of
+// their two blocks of 32 (block k of row r at 4096 + 128 k + r); rows past V and elements past D
+// are zero.  One CTA of 256 threads writes one block.
 __global__ void __launch_bounds__(256) mxfp4_pack_kernel(const uint8_t* __restrict__ W4, int64_t ldw4,
                                                           const uint8_t* __restrict__ S, int64_t lds,
                                                           int64_t V, int64_t D, int nk,
@@ -161,11 +193,12 @@ __global__ void __launch_bounds__(256) mxfp4_pack_kernel(const uint8_t* __restri
 #pragma unroll
         for (int e = 0; e < 16; ++e)
             piece[e] = (v < V && byte0 + e < D / 2) ? W4[v * ldw4 + byte0 + e] : 0;
-        uint4 w;
-        w.x = piece[0] | (piece[1] << 8) | (piece[2] << 16) | (static_cast<uint32_t>(piece[3]) << 24);
-        w.y = piece[4] | (piece[5] << 8) | (piece[6] << 16) | (static_cast<uint32_t>(piece[7]) << 24);
-        w.z = piece[8] | (piece[9] << 8) | (piece[10] << 16) | (static_cast<uint32_t>(piece[11]) << 24);
-        w.w = piece[12] | (piece[13] << 8) | (piece[14] << 16) | (static_cast<uint32_t>(piece[15]) << 24);
+        uint32_t word[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            word[q] = mx_tile_word(piece[4 * q] | (piece[4 * q + 1] << 8) | (piece[4 * q + 2] << 16) |
+                                   (static_cast<uint32_t>(piece[4 * q + 3]) << 24));
+        const uint4 w = make_uint4(word[0], word[1], word[2], word[3]);
         *reinterpret_cast<uint4*>(blk + i * 16) = w;
     }
     {
@@ -238,35 +271,35 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     auto emptyC = [&](int t) { return bar0 + 8u * (2 * SA + kSlots + t); };
     auto fullH = [&](int t) { return bar0 + 8u * (2 * SA + 2 * kSlots + t); };
     const uint32_t acc0 = bar0 + 8u * (2 * SA + 3 * kSlots);
-    auto accf_bar = [&](int ab) { return acc0 + 8u * ab; };
-    auto acce_bar = [&](int ab) { return acc0 + 8u * (2 + ab); };
-    const uint32_t drain_bar = acc0 + 32u;
+    auto accf_bar = [&](int st) { return acc0 + 8u * st; };
+    auto acce_bar = [&](int st) { return acc0 + 8u * (2 + st); };
+    auto drain_bar = [&](int st) { return acc0 + 8u * (4 + st); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.misc_off);
     volatile int* err = reinterpret_cast<volatile int*>(base + L.misc_off + 4);
     RowParams* rows = reinterpret_cast<RowParams*>(base + L.rows_off);
     unsigned long long* red = reinterpret_cast<unsigned long long*>(base + L.red_off);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < SA; ++s) {
-            mbar_init(fullA(s), 1);
-            mbar_init(emptyA(s), 4);             // the four warps of the stage's group
+        for (int k = 0; k < SA; ++k) {
+            mbar_init(fullA(k), 1);
+            mbar_init(emptyA(k), 4);             // the four warps of the stage's group
         }
         for (int t = 0; t < kSlots; ++t) {
             mbar_init(fullC(t), 4);
             mbar_init(emptyC(t), 1);
             mbar_init(fullH(t), 1);
         }
-        for (int ab = 0; ab < 2; ++ab) {
-            mbar_init(accf_bar(ab), 1);
-            mbar_init(acce_bar(ab), kMxEpiWarps);
+        for (int st = 0; st < kMxStreams; ++st) {
+            mbar_init(accf_bar(st), 1);
+            mbar_init(acce_bar(st), kMxEpiWarps);
+            mbar_init(drain_bar(st), 1);
         }
-        mbar_init(drain_bar, 1);
         *err = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     clear_status_bits(a.status_bits, a.row0);
-    if (warp == 0 && lane == 0) {
+    if (warp == kMxFirstConv && lane == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmH)) : "memory");
     }
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
@@ -279,101 +312,74 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
-    // this CTA's K chunks, in order: chunk j is K chunk j % nk of its (j / nk)-th tile, converted
-    // by group j % 2 into that group's slots in turn.  Every role walks them with incremental
-    // counters (no division in the loops).
+    // This CTA's tiles are blockIdx.x + i * gridDim.x, i < my_tiles; stream s takes i = s, s + 2,
+    // ...  Chunk u of a stream is K chunk u % nk of its (u / nk)-th tile.  Every role walks its
+    // chunks with incremental counters (no division in the loops).
     const int64_t my_tiles = nt > blockIdx.x ? (nt - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-    const int64_t n_chunks = my_tiles * prm.nk;
+    auto tiles_of = [&](int st) { return (my_tiles + 1 - st) / 2; };   // tiles of stream st
+    const int half = SA / 2;
 
     if (warp == 0) {
         // ---------------- bulk-copy producer: packed weights and scales (ring A) ----------------
+        // Both streams in lockstep: chunk u of stream 0, then chunk u of stream 1.
         if (lane == 0) {
             const uint64_t pol_w = l2_policy_evict_first();
+            const int64_t n0 = tiles_of(0) * prm.nk, n1 = tiles_of(1) * prm.nk;
             uint32_t issued = 0, issued_parity = 0;
-            int stage = 0;
+            int stage = 0;                       // stage within each stream's half of ring A
             uint32_t phase = 0;
             int kc = 0;
-            int64_t tile = blockIdx.x;
-            for (int64_t j = 0; j < n_chunks && *err == 0; ++j) {
-                if (!mbar_wait(emptyA(stage), phase ^ 1u, prm.timeout_ns, err)) {
-                    *err = 1;
-                    break;
+            int64_t tile0 = blockIdx.x;          // the current tile of stream 0; stream 1's is next
+            for (int64_t u = 0; u < n0 && *err == 0; ++u) {
+                for (int st = 0; st < kMxStreams; ++st) {
+                    if (st == 1 && u >= n1) break;
+                    const int k = st * half + stage;
+                    if (!mbar_wait_suspend(emptyA(k), phase ^ 1u, prm.timeout_ns, err, kSuspendNs)) {
+                        *err = 1;
+                        break;
+                    }
+                    const bool withhold = u == 0 && st == 0 && blockIdx.x == 0 &&
+                                          (prm.debug_flags & LMS_DEBUG_WITHHOLD_FIRST_LOAD);
+                    if (!withhold) {
+                        const int64_t block = (tile0 + st * gridDim.x) * prm.nk + kc;
+                        mbar_arrive_expect_tx(fullA(k), kAStageBytes);
+                        bulk_load(base_addr + L.a_off + k * kAStageBytes, Wt + block * kAStageBytes,
+                                  kAStageBytes, fullA(k), pol_w);
+                        issued |= 1u << k;
+                        issued_parity = (issued_parity & ~(1u << k)) | (phase << k);
+                    }
                 }
-                const bool withhold = j == 0 && blockIdx.x == 0 &&
-                                      (prm.debug_flags & LMS_DEBUG_WITHHOLD_FIRST_LOAD);
-                if (!withhold) {
-                    const int64_t block = tile * prm.nk + kc;
-                    mbar_arrive_expect_tx(fullA(stage), kAStageBytes);
-                    bulk_load(base_addr + L.a_off + stage * kAStageBytes, Wt + block * kAStageBytes,
-                              kAStageBytes, fullA(stage), pol_w);
-                    issued |= 1u << stage;
-                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                }
-                if (++stage == SA) { stage = 0; phase ^= 1u; }
-                if (++kc == prm.nk) { kc = 0; tile += gridDim.x; }
+                if (++stage == half) { stage = 0; phase ^= 1u; }
+                if (++kc == prm.nk) { kc = 0; tile0 += 2 * static_cast<int64_t>(gridDim.x); }
             }
-            for (int s = 0; s < SA; ++s)
-                if (issued & (1u << s))
-                    mbar_wait(fullA(s), (issued_parity >> s) & 1u, prm.timeout_ns, nullptr);
+            for (int k = 0; k < SA; ++k)
+                if (issued & (1u << k))
+                    mbar_wait_suspend(fullA(k), (issued_parity >> k) & 1u, prm.timeout_ns, nullptr, kSuspendNs);
         }
-    } else if (warp == 2) {
-        // ---------------- TMA producer: activations (ring H, one stage per TMEM slot) ----------------
-        if (lane == 0) {
-            const uint64_t pol_h = l2_policy_evict_last();
-            uint32_t issued = 0, issued_parity = 0;
-            // slot and phase of each group's next chunk (group 0's in t0/p0, group 1's in t1/p1)
-            int t0 = 0, t1 = kSlotsPerGroup;
-            uint32_t p0 = 0, p1 = 0;
-            int kc = 0;
-            for (int64_t j = 0; j < n_chunks && *err == 0; ++j) {
-                const bool g1 = (j & 1) != 0;
-                const int t = g1 ? t1 : t0;
-                const uint32_t pt = g1 ? p1 : p0;
-                // the slot's previous chunk has been consumed by the tensor cores
-                if (!mbar_wait(emptyC(t), pt ^ 1u, prm.timeout_ns, err)) {
-                    *err = 1;
-                    break;
-                }
-                mbar_arrive_expect_tx(fullH(t), prm.h_stage_bytes);
-                tma_load_2d(base_addr + L.h_off + t * prm.h_stage_bytes, &tmH, kc * kBK,
-                            static_cast<int>(a.row0), fullH(t), pol_h);
-                issued |= 1u << t;
-                issued_parity = (issued_parity & ~(1u << t)) | (pt << t);
-                if (g1) {
-                    if (++t1 == kSlots) { t1 = kSlotsPerGroup; p1 ^= 1u; }
-                } else {
-                    if (++t0 == kSlotsPerGroup) { t0 = 0; p0 ^= 1u; }
-                }
-                if (++kc == prm.nk) kc = 0;
-            }
-            for (int t = 0; t < kSlots; ++t)
-                if (issued & (1u << t))
-                    mbar_wait(fullH(t), (issued_parity >> t) & 1u, prm.timeout_ns, nullptr);
-        }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
+    } else if (warp <= kMxStreams) {
+        // ---------------- MMA warps: warp 1 + s issues stream s ----------------
         // The whole warp walks the loop, converged, so that the slot counters, TMEM addresses and
         // descriptors stay warp-uniform; one elected lane issues the tcgen05 instructions.
+        const int st = warp - 1;
         const bool leader = elect_one();
         const uint32_t idesc = mma_idesc_bf16(n_pad, kTileV);
+        const uint32_t d_tmem = tmem_base + kAccCol0 + static_cast<uint32_t>(st * n_pad);
         bool ok = true;
-        int t0 = 0, t1 = kSlotsPerGroup;       // as in the activation producer
-        uint32_t p0 = 0, p1 = 0;
-        bool g1 = false;
-        for (int64_t i = 0; i < my_tiles && ok; ++i) {
-            const int ab = static_cast<int>(i & 1);
-            const uint32_t use_parity = static_cast<uint32_t>((i >> 1) & 1);
-            if (!__all_sync(0xffffffffu, mbar_wait(acce_bar(ab), use_parity ^ 1u, prm.timeout_ns, err))) {
+        int idx = 0;
+        uint32_t pt = 0;
+        for (int64_t k = 0; k < tiles_of(st) && ok; ++k) {
+            // the epilogue is done with this stream's previous tile
+            if (!__all_sync(0xffffffffu, mbar_wait_suspend(acce_bar(st), static_cast<uint32_t>(k & 1) ^ 1u,
+                                                   prm.timeout_ns, err, kSuspendNs))) {
                 ok = false;
                 break;
             }
             tc_fence_after_sync();
-            const uint32_t d_tmem = tmem_base + kAccCol0 + static_cast<uint32_t>(ab * n_pad);
             for (int kc = 0; kc < prm.nk; ++kc) {
-                const int t = g1 ? t1 : t0;
+                const int t = st * kSlotsPerStream + idx;
                 // the group announces the slot once its rebuilt weights are stored and the
                 // chunk's activations have landed
-                if (!__all_sync(0xffffffffu, mbar_wait(fullC(t), g1 ? p1 : p0, prm.timeout_ns, err))) {
+                if (!__all_sync(0xffffffffu, mbar_wait_suspend(fullC(t), pt, prm.timeout_ns, err, kSuspendNs))) {
                     ok = false;
                     break;
                 }
@@ -382,59 +388,85 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                 const uint64_t bdesc = kmajor_sw128_desc(base_addr + L.h_off + t * prm.h_stage_bytes);
                 if (leader) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_bf16_tmem_a(d_tmem, a_tmem + 8u * k, bdesc + 2u * k, idesc,
-                                        (kc | k) != 0 ? 1u : 0u);
+                    for (int k4 = 0; k4 < 4; ++k4)
+                        mma_bf16_tmem_a(d_tmem, a_tmem + 8u * k4, bdesc + 2u * k4, idesc,
+                                        (kc | k4) != 0 ? 1u : 0u);
                     mma_commit(emptyC(t));
                 }
                 __syncwarp();
-                if (g1) {
-                    if (++t1 == kSlots) { t1 = kSlotsPerGroup; p1 ^= 1u; }
-                } else {
-                    if (++t0 == kSlotsPerGroup) { t0 = 0; p0 ^= 1u; }
-                }
-                g1 = !g1;
+                if (++idx == kSlotsPerStream) { idx = 0; pt ^= 1u; }
             }
             if (!ok) break;
-            if (leader) mma_commit(accf_bar(ab));
+            if (leader) mma_commit(accf_bar(st));
             __syncwarp();
         }
         if (!ok && lane == 0) *err = 1;
         if (leader) {
-            mma_commit(drain_bar);
-            mbar_wait(drain_bar, 0, prm.timeout_ns, nullptr);
+            mma_commit(drain_bar(st));
+            mbar_wait_suspend(drain_bar(st), 0, prm.timeout_ns, nullptr, kSuspendNs);
         }
         __syncwarp();
     } else if (warp < kMxFirstEpi) {
         // ---------------- converters ----------------
-        // Group g = (warp - 3) / 4 takes the chunks j = g, g + 2, ...; the warp's TMEM lane quarter
-        // q = warp % 4 gives its rows r = 32 q + lane.  Lane r reads its row's 32 code bytes (64
-        // weights) and two scale codes from the ring-A stage, rebuilds the 64 bf16 weights as 32
+        // Group G = (warp - 3) / 4 serves stream g = G / 2 and takes its chunks u of parity
+        // h = G % 2; the warp's TMEM lane quarter q = warp % 4 gives its rows r = 32 q + lane.  For
+        // chunk u (ring-A stage g * SA/2 + u % (SA/2), TMEM slot t = 4 g + u % 4), lane r reads its
+        // row's 32 code bytes (64 weights) and two scale codes, rebuilds the 64 bf16 weights as 32
         // bf16x2 words (word c = K elements 2c, 2c + 1) and stores them into TMEM lane r, columns
-        // 32 t .. 32 t + 31 of the group's current slot t.  Ring-A stage of the group's u-th
-        // chunk: g + 2 (u % (SA / 2)), phase (u / (SA / 2)) & 1.
-        const int g = (warp - kMxFirstConv) >> 2;
+        // 32 t .. 32 t + 31.
+        const int G = (warp - kMxFirstConv) >> 2;
+        const int g = G >> 1, h = G & 1;
+        const bool h_loader = ((warp - kMxFirstConv) & 3) == 0 && lane == 0;
+        const uint64_t pol_h = l2_policy_evict_last();
         const int q = warp & 3;
         const int r = 32 * q + lane;
         const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
-        bool ok = true;
-        int sa = g, idx = 0;
-        uint32_t pa = 0, pt = 0;
-        for (int64_t j = g; j < n_chunks && ok; j += kMxGroups) {
-            // every wait's outcome is made warp-uniform: tcgen05.st needs the whole warp
-            if (!__all_sync(0xffffffffu, mbar_wait(fullA(sa), pa, prm.timeout_ns, err))) {
-                ok = false;
-                break;
+        const int64_t n_mine = (tiles_of(g) * prm.nk + 1 - h) / 2;
+        uint32_t h_issued = 0, h_parity = 0;     // the loader's activation loads, by slot
+        // Software pipeline: while chunk u is rebuilt and stored, chunk u + 1's codes are already
+        // in registers and its activations on their way.  fetch() takes the next chunk: it waits
+        // until that chunk's slot is free, issues its activation load, waits for its ring-A stage
+        // and reads the lane's codes and scales.
+        // counters of the group's chunks u = h, h + 2, ...: ring-A stage u % (SA/2), slot u % 4 and
+        // K chunk u % nk (for the next chunk to fetch and the chunk being stored)
+        int stage = h, idx_f = h, idx = h;
+        int kc = h < prm.nk ? h : 0;
+        uint32_t pa = 0, pt_f = 0, pt = 0;
+        uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
+        uint32_t s0 = 0, s1 = 0;
+        // every wait's outcome is made warp-uniform: tcgen05.st needs the whole warp
+        auto fetch = [&]() -> bool {
+            const int t = g * kSlotsPerStream + idx_f;
+            if (!__all_sync(0xffffffffu, mbar_wait_suspend(emptyC(t), pt_f ^ 1u, prm.timeout_ns, err, kSuspendNs)))
+                return false;
+            if (h_loader) {
+                mbar_arrive_expect_tx(fullH(t), prm.h_stage_bytes);
+                tma_load_2d(base_addr + L.h_off + t * prm.h_stage_bytes, &tmH, kc * kBK,
+                            static_cast<int>(a.row0), fullH(t), pol_h);
+                h_issued |= 1u << t;
+                h_parity = (h_parity & ~(1u << t)) | (pt_f << t);
             }
-            const uint8_t* w4 = base + L.a_off + sa * kAStageBytes;
-            const uint4 c0 = *reinterpret_cast<const uint4*>(w4 + r * 32);
-            const uint4 c1 = *reinterpret_cast<const uint4*>(w4 + r * 32 + 16);
-            const uint32_t s0 = w4[kW4StageBytes + r], s1 = w4[kW4StageBytes + kTileV + r];
+            idx_f += 2;
+            if (idx_f >= kSlotsPerStream) { idx_f -= kSlotsPerStream; pt_f ^= 1u; }
+            kc += 2;
+            if (kc >= prm.nk) kc -= prm.nk;
+            if (kc >= prm.nk) kc -= prm.nk;
+            const int k = g * half + stage;
+            if (!__all_sync(0xffffffffu, mbar_wait_suspend(fullA(k), pa, prm.timeout_ns, err, kSuspendNs))) return false;
+            const uint8_t* w4 = base + L.a_off + k * kAStageBytes;
+            c0 = *reinterpret_cast<const uint4*>(w4 + r * 32);
+            c1 = *reinterpret_cast<const uint4*>(w4 + r * 32 + 16);
+            s0 = w4[kW4StageBytes + r];
+            s1 = w4[kW4StageBytes + kTileV + r];
             // the codes and scales are in registers: this warp is done with the ring-A stage
             __syncwarp();
-            if (lane == 0) mbar_arrive(emptyA(sa));
-            sa += kMxGroups;
-            if (sa >= SA) { sa = g; pa ^= 1u; }
+            if (lane == 0) mbar_arrive(emptyA(k));
+            stage += 2;
+            if (stage >= half) { stage -= half; pa ^= 1u; }
+            return true;
+        };
+        bool ok = n_mine == 0 || fetch();
+        for (int64_t u = 0; u < n_mine && ok; ++u) {
             uint32_t v[32];
             {
                 const __nv_bfloat162 sc0 = ue8m0_to_bf16x2(s0), sc1 = ue8m0_to_bf16x2(s1);
@@ -447,25 +479,30 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                     for (int i = 0; i < 4; ++i) v[4 * wd + i] = o[i];
                 }
             }
-            const int t = g * kSlotsPerGroup + idx;
-            // the slot's previous chunk has been consumed by the tensor cores
-            if (!__all_sync(0xffffffffu, mbar_wait(emptyC(t), pt ^ 1u, prm.timeout_ns, err))) {
+            if (u + 1 < n_mine && !fetch()) {
                 ok = false;
                 break;
             }
+            const int t = g * kSlotsPerStream + idx;
             tc_fence_after_sync();
             tmem_store_32(lane_addr + static_cast<uint32_t>(t) * kSlotCols, v);
             // the chunk's activations must have landed too before the slot is announced
-            if (!__all_sync(0xffffffffu, mbar_wait(fullH(t), pt, prm.timeout_ns, err))) {
+            if (!__all_sync(0xffffffffu, mbar_wait_suspend(fullH(t), pt, prm.timeout_ns, err, kSuspendNs))) {
                 ok = false;
                 break;
             }
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(fullC(t));
-            if (++idx == kSlotsPerGroup) { idx = 0; pt ^= 1u; }
+            idx += 2;
+            if (idx >= kSlotsPerStream) { idx -= kSlotsPerStream; pt ^= 1u; }
         }
-        if (!ok) *err = 1;
+        if (!ok && lane == 0) *err = 1;
+        // the loader waits (bounded) for its own activation loads still in flight
+        if (h_loader)
+            for (int t = 0; t < kSlots; ++t)
+                if (h_issued & (1u << t))
+                    mbar_wait_suspend(fullH(t), (h_parity >> t) & 1u, prm.timeout_ns, nullptr, kSuspendNs);
     } else {
         // ---------------- epilogue ----------------
         const int epi_tid = threadIdx.x - 32 * kMxFirstEpi;
@@ -476,9 +513,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         int i = 0;
         bool ok = true;
         for (int64_t tile = blockIdx.x; tile < nt; tile += gridDim.x, ++i) {
-            const int ab = i & 1;
+            const int st = i & 1;
             const uint32_t use_parity = (i >> 1) & 1;
-            if (ok) ok = mbar_wait(accf_bar(ab), use_parity, prm.timeout_ns, err);
+            if (ok) ok = mbar_wait_suspend(accf_bar(st), use_parity, prm.timeout_ns, err, kSuspendNs);
             ok = epi_barrier_and(epi_threads, ok);
             if (!ok) {
                 if (epi_tid == 0) *err = 1;
@@ -490,19 +527,19 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             }
             tc_fence_after_sync();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + kAccCol0 +
-                                   static_cast<uint32_t>(ab * n_pad);
+                                   static_cast<uint32_t>(st * n_pad);
             epilogue_tile_columns<kMxEpiWarps, kWide, kPlain>(a, rows, red, tr, t_row, tile, quad,
                                                               col_group, lane, B);
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acce_bar(ab));
+            if (lane == 0) mbar_arrive(acce_bar(st));
             epi_barrier(epi_threads);
             for (int b = epi_tid; b < B; b += epi_threads) {
                 const unsigned long long key = red[b];
                 red[b] = 0ull;
-                const float s = unpack_score(key);
-                a.cand_score[b * nt + tile] = s;
-                a.cand_index[b * nt + tile] = candidate_index(s, unpack_index(key));
+                const float sc = unpack_score(key);
+                a.cand_score[b * nt + tile] = sc;
+                a.cand_index[b * nt + tile] = candidate_index(sc, unpack_index(key));
             }
             epi_barrier(epi_threads);
         }
@@ -555,9 +592,9 @@ cudaError_t launch_lmhead_mx(const uint8_t* Wt, const CUtensorMap& tmH, int64_t 
     if (n_pad > 128) return cudaErrorInvalidValue;       // two accumulators in TMEM columns 256..511
     const uint32_t budget = 227u * 1024u - 1024u;        // opt-in maximum minus alignment slack
     const uint32_t fixed = MxLayout(0, prm.h_stage_bytes, n_pad).total + 2u * kMaxStagesA * 8u;
-    // ring A as deep as fits, an even number of stages from 32 down to 8
+    // ring A as deep as fits, a multiple of 4 stages from 32 down to 8
     int sa = kMaxStagesA;
-    while (fixed + sa * kAStageBytes > budget && sa > 8) sa -= 2;
+    while (fixed + sa * kAStageBytes > budget && sa > 8) sa -= 4;
     if (fixed + sa * kAStageBytes > budget) return cudaErrorInvalidValue;
     prm.stages_a = sa;
     prm.timeout_ns = static_cast<uint64_t>(timeout_ms) * 1000000ull;

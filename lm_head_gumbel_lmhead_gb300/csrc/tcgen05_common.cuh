@@ -65,6 +65,29 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
+// As mbar_wait, but each try suspends the thread for up to `suspend_ns` while the phase is
+// incomplete (the thread resumes when the phase completes), so a long wait issues almost no
+// instructions and leaves the issue slots to the warps doing work.  The error flag and the
+// deadline are checked after every try.
+__device__ __forceinline__ bool mbar_wait_suspend(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                                  const volatile int* err, uint32_t suspend_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t deadline = global_timer_ns() + timeout_ns;
+    for (;;) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity), "r"(suspend_ns)
+            : "memory");
+        if (done) return true;
+        if (err != nullptr && *err != 0) return false;
+        if (global_timer_ns() > deadline) return false;
+    }
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));

@@ -7,8 +7,9 @@
     scales spread over 2^-27 .. 2^27;
   * every row at the Qwen3-8B shape (D = 4096, V = 151936) at B = 64;
   * a device-side wait that runs out of time reports row status 3, and the context survives;
-  * the packer (lms_mxfp4_pack) writes exactly the tiled layout the header states, checked against
-    this file's own re-tiling on the host, with ragged V and D and scale rows with a stride.
+  * the packer (lms_mxfp4_pack) writes exactly the tiled layout the header states (including the
+    word layout that moves each sign next to its bf16 high byte), checked against this file's own
+    re-tiling on the host, with ragged V and D and scale rows with a stride.
 The parity rule is tests/parity.py's: the oracle decodes the same codes and scales exactly in
 fp64, the kernel rebuilds them as exact bf16 values and accumulates in fp32.
 """
@@ -114,22 +115,38 @@ def test_mxfp4_timeout_reports_status_and_context_survives():
     mx_parity(w, W4, S)
 
 
+def tiled_words(codes):
+    """The header's word layout for elements e0..e7 of each group of eight (codes [..., 8], values
+    0..15): magnitude bits of e_k at bits 4k..4k+2, sign of e_k at bit 8k+7 (k < 4) or 8(k-4)+3
+    (k >= 4); returned as little-endian bytes [..., 4]."""
+    codes = codes.astype(np.uint64)
+    word = np.zeros(codes.shape[:-1], np.uint64)
+    for k in range(8):
+        word |= (codes[..., k] & 7) << np.uint64(4 * k)
+        word |= (codes[..., k] >> np.uint64(3)) << np.uint64(8 * k + 7 if k < 4 else 8 * (k - 4) + 3)
+    return np.stack([(word >> np.uint64(8 * i)) & np.uint64(0xFF) for i in range(4)], -1).astype(np.uint8)
+
+
 def retile_on_host(W4, S, V, D):
     """This file's own writing of the tiled format, from the header's statement: block (t, c) of
-    4352 bytes at (t * ceil(D/64) + c) * 4352: row r's 32 code bytes at 32 r, then the scale codes
-    of blocks 2c and 2c + 1 (row r at 4096 + r and 4096 + 128 + r); zero past V and D."""
+    4352 bytes at (t * ceil(D/64) + c) * 4352: row r's 32 code bytes at 32 r (elements 64 c ..
+    64 c + 63 as eight words of eight, zero past D), then the scale codes of blocks 2c and 2c + 1
+    (row r at 4096 + r and 4096 + 128 + r); zero past V."""
     W4, S = W4.numpy(), S.numpy()
     nt, nk = -(-V // 128), -(-D // 64)
+    codes = np.zeros((nt * 128, nk * 64), np.uint8)            # logical codes, zero padded
+    codes[:V, 0:D:2] = W4[:, :D // 2] & 0xF
+    codes[:V, 1:D:2] = W4[:, :D // 2] >> 4
+    words = tiled_words(codes.reshape(nt * 128, nk * 8, 8)).reshape(nt * 128, nk, 32)
     out = np.zeros(nt * nk * 4352, np.uint8)
     for t in range(nt):
         for c in range(nk):
             base = (t * nk + c) * 4352
+            out[base: base + 4096] = words[128 * t: 128 * t + 128, c].reshape(-1)
             for r in range(128):
                 v = 128 * t + r
                 if v >= V:
                     continue
-                lo, hi = 32 * c, min(32 * c + 32, D // 2)
-                out[base + 32 * r: base + 32 * r + (hi - lo)] = W4[v, lo:hi]
                 for k in range(2):
                     if 2 * c + k < D // 32:
                         out[base + 4096 + 128 * k + r] = S[2 * c + k, v]
