@@ -228,9 +228,12 @@ lms_status lms_lmhead_sample_mxfp4(const void* H, int64_t ldh, const void* Wt, s
  *   out      int64 [B][k] (device): vocabulary indices; -1 past a row's finite scores
  *   scores   fp32 [B][k] (device) or NULL: the perturbed scores (-inf where out is -1)
  *   workspace  lms_workspace_bytes_topk(B, V, k) bytes: the 256-byte status block; ordered key
- *              lists, one per row, tile and quarter of the tile's 128 rows,
- *              uint64 [B][ceil(V / 128)][4][k]; then, at the next 256-byte boundary, Stage 2's
- *              per-row part lists uint64 [B][32][k]
+ *              lists in a region of uint64 [B][ceil(V / 128)][4][k]: one per row, tile and
+ *              quarter of the tile's 128 rows ([B][ceil(V / 128)][4][k]), or, when
+ *              4 * n_pad * k * 8 <= 32 KB (n_pad: min(B, 256) rounded up to a multiple of 16),
+ *              one per row, Stage-1 CTA and quarter, each the k best keys of those rows over the
+ *              CTA's tiles ([B][4 G][k], G = min(ceil(V / 128), SM count)); then, at the next
+ *              256-byte boundary, Stage 2's per-row part lists uint64 [B][32][k]
  * Row statuses as for lms_lmhead_sample (1: no finite score, 2: invalid T, 3: a bounded wait ran
  * out).  Requirements as for lms_lmhead_sample; path AUTO or TCGEN05 (bf16 H and W). */
 #define LMS_TOPK_MAX 16

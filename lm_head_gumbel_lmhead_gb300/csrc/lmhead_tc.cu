@@ -59,9 +59,10 @@ struct TcParams {
 // ------------------------------------------------------------------------------------------
 struct SmemLayout {
     uint32_t stages_off, bars_off, misc_off, rows_off, red_off, tr_off, run_off, total;
-    // topk > 0: per TMEM quadrant and batch column, the top-k threshold key (Gumbel-top-k only)
+    // Gumbel-top-k only: run_keys 64-bit keys (per TMEM quadrant and batch column, the threshold
+    // key of the per-tile lists, or the whole running list)
     __host__ __device__ SmemLayout(int stages, uint32_t stage_bytes, int n_pad, int epi_warps,
-                                   int topk = 0) {
+                                   uint32_t run_keys = 0) {
         stages_off = 0;
         bars_off = stages * stage_bytes;
         // full[S], empty[S], acc_full[2], acc_empty[2], drain
@@ -70,11 +71,19 @@ struct SmemLayout {
         red_off = rows_off + n_pad * static_cast<uint32_t>(sizeof(RowParams));
         tr_off = red_off + n_pad * 8;
         run_off = tr_off + epi_warps * kTrWarpBytes;
-        total = run_off + (topk > 0 ? static_cast<uint32_t>(4 * n_pad) * 8u : 0u);
+        total = run_off + run_keys * 8u;
     }
 };
 
-template <int kEpiWarps, bool kWide, bool kFp8, bool kTopK, bool kPlain>
+// Gumbel-top-k keys in shared memory: the per-tile lists' thresholds (4 n_pad keys) or the running
+// lists (4 n_pad k keys).
+__host__ __device__ inline uint32_t topk_run_keys(int mode, int n_pad, int k) {
+    return mode == 0 ? 0u : static_cast<uint32_t>(4 * n_pad) * (mode == kTopKRunning ? static_cast<uint32_t>(k) : 1u);
+}
+
+// kTopK: 0 = the race; kTopKTileLists = Gumbel-top-k with per-tile lists; kTopKRunning = with
+// running lists in shared memory.
+template <int kEpiWarps, bool kWide, bool kFp8, int kTopK, bool kPlain>
 __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     lmhead_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
                      const TcParams prm) {
@@ -82,7 +91,8 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
     uint8_t* base = smem_raw + (base_addr - raw_addr);
-    const SmemLayout L(prm.stages, prm.stage_bytes, prm.n_pad, kEpiWarps, kTopK ? prm.a.topk : 0);
+    const SmemLayout L(prm.stages, prm.stage_bytes, prm.n_pad, kEpiWarps,
+                       topk_run_keys(kTopK, prm.n_pad, prm.a.topk));
 
     const SampleArgs& a = prm.a;
     const int S = prm.stages;
@@ -127,9 +137,10 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
                                   a.row0 + b);
         red[b] = 0ull;
     }
-    if constexpr (kTopK) {
+    if constexpr (kTopK != 0) {
         unsigned long long* run = reinterpret_cast<unsigned long long*>(base + L.run_off);
-        for (int i = threadIdx.x; i < 4 * n_pad; i += blockDim.x) run[i] = 0ull;
+        const int run_keys = static_cast<int>(topk_run_keys(kTopK, n_pad, a.topk));
+        for (int i = threadIdx.x; i < run_keys; i += blockDim.x) run[i] = 0ull;
     }
     if (warp == 1) tmem_alloc(base_addr + L.misc_off, prm.tmem_cols);
     tc_fence_before_sync();
@@ -252,10 +263,11 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
             if (ok) ok = mbar_wait(accf_bar(ab), use_parity, prm.timeout_ns, err);
             ok = epi_barrier_and(epi_threads, ok);
             if (!ok) {
-                // Poison this tile's candidates (and, through the loop, every later one).
+                // Poison this tile's candidates (and, through the loop, every later one); running
+                // lists are poisoned by their owners when they publish them after the loop
                 if (epi_tid == 0) *err = 1;
-                for (int b = epi_tid; b < B; b += epi_threads) {
-                    if constexpr (kTopK) {
+                for (int b = epi_tid; b < B && kTopK != kTopKRunning; b += epi_threads) {
+                    if constexpr (kTopK == kTopKTileLists) {
                         for (int r = 0; r < 4 * a.topk; ++r)
                             a.cand_keys[(b * nt + tile) * 4 * a.topk + r] = kPoisonKey;
                     } else {
@@ -268,7 +280,11 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
             tc_fence_after_sync();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) +
                                    static_cast<uint32_t>(ab * n_pad);
-            if constexpr (kTopK) {
+            if constexpr (kTopK == kTopKRunning) {
+                unsigned long long* run = reinterpret_cast<unsigned long long*>(base + L.run_off);
+                epilogue_tile_topk_running<kEpiWarps, kWide, kPlain>(a, rows, tr, run, n_pad, t_row,
+                                                                     tile, quad, col_group, lane, B);
+            } else if constexpr (kTopK == kTopKTileLists) {
                 unsigned long long* thr = reinterpret_cast<unsigned long long*>(base + L.run_off);
                 epilogue_tile_topk<kEpiWarps, kWide, kPlain>(a, rows, tr, thr, n_pad, t_row, tile,
                                                              quad, col_group, lane, B);
@@ -280,7 +296,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(ab));
-            if constexpr (!kTopK) {
+            if constexpr (kTopK == 0) {
                 epi_barrier(epi_threads);
                 for (int b = epi_tid; b < B; b += epi_threads) {
                     const unsigned long long key = red[b];
@@ -291,6 +307,10 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
                 }
                 epi_barrier(epi_threads);
             }
+        }
+        if constexpr (kTopK == kTopKRunning) {
+            const unsigned long long* run = reinterpret_cast<const unsigned long long*>(base + L.run_off);
+            topk_running_lists_publish<kEpiWarps>(a, run, n_pad, quad, col_group, lane, B, ok);
         }
     }
 
@@ -304,7 +324,7 @@ __global__ void __launch_bounds__(32 * (2 + kEpiWarps), 1)
     }
 }
 
-template <int kEpiWarps, bool kWide, bool kFp8, bool kTopK = false, bool kPlain = false>
+template <int kEpiWarps, bool kWide, bool kFp8, int kTopK = 0, bool kPlain = false>
 cudaError_t launch_variant(const CUtensorMap& tmW, const CUtensorMap& tmH, const TcParams& prm,
                            size_t smem, int grid, cudaStream_t stream) {
     auto kern = lmhead_tc_kernel<kEpiWarps, kWide, kFp8, kTopK, kPlain>;
@@ -341,7 +361,9 @@ cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int
     prm.n_pad = n_pad;
     prm.stage_bytes = static_cast<uint32_t>(kWStageBytes + n_pad * kBK * 2);
     const uint32_t budget = 227u * 1024u - 1024u;   // opt-in maximum minus alignment slack
-    const SmemLayout fixed(0, prm.stage_bytes, n_pad, kEpilogueWarps, a.topk);
+    const int topk_mode = a.topk > 0 ? a.topk_mode : 0;
+    const uint32_t run_keys = topk_run_keys(topk_mode, n_pad, a.topk);
+    const SmemLayout fixed(0, prm.stage_bytes, n_pad, kEpilogueWarps, run_keys);
     int stages = static_cast<int>((budget - fixed.total - (2 * kMaxStages + 5) * 8) / prm.stage_bytes);
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return cudaErrorInvalidValue;
@@ -351,7 +373,7 @@ cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int
     prm.tmem_cols = cols;
     prm.timeout_ns = static_cast<uint64_t>(timeout_ms) * 1000000ull;
     prm.debug_flags = debug_flags;
-    const SmemLayout L(stages, prm.stage_bytes, n_pad, kEpilogueWarps, a.topk);
+    const SmemLayout L(stages, prm.stage_bytes, n_pad, kEpilogueWarps, run_keys);
     const size_t smem = L.total + 1024;
     int sms = device_sm_count();
     int grid = static_cast<int>(a.n_tiles < sms ? a.n_tiles : sms);
@@ -359,11 +381,19 @@ cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int
     const bool plain = a.bias == nullptr && a.mask == nullptr;
     if (a.topk > 0) {
         if (fp8 || a.topk > kMaxTopK || a.cand_keys == nullptr) return cudaErrorInvalidValue;
+        if (topk_mode == kTopKRunning) {
+            if (plain)
+                return wide ? launch_variant<kEpilogueWarps, true, false, kTopKRunning, true>(tmW, tmH, prm, smem, grid, stream)
+                            : launch_variant<kEpilogueWarps, false, false, kTopKRunning, true>(tmW, tmH, prm, smem, grid, stream);
+            return wide ? launch_variant<kEpilogueWarps, true, false, kTopKRunning>(tmW, tmH, prm, smem, grid, stream)
+                        : launch_variant<kEpilogueWarps, false, false, kTopKRunning>(tmW, tmH, prm, smem, grid, stream);
+        }
+        if (topk_mode != kTopKTileLists) return cudaErrorInvalidValue;
         if (plain)
-            return wide ? launch_variant<kEpilogueWarps, true, false, true, true>(tmW, tmH, prm, smem, grid, stream)
-                        : launch_variant<kEpilogueWarps, false, false, true, true>(tmW, tmH, prm, smem, grid, stream);
-        return wide ? launch_variant<kEpilogueWarps, true, false, true>(tmW, tmH, prm, smem, grid, stream)
-                    : launch_variant<kEpilogueWarps, false, false, true>(tmW, tmH, prm, smem, grid, stream);
+            return wide ? launch_variant<kEpilogueWarps, true, false, kTopKTileLists, true>(tmW, tmH, prm, smem, grid, stream)
+                        : launch_variant<kEpilogueWarps, false, false, kTopKTileLists, true>(tmW, tmH, prm, smem, grid, stream);
+        return wide ? launch_variant<kEpilogueWarps, true, false, kTopKTileLists>(tmW, tmH, prm, smem, grid, stream)
+                    : launch_variant<kEpilogueWarps, false, false, kTopKTileLists>(tmW, tmH, prm, smem, grid, stream);
     }
     if (fp8) {
         if (plain)

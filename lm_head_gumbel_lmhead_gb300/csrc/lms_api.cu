@@ -343,6 +343,14 @@ lms_status lms_lmhead_sample_topk(const void* H, int64_t ldh, const void* W, int
     CUtensorMap tmW;
     if ((st = encode_bf16_map(&tmW, W, V, D, ldw, 128)) != LMS_OK) return st;
     const uint32_t timeout_ms = params->timeout_ms ? params->timeout_ms : 2000u;
+    // One list mode for the whole call, from the widest launch: running lists (one per row,
+    // Stage-1 CTA and TMEM quadrant; the persistent grid is min(n_tiles, SMs) CTAs) when they fit
+    // in shared memory, else one list per row, tile and quadrant.
+    const int64_t nb0 = B < kTcMaxBatchPerLaunch ? B : kTcMaxBatchPerLaunch;
+    a.topk_mode = lms::topk_mode_for(static_cast<int>(nb0 < 16 ? 16 : (nb0 + 15) / 16 * 16), k);
+    const int sms = lms::device_sm_count();
+    const int64_t n_lists =
+        a.topk_mode == lms::kTopKRunning ? 4 * (t.n_tiles < sms ? t.n_tiles : sms) : 4 * t.n_tiles;
     for (int64_t r0 = 0; r0 < B; r0 += kTcMaxBatchPerLaunch) {
         const int64_t nb = (B - r0 < kTcMaxBatchPerLaunch) ? B - r0 : kTcMaxBatchPerLaunch;
         const int n_pad = static_cast<int>(nb < 16 ? 16 : (nb + 15) / 16 * 16);
@@ -351,7 +359,7 @@ lms_status lms_lmhead_sample_topk(const void* H, int64_t ldh, const void* W, int
         lms::SampleArgs ac = a;
         ac.B = nb;
         ac.row0 = r0;
-        ac.cand_keys = a.cand_keys + r0 * t.n_tiles * 4 * k;
+        ac.cand_keys = a.cand_keys + r0 * n_lists * k;
         const cudaError_t e = lms::launch_lmhead_tc(tmW, tmH, D, n_pad, wide, timeout_ms,
                                                     params->debug_flags, ac, s);
         if (e != cudaSuccess) return cuda_fail(e, "tcgen05 top-k Stage-1 launch");
@@ -359,7 +367,7 @@ lms_status lms_lmhead_sample_topk(const void* H, int64_t ldh, const void* W, int
     unsigned long long* part = reinterpret_cast<unsigned long long*>(
         static_cast<char*>(workspace) + kStatusBlock +
         round_up(static_cast<size_t>(B) * static_cast<size_t>(t.n_tiles) * 4 * static_cast<size_t>(k) * 8, 256));
-    const cudaError_t e = lms::launch_stage2_topk(a.cand_keys, 4 * t.n_tiles, k, B, params->temperature,
+    const cudaError_t e = lms::launch_stage2_topk(a.cand_keys, n_lists, k, B, params->temperature,
                                                   out, scores, params->row_status, a.status_bits, part, s);
     if (e != cudaSuccess) return cuda_fail(e, "top-k Stage-2 launch");
     return LMS_OK;

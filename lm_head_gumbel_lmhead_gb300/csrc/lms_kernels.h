@@ -27,10 +27,12 @@ struct SampleArgs {
     // FP8 (W8A8) fused path only, else null: logits = acc * 2^h_exp[row] * w_scale[v]
     const int32_t* h_exp;
     const float* w_scale;
-    // Gumbel-top-k (topk > 0) only: [B][n_tiles][4][topk] ordered (score, index) keys per tile
-    // and TMEM quadrant
+    // Gumbel-top-k (topk > 0) only: ordered (score, index) key lists, per tile and TMEM quadrant
+    // ([B][n_tiles][4][topk], topk_mode kTopKTileLists) or per Stage-1 CTA and TMEM quadrant
+    // ([B][4 grid][topk], kTopKRunning)
     unsigned long long* cand_keys = nullptr;
     int topk = 0;
+    int topk_mode = 0;
     // the call's status word (the head of the workspace) or null: Stage 1 of the launch with
     // row0 == 0 clears it, Stage 2 sets bit s for every row that ends with status s != 0
     uint32_t* status_bits = nullptr;
@@ -122,7 +124,18 @@ cudaError_t launch_lmhead_gemv(const uint16_t* H, int64_t ldh, const uint16_t* W
 cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int64_t D, int n_pad,
                              bool wide, uint32_t timeout_ms, uint32_t debug_flags,
                              const SampleArgs& a, cudaStream_t stream, bool fp8 = false);
-// (a.topk > 0 selects the Gumbel-top-k epilogue: bf16 only.)
+// (a.topk > 0 selects the Gumbel-top-k epilogue: bf16 only; a.topk_mode says which lists.)
+
+// Gumbel-top-k list modes.  Running lists keep, in shared memory, each CTA's k best keys per
+// TMEM quadrant and batch column, written out once per CTA; they are used when they fit
+// (4 n_pad k keys of 8 bytes within kTopKRunningBytes), else each tile writes its own lists.
+constexpr int kTopKTileLists = 1;
+constexpr int kTopKRunning = 2;
+constexpr uint32_t kTopKRunningBytes = 32u * 1024u;
+inline int topk_mode_for(int n_pad, int k) {
+    return static_cast<uint32_t>(4 * n_pad) * static_cast<uint32_t>(k) * 8u <= kTopKRunningBytes ? kTopKRunning
+                                                                                                  : kTopKTileLists;
+}
 
 // The MXFP4-weight path (W4A16).  Wt is the tiled format mxfp4_pack writes (mxfp4_tiled_bytes(V, D)
 // bytes: one contiguous 4352-byte block per (128-row tile, 64-element K chunk)); tmH as for

@@ -86,6 +86,9 @@ __global__ void __launch_bounds__(kStage2Threads) stage2_kernel(
 // the top-k Stage 1 (measured).
 constexpr int kTopKThreads = 256;
 constexpr int kTopKMaxSplit = 32;
+// rows with at most this many lists are merged by one CTA of kTopKThreads threads (a few lists a
+// thread), which also writes the outputs
+constexpr int64_t kTopKOneCtaLists = 4 * kTopKThreads;
 
 // best <- the kM largest keys of best and q, both ordered largest first (kM a power of two).
 // The elementwise maximum of best and q reversed is a bitonic sequence holding the kM largest
@@ -110,10 +113,44 @@ __device__ __forceinline__ void merge_top(unsigned long long (&best)[kM], const 
     }
 }
 
-template <int kM>
+// The row's k best keys, ordered, in the lanes r < k of one warp (0 past the finite ones) -> the
+// indices, scores and status of row b.
+__device__ __forceinline__ void write_topk_row(int64_t b, unsigned long long mine, int k, int lane,
+                                               const float* __restrict__ temperature,
+                                               int64_t* __restrict__ out, float* __restrict__ scores,
+                                               int32_t* __restrict__ row_status,
+                                               uint32_t* __restrict__ status_bits) {
+    const unsigned long long top = __shfl_sync(0xffffffffu, mine, 0);
+    const float T = temperature ? temperature[b] : 1.0f;
+    const bool poisoned = top == tc::kPoisonKey;
+    const bool invalid = !(T >= 0.0f);
+    float sc = -CUDART_INF_F;
+    int64_t idx = -1;
+    if (lane < k && !poisoned && !invalid && mine != 0ull) {
+        sc = tc::unpack_score(mine);
+        idx = candidate_index(sc, tc::unpack_index(mine));
+        if (idx < 0) sc = -CUDART_INF_F;
+    }
+    if (lane < k) {
+        out[b * k + lane] = idx;
+        if (scores) scores[b * k + lane] = sc;
+    }
+    const int found = __popc(__ballot_sync(0xffffffffu, lane < k && idx >= 0));
+    if (lane == 0) {
+        const int status = poisoned ? 3 : invalid ? 2 : (found > 0 ? 0 : 1);
+        if (row_status) row_status[b] = status;
+        note_row_status(status_bits, status);
+    }
+}
+
+// kFinal: one CTA takes all of a row's lists (gridDim.x == 1) and its first warp writes the row's
+// indices, scores and status directly (no part lists, no second kernel).
+template <int kM, bool kFinal>
 __global__ void __launch_bounds__(kTopKThreads) stage2_topk_part(
     const unsigned long long* __restrict__ cand_keys, int64_t n_lists, int k,
-    unsigned long long* __restrict__ part_keys) {
+    unsigned long long* __restrict__ part_keys, const float* __restrict__ temperature,
+    int64_t* __restrict__ out, float* __restrict__ scores, int32_t* __restrict__ row_status,
+    uint32_t* __restrict__ status_bits) {
     // lst[r * kTopKThreads + t]: rank r of thread t's list (thread-minor, so that the threads of
     // a warp touch distinct banks)
     extern __shared__ unsigned long long lst[];
@@ -180,7 +217,14 @@ __global__ void __launch_bounds__(kTopKThreads) stage2_topk_part(
         }
         __syncthreads();
     }
-    if (tid < k) part_keys[(b * S + s) * k + tid] = at(lst, tid);
+    if constexpr (kFinal) {
+        if (tid < 32) {
+            const unsigned long long mine = tid < k ? at(lst, tid) : 0ull;
+            write_topk_row(b, mine, k, tid, temperature, out, scores, row_status, status_bits);
+        }
+    } else {
+        if (tid < k) part_keys[(b * S + s) * k + tid] = at(lst, tid);
+    }
 }
 
 // Part 2: one warp per row takes the k best of the row's S ordered part lists by k rounds of a
@@ -223,27 +267,7 @@ __global__ void __launch_bounds__(256) stage2_topk_final(
             best[kM - 1] = 0ull;
         }
     }
-    const unsigned long long top = __shfl_sync(0xffffffffu, mine, 0);
-    const float T = temperature ? temperature[b] : 1.0f;
-    const bool poisoned = top == tc::kPoisonKey;
-    const bool invalid = !(T >= 0.0f);
-    float sc = -CUDART_INF_F;
-    int64_t idx = -1;
-    if (lane < k && !poisoned && !invalid && mine != 0ull) {
-        sc = tc::unpack_score(mine);
-        idx = candidate_index(sc, tc::unpack_index(mine));
-        if (idx < 0) sc = -CUDART_INF_F;
-    }
-    if (lane < k) {
-        out[b * k + lane] = idx;
-        if (scores) scores[b * k + lane] = sc;
-    }
-    const int found = __popc(__ballot_sync(0xffffffffu, lane < k && idx >= 0));
-    if (lane == 0) {
-        const int status = poisoned ? 3 : invalid ? 2 : (found > 0 ? 0 : 1);
-        if (row_status) row_status[b] = status;
-        note_row_status(status_bits, status);
-    }
+    write_topk_row(b, mine, k, lane, temperature, out, scores, row_status, status_bits);
 }
 
 }  // namespace
@@ -264,21 +288,23 @@ cudaError_t launch_stage2_topk(const unsigned long long* cand_keys, int64_t n_li
                                unsigned long long* part_keys, cudaStream_t stream) {
     if (k < 1 || k > tc::kMaxTopK) return cudaErrorInvalidValue;
     const size_t smem = static_cast<size_t>(kTopKThreads) * k * sizeof(unsigned long long);
-    for (const void* f : {reinterpret_cast<const void*>(stage2_topk_part<1>),
-                          reinterpret_cast<const void*>(stage2_topk_part<2>),
-                          reinterpret_cast<const void*>(stage2_topk_part<4>),
-                          reinterpret_cast<const void*>(stage2_topk_part<8>),
-                          reinterpret_cast<const void*>(stage2_topk_part<16>)}) {
-        const cudaError_t e = ensure_dynamic_smem(f, smem);
-        if (e != cudaSuccess) return e;
-    }
-    const int S = static_cast<int>(stage2_topk_split(B));
-    auto part = k <= 1 ? stage2_topk_part<1> : k <= 2 ? stage2_topk_part<2>
-              : k <= 4 ? stage2_topk_part<4> : k <= 8 ? stage2_topk_part<8> : stage2_topk_part<16>;
-    part<<<dim3(static_cast<unsigned>(S), static_cast<unsigned>(B)), kTopKThreads, smem, stream>>>(
-        cand_keys, n_lists, k, part_keys);
-    cudaError_t e = cudaGetLastError();
+    // A row of at most kTopKOneCtaLists lists (the running lists: 4 per Stage-1 CTA) is merged by
+    // one CTA, which writes the outputs; more lists (one per tile and quadrant) are split over S
+    // CTAs per row and merged by the final kernel.
+    const bool one_cta = n_lists <= kTopKOneCtaLists;
+    auto part = one_cta ? (k <= 1 ? stage2_topk_part<1, true> : k <= 2 ? stage2_topk_part<2, true>
+                           : k <= 4 ? stage2_topk_part<4, true> : k <= 8 ? stage2_topk_part<8, true>
+                                                                        : stage2_topk_part<16, true>)
+                        : (k <= 1 ? stage2_topk_part<1, false> : k <= 2 ? stage2_topk_part<2, false>
+                           : k <= 4 ? stage2_topk_part<4, false> : k <= 8 ? stage2_topk_part<8, false>
+                                                                        : stage2_topk_part<16, false>);
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(part), smem);
     if (e != cudaSuccess) return e;
+    const int S = one_cta ? 1 : static_cast<int>(stage2_topk_split(B));
+    part<<<dim3(static_cast<unsigned>(S), static_cast<unsigned>(B)), kTopKThreads, smem, stream>>>(
+        cand_keys, n_lists, k, part_keys, temperature, out, scores, row_status, status_bits);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || one_cta) return e;
     auto fin = k <= 1 ? stage2_topk_final<1> : k <= 2 ? stage2_topk_final<2>
              : k <= 4 ? stage2_topk_final<4> : k <= 8 ? stage2_topk_final<8> : stage2_topk_final<16>;
     cudaLaunchConfig_t cfg = {};

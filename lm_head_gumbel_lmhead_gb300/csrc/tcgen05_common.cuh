@@ -484,5 +484,164 @@ __device__ __forceinline__ void epilogue_tile_topk(const SampleArgs& a, const Ro
     }
 }
 
+// Gumbel-top-k with running lists (used when they fit in shared memory): per TMEM quadrant and
+// batch column, the ordered k largest keys of the quadrant's rows over the CTA's tiles so far,
+// run[(quad * n_pad + b) * k + r], larger first, key 0 for an empty slot.  The list of (b, quad)
+// belongs to one epilogue lane (lane b % 8 of the quadrant's warp that takes b's column chunk),
+// which alone writes it while the tiles run.  Scores and extraction rounds as in
+// epilogue_tile_topk.  The threshold is the largest k-th key among row b's four quadrant lists:
+// that quadrant alone holds k keys above it, so no key at or below it is among the row's k best,
+// and since the lists' k-th keys only grow, reading another quadrant's while its owner updates it
+// gives a threshold that is still valid, if lower.  After a CTA's first tiles almost every chunk
+// ends before its first round.  Nothing is written to global memory per tile:
+// topk_running_lists_publish writes each list once, after the CTA's last tile.
+template <int kEpiWarps, bool kWide, bool kPlain = false>
+__device__ __forceinline__ void epilogue_tile_topk_running(const SampleArgs& a, const RowParams* rows,
+                                                           float* tr, unsigned long long* run, int n_pad,
+                                                           uint32_t t_row, int64_t tile, int quad,
+                                                           int col_group, int lane, int B) {
+    constexpr int kColGroups = kEpiWarps / 4;
+    const int k = a.topk;
+    const int n_chunks = (B + 7) / 8;
+    const int my_col = lane & 7;
+    const int my_r0 = (lane >> 3) * 8;
+    const int64_t v0 = tile * kTileV + 32 * quad + my_r0;   // a multiple of 8
+    for (int cc = col_group; cc < n_chunks; cc += kColGroups) {
+        uint32_t acc[8];
+        tmem_load_8(t_row + 8u * cc, acc);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) tr[j * kTrStride + lane] = __uint_as_float(acc[j]);
+        __syncwarp();
+        float y[8];
+        const float4 y0 = *reinterpret_cast<const float4*>(tr + my_col * kTrStride + my_r0);
+        const float4 y1 = *reinterpret_cast<const float4*>(tr + my_col * kTrStride + my_r0 + 4);
+        __syncwarp();
+        y[0] = y0.x; y[1] = y0.y; y[2] = y0.z; y[3] = y0.w;
+        y[4] = y1.x; y[5] = y1.y; y[6] = y1.z; y[7] = y1.w;
+        const int b = cc * 8 + my_col;
+        const int bb = b < B ? b : 0;
+        unsigned long long* lst = run + (static_cast<int64_t>(quad) * n_pad + bb) * k;
+        unsigned long long theta = 0ull;
+        if (b < B) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const unsigned long long t = *reinterpret_cast<volatile const unsigned long long*>(
+                    run + (static_cast<int64_t>(q4) * n_pad + bb) * k + (k - 1));
+                theta = t > theta ? t : theta;
+            }
+        }
+        unsigned long long ky[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ky[e] = 0ull;
+        if (b < B && v0 < a.V) {
+            const RowParams p = rows[b];
+            if (!(p.flags & kRowInvalid)) {
+                float g[8];
+                if (p.flags & kRowGreedy) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) g[e] = 0.0f;
+                } else {
+                    gumbel_run<kWide, 8>(p.key, static_cast<uint32_t>(v0), g);
+                }
+                const int64_t row = a.row0 + b;
+                if constexpr (kPlain) {
+                    // no bias and no mask in this launch: s = y / T + g (greedy: y); a NaN score
+                    // fails the -inf test below and gets no key, as a masked entry
+                    const float scale = (p.flags & kRowGreedy) ? 1.0f : p.inv_t;
+                    const int v0i = static_cast<int>(v0);
+                    const int n_in = (a.V - v0 < 8) ? static_cast<int>(a.V - v0) : 8;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float sc = fmaf(y[e], scale, g[e]);
+                        const unsigned long long key = pack_candidate(sc, v0i + e);
+                        ky[e] = (e < n_in && sc > -CUDART_INF_F && key > theta) ? key : 0ull;
+                    }
+                } else {
+                    const float* brow = a.bias ? a.bias + row * a.ld_bias : nullptr;
+                    const uint32_t mword =
+                        a.mask ? (__ldg(a.mask + row * a.ld_mask + (v0 >> 5)) >> (v0 & 31)) : 0xffu;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int64_t v = v0 + e;
+                        if (v < a.V) {
+                            const float bias = brow ? __ldg(brow + v) : 0.0f;
+                            const float sc = perturb(p, y[e], bias, (mword >> e) & 1u, g[e]);
+                            const unsigned long long key = pack_candidate(sc, static_cast<int>(v));
+                            ky[e] = (sc > -CUDART_INF_F && key > theta) ? key : 0ull;
+                        }
+                    }
+                }
+            }
+        }
+        // rounds: the column's best remaining key; its owner drops it and, while it beats the
+        // threshold (the row-wide one, raised by the owner's own list as it fills), inserts it;
+        // after each round the 4 lanes of a column take the owner's threshold.  A chunk with no
+        // key left above its thresholds (most chunks after a CTA's first tiles) skips the rounds.
+        unsigned long long kth = theta;
+        bool mine = false;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mine = mine || ky[e] != 0ull;
+        const int rounds = __any_sync(0xffffffffu, mine) ? k : 0;
+        for (int r = 0; r < rounds; ++r) {
+            unsigned long long bk = 0ull;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) bk = ky[e] > bk ? ky[e] : bk;
+            unsigned long long wk = bk;
+#pragma unroll
+            for (int off = 8; off <= 16; off <<= 1) {
+                const unsigned long long o = __shfl_xor_sync(0xffffffffu, wk, off);
+                wk = o > wk ? o : wk;
+            }
+            // no column of the warp has a key left that would enter its list
+            if (!__any_sync(0xffffffffu, wk > kth)) break;
+            if (wk != 0ull && wk == bk) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ky[e] = ky[e] == bk ? 0ull : ky[e];
+            }
+            if (lane < 8 && b < B && wk > kth) {
+                // insertion into the ordered list: carry the displaced key down.  The list's new
+                // k-th key is the smaller of wk and its old (k-1)-th (for k = 1: wk), kept in a
+                // register rather than read back.
+                unsigned long long cur = wk, before_last = wk;
+#pragma unroll
+                for (int i = 0; i < kMaxTopK; ++i) {
+                    if (i < k) {
+                        const unsigned long long li = lst[i];
+                        if (i == k - 2) before_last = li;
+                        lst[i] = cur > li ? cur : li;
+                        cur = cur > li ? li : cur;
+                    }
+                }
+                const unsigned long long own = (k >= 2 && before_last < wk) ? before_last : wk;
+                kth = own > kth ? own : kth;
+            }
+            kth = __shfl_sync(0xffffffffu, kth, lane & 7);
+        }
+    }
+}
+
+// After the CTA's last tile: each owner lane writes its running lists to the workspace,
+// uint64 [B][4 G][k] (G = gridDim.x): list (b, blockIdx.x, quad) at ((b * 4 G) + 4 blockIdx.x +
+// quad) * k.  A CTA whose bounded wait ran out (ok false, the same in every epilogue thread)
+// heads each list with the poison key instead.
+template <int kEpiWarps>
+__device__ __forceinline__ void topk_running_lists_publish(const SampleArgs& a, const unsigned long long* run,
+                                                           int n_pad, int quad, int col_group, int lane,
+                                                           int B, bool ok) {
+    constexpr int kColGroups = kEpiWarps / 4;
+    const int k = a.topk;
+    const int n_chunks = (B + 7) / 8;
+    for (int cc = col_group; cc < n_chunks; cc += kColGroups) {
+        const int b = cc * 8 + (lane & 7);
+        if (lane < 8 && b < B) {
+            const unsigned long long* lst = run + (static_cast<int64_t>(quad) * n_pad + b) * k;
+            unsigned long long* out =
+                a.cand_keys + ((static_cast<int64_t>(b) * 4 * gridDim.x + 4 * blockIdx.x + quad) * k);
+            out[0] = ok ? lst[0] : kPoisonKey;
+            for (int i = 1; i < k; ++i) out[i] = lst[i];
+        }
+    }
+}
+
 }  // namespace tc
 }  // namespace lms
