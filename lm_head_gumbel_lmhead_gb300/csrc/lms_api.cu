@@ -276,11 +276,28 @@ lms_status lms_lmhead_sample(const void* H, int64_t ldh, const void* W, int64_t 
         CUtensorMap tmW;
         if ((st = encode_bf16_map(&tmW, W, V, D, ldw, 128)) != LMS_OK) return st;
         const uint32_t timeout_ms = params->timeout_ms ? params->timeout_ms : 2000u;
-        // Batches above 256 rows run as several launches of <= 256 rows (one MMA N each).
-        for (int64_t r0 = 0; r0 < B; r0 += kTcMaxBatchPerLaunch) {
-            const int64_t nb = (B - r0 < kTcMaxBatchPerLaunch) ? B - r0 : kTcMaxBatchPerLaunch;
+        // Batches above 256 rows (one MMA N) run as row-group launches of up to 1024 rows that
+        // stream W once each (lmhead_tc_rows.cu); a remainder of <= 256 rows, and the pair path,
+        // as launches of <= 256 rows.
+        const bool pair = path == LMS_PATH_TCGEN05_PAIR;
+        constexpr int64_t kRowGroupLaunch = static_cast<int64_t>(lms::kMaxRowGroups) * kTcMaxBatchPerLaunch;
+        for (int64_t r0 = 0, nb = 0; r0 < B; r0 += nb) {
+            if (!pair && B - r0 > kTcMaxBatchPerLaunch) {
+                nb = (B - r0 < kRowGroupLaunch) ? B - r0 : kRowGroupLaunch;
+                CUtensorMap tmH;
+                if ((st = encode_bf16_map(&tmH, H, B, D, ldh, static_cast<int>(kTcMaxBatchPerLaunch))) != LMS_OK)
+                    return st;
+                lms::SampleArgs ac = a;
+                ac.B = nb;
+                ac.row0 = r0;
+                ac.cand_score = a.cand_score + r0 * t.n_tiles;
+                ac.cand_index = a.cand_index + r0 * t.n_tiles;
+                e = lms::launch_lmhead_tc_rows(tmW, tmH, D, wide, timeout_ms, params->debug_flags, ac, s);
+                if (e != cudaSuccess) return cuda_fail(e, "tcgen05 row-group Stage-1 launch");
+                continue;
+            }
+            nb = (B - r0 < kTcMaxBatchPerLaunch) ? B - r0 : kTcMaxBatchPerLaunch;
             const int n_pad = static_cast<int>(nb < 16 ? 16 : (nb + 15) / 16 * 16);
-            const bool pair = path == LMS_PATH_TCGEN05_PAIR;
             CUtensorMap tmH;
             if ((st = encode_bf16_map(&tmH, H, B, D, ldh, pair ? n_pad / 2 : n_pad)) != LMS_OK) return st;
             lms::SampleArgs ac = a;

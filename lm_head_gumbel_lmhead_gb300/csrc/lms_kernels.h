@@ -126,6 +126,14 @@ cudaError_t launch_lmhead_tc(const CUtensorMap& tmW, const CUtensorMap& tmH, int
                              const SampleArgs& a, cudaStream_t stream, bool fp8 = false);
 // (a.topk > 0 selects the Gumbel-top-k epilogue: bf16 only; a.topk_mode says which lists.)
 
+// Batches of 257 .. 1024 rows in one launch (bf16 race only): up to kMaxRowGroups groups of 256
+// rows whose CTAs walk the vocabulary tiles together, so W streams from HBM once.  tmH has a box
+// of 256 rows; a.B is the launch's row count.
+constexpr int kMaxRowGroups = 4;
+cudaError_t launch_lmhead_tc_rows(const CUtensorMap& tmW, const CUtensorMap& tmH, int64_t D, bool wide,
+                                  uint32_t timeout_ms, uint32_t debug_flags, const SampleArgs& a,
+                                  cudaStream_t stream);
+
 // Gumbel-top-k list modes.  Running lists keep, in shared memory, each CTA's k best keys per
 // TMEM quadrant and batch column, written out once per CTA; they are used when they fit
 // (4 n_pad k keys of 8 bytes within kTopKRunningBytes), else each tile writes its own lists.

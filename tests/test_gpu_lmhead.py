@@ -108,9 +108,23 @@ def test_tcgen05_ragged(B, D, V, wide):
                                                  (1100, 64, 2100, True, True),
                                                  (520, 96, 1500, False, False)])
 def test_tcgen05_batches_above_256(B, D, V, wide, features):
-    # above 256 rows the tcgen05 path runs one launch per 256 rows: 3 launches (700), 5 (1100), and
-    # 3 with an 8-row last one (520)
+    # above 256 rows the tcgen05 path runs row-group launches of up to 1024 rows (groups of 256
+    # whose CTAs share each tile of W): one launch of 3 groups (700), one of 4 groups and a 76-row
+    # single-group launch (1100), one of 3 groups with an 8-row last group (520)
     full_parity(_ragged(B, D, V, seed=B + V, wide=wide, features=features), lms.PATH_TCGEN05)
+
+
+def test_row_group_timeout_poisons_its_group_only():
+    # CTA 0 serves row group 0; its withheld first load runs out, so every row of group 0 (one
+    # tile of each is CTA 0's) reports status 3 and the other group's rows are sampled as usual
+    w = _ragged(300, 128, 3000, seed=23, features=False)
+    d = to_dev(w)
+    out, st, _, ci = run_fused(w, d, lms.PATH_TCGEN05, timeout_ms=20,
+                               debug_flags=lms.DEBUG_WITHHOLD_FIRST_LOAD)
+    assert (st[:256] == lms.ROW_DEVICE_TIMEOUT).all() and (out[:256] == -1).all()
+    assert (st[256:] != lms.ROW_DEVICE_TIMEOUT).all()
+    # the next call on the same context is correct
+    full_parity(w, lms.PATH_TCGEN05)
 
 
 def test_tcgen05_without_optional_inputs():
@@ -183,7 +197,8 @@ def test_large_vocab_wide_noise_every_row_b128():
 
 
 def test_large_vocab_wide_noise_b512_launch_boundaries():
-    # two launches of 256 rows: rows on both sides of the boundary and at both ends
+    # one row-group launch of two groups of 256 rows: rows on both sides of the group boundary and
+    # at both ends
     w = workloads.large_vocab(512)
     rows = list(range(0, 8)) + list(range(248, 264)) + list(range(504, 512))
     sampled_parity(w, rows)
