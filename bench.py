@@ -69,12 +69,31 @@ UNIT = "us/step"
 TC_SOURCES = ["lm_head_gumbel_lmhead_gb300/csrc/lmhead_tc.cu",
               "lm_head_gumbel_lmhead_gb300/csrc/tcgen05_common.cuh",
               "lm_head_gumbel_lmhead_gb300/csrc/lms_device.cuh"]
+# the Stage-1 kernel of each fused workload and its sources: the single-group kernel, the row-group
+# kernel (race workloads above 256 rows) and the MXFP4 kernel
+STAGE1_SOURCES = {
+    "tc": TC_SOURCES,
+    "rows": ["lm_head_gumbel_lmhead_gb300/csrc/lmhead_tc_rows.cu",
+             "lm_head_gumbel_lmhead_gb300/csrc/tcgen05_common.cuh",
+             "lm_head_gumbel_lmhead_gb300/csrc/lms_device.cuh"],
+    "mx": ["lm_head_gumbel_lmhead_gb300/csrc/lmhead_mx.cu",
+           "lm_head_gumbel_lmhead_gb300/csrc/tcgen05_common.cuh",
+           "lm_head_gumbel_lmhead_gb300/csrc/lms_device.cuh"],
+}
 FUSED = ("qwen3-8b", "llama3-hetero", "large-vocab", "qwen3-8b-fp8", "qwen3-8b-topk", "qwen3-8b-mxfp4")
 
 
-def kernel_source_hash() -> str:
+def stage1_kind(workload: str, B: int) -> str:
+    if workload == "qwen3-8b-mxfp4":
+        return "mx"
+    if workload in ("qwen3-8b", "llama3-hetero", "large-vocab") and B > 256:
+        return "rows"
+    return "tc"
+
+
+def kernel_source_hash(kind: str = "tc") -> str:
     h = hashlib.sha256()
-    for p in TC_SOURCES:
+    for p in STAGE1_SOURCES[kind]:
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -93,15 +112,15 @@ def measured_peaks() -> dict:
 
 
 def recorded_traffic(workload: str, B: int):
-    """DRAM bytes per launch of the fused kernel from the committed ncu summary, if it was taken
-    for this workload on the current kernel source (else None)."""
+    """DRAM bytes per launch of the fused Stage-1 kernel from the committed ncu summary, if it was
+    taken for this workload on the current sources of that kernel (else None)."""
     p = os.path.join(ROOT, "profiles", "lmhead_tc_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     rec = d.get(f"{workload}/B={B}")
-    if rec is None or rec.get("kernel_source_hash") != kernel_source_hash():
+    if rec is None or rec.get("kernel_source_hash") != kernel_source_hash(stage1_kind(workload, B)):
         return None
     return rec
 
@@ -522,6 +541,7 @@ def run_gpu(args):
         kernel = ("quantize_rows_e4m3_kernel + " if fp8 else "") + \
             ("lmhead_tc_kernel (top-k epilogue) + stage2_topk_kernel" if topk else
              "lmhead_mx_kernel + stage2_kernel" if mx else
+             "lmhead_tc_rows_kernel (row groups) + stage2_kernel" if path == 2 and B > 256 else
              "lmhead_tc_kernel + stage2_kernel") + " (one step, CUDA events)"
     elif args.workload == "logits":
         V = args.V or 131072
