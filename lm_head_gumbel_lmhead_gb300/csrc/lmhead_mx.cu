@@ -36,11 +36,12 @@
 //                    SM about 300 cycles of issue once eight or more warps share it, against ~420
 //                    cycles of tensor time for its four MMAs; sixteen warps leave room for each
 //                    group's barrier waits and loads to overlap the others' rebuilding.
-//   warps 19..22     epilogue: as in the bf16 kernel (transform, noise, argmax per tile), over the
+//   warps 19..26     epilogue: as in the bf16 kernel (transform, noise, argmax per tile), over the
 //                    tiles in order, each from its stream's accumulator.
 // Ring A (packed codes and scales, 4.25 KB a stage, half the stages per stream) is deep so that
 // enough weight bytes are in flight to keep HBM busy.  TMEM holds eight rebuilt-weight slots of 32
-// columns (four per stream) in columns 0..255 and the two accumulators from column 256; ring H has
+// columns (four per stream) in columns 0..255 and, from column 256, each stream's accumulators (two
+// when 4 n_pad <= 256, so a stream's next tile need not wait for the epilogue; else one); ring H has
 // one activation stage per slot, and one tcgen05.commit per chunk frees both.  Every wait is
 // bounded in time; a CTA whose wait runs out flags the error, drains its copies and MMAs, poisons
 // its remaining candidates (row status 3), frees TMEM and exits.
@@ -60,7 +61,7 @@ using namespace tc;
 constexpr int kMxStreams = 2;
 constexpr int kMxGroups = 4;                           // converter groups of four warps, two per stream
 constexpr int kMxConvWarps = 4 * kMxGroups;
-constexpr int kMxEpiWarps = 4;
+constexpr int kMxEpiWarps = 8;
 constexpr int kMxFirstConv = 3;
 constexpr int kMxFirstEpi = kMxFirstConv + kMxConvWarps;
 constexpr int kMxThreads = 32 * (kMxFirstEpi + kMxEpiWarps);
@@ -68,8 +69,8 @@ constexpr int kMxThreads = 32 * (kMxFirstEpi + kMxEpiWarps);
 // of a stream is only ever read by one of its two groups (the one taking chunks of parity k % 2).
 constexpr int kMaxStagesA = 32;
 // TMEM: slot t (stream t / 4, the stream's slot t % 4) holds one rebuilt 128 x 64 bf16 chunk in
-// columns 32 t .. 32 t + 31; the accumulator of stream s starts at column 256 + s * n_pad
-// (n_pad <= 128).
+// columns 32 t .. 32 t + 31; from column 256, each stream's accumulators: two (double-buffered, so a
+// stream's next tile need not wait for the epilogue) when 4 n_pad <= 256, else one (n_pad <= 128).
 constexpr int kSlotsPerStream = 4;
 constexpr int kSlots = kMxStreams * kSlotsPerStream;
 constexpr uint32_t kSlotCols = kBK / 2;
@@ -86,6 +87,7 @@ struct MxParams {
     int nk;              // K chunks of 64, ceil(D / 64)
     int n_pad;
     int stages_a;
+    int acc_bufs;             // accumulators per stream: 2 when 4 n_pad columns fit beside the slots
     uint32_t h_stage_bytes;   // n_pad * 128
     uint64_t timeout_ns;
     uint32_t debug_flags;
@@ -101,8 +103,8 @@ struct MxLayout {
         a_off = h_off + kSlots * h_stage_bytes;
         bars_off = a_off + sa * kAStageBytes;
         // fullA, emptyA [SA]; fullC (slot written, count 4), emptyC (slot and its H stage free,
-        // one commit), fullH [kSlots]; acc_full[2], acc_empty[2], drain[2]
-        misc_off = bars_off + (2 * sa + 3 * kSlots + 6) * 8;
+        // one commit), fullH [kSlots]; acc_full[4], acc_empty[4] (stream x buffer), drain[2]
+        misc_off = bars_off + (2 * sa + 3 * kSlots + 10) * 8;
         rows_off = (misc_off + 16 + 15) & ~15u;   // misc: tmem slot, error flag
         red_off = rows_off + n_pad * static_cast<uint32_t>(sizeof(RowParams));
         tr_off = red_off + n_pad * 8;
@@ -271,9 +273,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     auto emptyC = [&](int t) { return bar0 + 8u * (2 * SA + kSlots + t); };
     auto fullH = [&](int t) { return bar0 + 8u * (2 * SA + 2 * kSlots + t); };
     const uint32_t acc0 = bar0 + 8u * (2 * SA + 3 * kSlots);
-    auto accf_bar = [&](int st) { return acc0 + 8u * st; };
-    auto acce_bar = [&](int st) { return acc0 + 8u * (2 + st); };
-    auto drain_bar = [&](int st) { return acc0 + 8u * (4 + st); };
+    auto accf_bar = [&](int st, int ab) { return acc0 + 8u * (2 * st + ab); };
+    auto acce_bar = [&](int st, int ab) { return acc0 + 8u * (4 + 2 * st + ab); };
+    auto drain_bar = [&](int st) { return acc0 + 8u * (8 + st); };
+    // accumulator (stream st, buffer ab) in TMEM columns kAccCol0 + (st * bufs + ab) * n_pad
+    const int bufs = prm.acc_bufs;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.misc_off);
     volatile int* err = reinterpret_cast<volatile int*>(base + L.misc_off + 4);
     RowParams* rows = reinterpret_cast<RowParams*>(base + L.rows_off);
@@ -290,8 +294,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             mbar_init(fullH(t), 1);
         }
         for (int st = 0; st < kMxStreams; ++st) {
-            mbar_init(accf_bar(st), 1);
-            mbar_init(acce_bar(st), kMxEpiWarps);
+            for (int ab = 0; ab < 2; ++ab) {
+                mbar_init(accf_bar(st, ab), 1);
+                mbar_init(acce_bar(st, ab), kMxEpiWarps);
+            }
             mbar_init(drain_bar(st), 1);
         }
         *err = 0;
@@ -363,13 +369,15 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         const int st = warp - 1;
         const bool leader = elect_one();
         const uint32_t idesc = mma_idesc_bf16(n_pad, kTileV);
-        const uint32_t d_tmem = tmem_base + kAccCol0 + static_cast<uint32_t>(st * n_pad);
         bool ok = true;
         int idx = 0;
         uint32_t pt = 0;
         for (int64_t k = 0; k < tiles_of(st) && ok; ++k) {
-            // the epilogue is done with this stream's previous tile
-            if (!__all_sync(0xffffffffu, mbar_wait_suspend(acce_bar(st), static_cast<uint32_t>(k & 1) ^ 1u,
+            const int ab = bufs == 2 ? static_cast<int>(k & 1) : 0;
+            const uint32_t round = static_cast<uint32_t>(bufs == 2 ? k >> 1 : k);
+            const uint32_t d_tmem = tmem_base + kAccCol0 + static_cast<uint32_t>((st * bufs + ab) * n_pad);
+            // the epilogue is done with the tile this accumulator held before
+            if (!__all_sync(0xffffffffu, mbar_wait_suspend(acce_bar(st, ab), (round & 1u) ^ 1u,
                                                    prm.timeout_ns, err, kSuspendNs))) {
                 ok = false;
                 break;
@@ -397,7 +405,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                 if (++idx == kSlotsPerStream) { idx = 0; pt ^= 1u; }
             }
             if (!ok) break;
-            if (leader) mma_commit(accf_bar(st));
+            if (leader) mma_commit(accf_bar(st, ab));
             __syncwarp();
         }
         if (!ok && lane == 0) *err = 1;
@@ -514,8 +522,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         bool ok = true;
         for (int64_t tile = blockIdx.x; tile < nt; tile += gridDim.x, ++i) {
             const int st = i & 1;
-            const uint32_t use_parity = (i >> 1) & 1;
-            if (ok) ok = mbar_wait_suspend(accf_bar(st), use_parity, prm.timeout_ns, err, kSuspendNs);
+            const int k = i >> 1;                        // the stream's k-th tile
+            const int ab = bufs == 2 ? (k & 1) : 0;
+            const uint32_t use_parity = static_cast<uint32_t>(bufs == 2 ? k >> 1 : k) & 1u;
+            if (ok) ok = mbar_wait_suspend(accf_bar(st, ab), use_parity, prm.timeout_ns, err, kSuspendNs);
             ok = epi_barrier_and(epi_threads, ok);
             if (!ok) {
                 if (epi_tid == 0) *err = 1;
@@ -527,12 +537,12 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             }
             tc_fence_after_sync();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + kAccCol0 +
-                                   static_cast<uint32_t>(st * n_pad);
+                                   static_cast<uint32_t>((st * bufs + ab) * n_pad);
             epilogue_tile_columns<kMxEpiWarps, kWide, kPlain>(a, rows, red, tr, t_row, tile, quad,
                                                               col_group, lane, B);
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acce_bar(st));
+            if (lane == 0) mbar_arrive(acce_bar(st, ab));
             epi_barrier(epi_threads);
             for (int b = epi_tid; b < B; b += epi_threads) {
                 const unsigned long long key = red[b];
@@ -597,6 +607,7 @@ cudaError_t launch_lmhead_mx(const uint8_t* Wt, const CUtensorMap& tmH, int64_t 
     while (fixed + sa * kAStageBytes > budget && sa > 8) sa -= 4;
     if (fixed + sa * kAStageBytes > budget) return cudaErrorInvalidValue;
     prm.stages_a = sa;
+    prm.acc_bufs = 4 * n_pad <= static_cast<int>(kMxTmemCols - kAccCol0) ? 2 : 1;
     prm.timeout_ns = static_cast<uint64_t>(timeout_ms) * 1000000ull;
     prm.debug_flags = debug_flags;
     const MxLayout L(sa, prm.h_stage_bytes, n_pad);
