@@ -10,13 +10,13 @@
 // two bf16 of K per 32-bit column), so the tensor cores run the same bf16 x bf16 -> fp32
 // contraction and the rebuilt weights never pass through shared memory.
 //
-// The tensor cores take about as long for one M = 128, K = 16 instruction at N = 16 as at
-// N = 128 (measured: ~105 cycles), so at decode batch sizes the weight stream is bounded by the
-// instruction rate, and any gap between a chunk's MMAs and the next (barrier wait, fence, commit)
-// leaves the tensor cores idle.  The CTA therefore runs two independent streams: stream s takes
-// the CTA's vocabulary tiles of parity s, with its own MMA warp, converter group, ring-A stages,
-// TMEM slots and accumulator, so one stream's handshakes overlap the other's MMAs.  Each tile is
-// still accumulated in a fixed order by one warp.
+// One thread issues a tcgen05.mma of M = 128, K = 16 about every 105-117 cycles whatever N is
+// (measured), while the tensor cores accept several threads' MMAs at once.  A single MMA warp would
+// bound the weight stream at decode batch sizes, with every gap between a chunk's MMAs and the next
+// (barrier wait, fence, commit) idle.  The CTA therefore runs two independent streams: stream s
+// takes the CTA's vocabulary tiles of parity s, with its own MMA warp, converter groups, ring-A
+// stages, TMEM slots and accumulators, so the two issue at once.  Each tile is still accumulated
+// in a fixed order by one warp.
 //
 // Warp roles (one persistent CTA per SM):
 //   warp 0           bulk-copy producer of the packed weights for both streams: the library's
@@ -33,9 +33,9 @@
 //                    per pair), and stores them with tcgen05.st into the chunk's TMEM slot.  The
 //                    group's first warp also issues the TMA load of the chunk's activations
 //                    [n_pad x 64] bf16 into the slot's ring-H stage.  Rebuilding a chunk takes the
-//                    SM about 300 cycles of issue once eight or more warps share it, against ~420
-//                    cycles of tensor time for its four MMAs; sixteen warps leave room for each
-//                    group's barrier waits and loads to overlap the others' rebuilding.
+//                    SM about 300 cycles of integer-pipe issue once eight or more warps share it,
+//                    which bounds this kernel; sixteen warps let each group's barrier waits and
+//                    loads overlap the others' rebuilding.
 //   warps 19..26     epilogue: as in the bf16 kernel (transform, noise, argmax per tile), over the
 //                    tiles in order, each from its stream's accumulator.
 // Ring A (packed codes and scales, 4.25 KB a stage, half the stages per stream) is deep so that
