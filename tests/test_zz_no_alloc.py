@@ -88,8 +88,9 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
 
 @pytest.mark.gpu
 def test_noalloc_fills_its_scratch_across_launches():
-    # B * ceil(V / 128) = 512 * 1024 = 524288 candidates: the whole array, written by two Stage-1
-    # launches of 256 rows (the second at candidate offset 256 * 1024); then a smaller call
+    # B * ceil(V / 128) = 512 * 1024 = 524288 candidates: the whole array, written by one row-group
+    # Stage-1 launch of two groups of 256 rows (the second group from candidate offset 256 * 1024);
+    # then a smaller call
     L = _lib()
     w = _case(512, 64, 131072, seed=5)
     out_ref, st_ref, out_new, st_new = _run_both(L, w, torch.arange(w.B, dtype=torch.int64) * 3, True)
