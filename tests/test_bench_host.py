@@ -98,3 +98,21 @@ def test_recorded_counters_follow_the_kernel_sources(tmp_path, monkeypatch):
     fake.write_text("// another kernel\n")
     monkeypatch.setitem(bench.ALU_SOURCES, "noise", [str(fake)])
     assert bench.recorded_instructions("noise/B=64/V=151936", "noise") is None
+
+
+def test_traffic_records_follow_their_own_stage1_kernel():
+    # each fused workload's DRAM record is tied to the sources of the Stage-1 kernel that runs it:
+    # the MXFP4 kernel, the row-group kernel above 256 rows (race workloads), else the single-group one
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.stage1_kind("qwen3-8b-mxfp4", 1) == "mx"
+    assert bench.stage1_kind("qwen3-8b", 512) == "rows" and bench.stage1_kind("large-vocab", 512) == "rows"
+    assert bench.stage1_kind("qwen3-8b", 256) == "tc" and bench.stage1_kind("qwen3-8b-topk", 512) == "tc"
+    assert bench.stage1_kind("qwen3-8b-fp8", 512) == "tc"
+    for workload, B, kind in (("qwen3-8b-mxfp4", 1, "mx"), ("qwen3-8b-mxfp4", 64, "mx"),
+                              ("large-vocab", 512, "rows")):
+        rec = bench.recorded_traffic(workload, B)
+        assert rec is not None and rec["kernel_source_hash"] == bench.kernel_source_hash(kind), (workload, B)
+        assert rec["dram_bytes_per_launch"] == rec["dram_bytes_read"] + rec["dram_bytes_write"]
+    # the three kernels' hashes differ (a record cannot pass for another kernel's)
+    assert len({bench.kernel_source_hash(k) for k in ("tc", "rows", "mx")}) == 3
