@@ -69,6 +69,13 @@ def test_topk_ragged(B, D, V, wide, k):
     full_topk_parity(_ragged(B, D, V, seed=B * 11 + D, wide=wide), k)
 
 
+def test_topk_many_lists_split_stage2():
+    # 160 rows at k = 16 keep one list per tile and quadrant (running lists would not fit in shared
+    # memory), and 313 tiles give 1252 lists a row: more than one Stage-2 CTA takes, so each row is
+    # split over several CTAs whose part lists the final kernel merges
+    full_topk_parity(_ragged(160, 64, 40000, seed=29, wide=False), 16)
+
+
 @pytest.mark.parametrize("wide,k", [(False, 8), (True, 16)])
 def test_topk_plain_launch_greedy_invalid_and_ragged(wide, k):
     # no bias and no mask (the plain epilogue), with greedy, invalid and unseeded rows and a
