@@ -539,7 +539,8 @@ def run_gpu(args):
                   "path": {1: "gemv", 2: "tcgen05"}[path], "tile_v": tv,
                   "l2": "inputs larger than L2 (W is %.2f GB), no flush" % (V * D * (1 if fp8 else 0.53125 if mx else 2) / 1e9)}
         kernel = ("quantize_rows_e4m3_kernel + " if fp8 else "") + \
-            ("lmhead_tc_kernel (top-k epilogue) + stage2_topk_kernel" if topk else
+            ("lmhead_tc_kernel (top-k epilogue) + stage2_topk_row (stage2_topk_part + stage2_topk_final above "
+             "1024 lists a row)" if topk else
              "lmhead_mx_kernel + stage2_kernel" if mx else
              "lmhead_tc_rows_kernel (row groups) + stage2_kernel" if path == 2 and B > 256 else
              "lmhead_tc_kernel + stage2_kernel") + " (one step, CUDA events)"
