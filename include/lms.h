@@ -233,7 +233,8 @@ lms_status lms_lmhead_sample_mxfp4(const void* H, int64_t ldh, const void* Wt, s
  *              4 * n_pad * k * 8 <= 32 KB (n_pad: min(B, 256) rounded up to a multiple of 16),
  *              one per row, Stage-1 CTA and quarter, each the k best keys of those rows over the
  *              CTA's tiles ([B][4 G][k], G = min(ceil(V / 128), SM count)); then, at the next
- *              256-byte boundary, Stage 2's per-row part lists uint64 [B][32][k]
+ *              256-byte boundary, Stage 2's per-row part lists uint64 [B][32][k] (written only when
+ *              a row has more than 1024 lists and is split over several Stage-2 CTAs)
  * Row statuses as for lms_lmhead_sample (1: no finite score, 2: invalid T, 3: a bounded wait ran
  * out).  Requirements as for lms_lmhead_sample; path AUTO or TCGEN05 (bf16 H and W). */
 #define LMS_TOPK_MAX 16
